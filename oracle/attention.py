@@ -1,0 +1,127 @@
+"""Attention-side oracle: exact masked scaled-dot-product attention and its
+gradients in float64.  Test infrastructure only (see ``oracle/__init__.py``).
+
+The method is exact attention computed faster (FlashAttention-2 page,
+«Блочная обработка сохраняет общую нормализацию»: streaming softmax with
+rescaling keeps the normalisation over the whole row and the result is exact
+attention; outputs and gradients differ only by floating-point order).  So the
+oracle is the plain definition, one (batch, head) at a time:
+
+  s_ij = scale * q_i . k_j                    for visible (i, j)
+  lse_i = log sum_j exp(s_ij)                 (natural log; -inf if row i sees nothing)
+  p_ij = exp(s_ij - lse_i)                    (0 for hidden entries, 0 on a row that sees nothing)
+  o_i = sum_j p_ij v_j
+  dV_j = sum_i p_ij dO_i,  dP_ij = dO_i . v_j,  D_i = sum_j p_ij dP_ij
+  dS_ij = p_ij (dP_ij - D_i),  dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i
+
+Tensors are BSHD ([batch][seq][head][d]) float64 arrays holding the bf16
+values exactly; bounds are [4][B][Hm][Skv] (head h uses mask head 0 when
+Hm == 1, else h).  Rows are independent: ``slice_rows`` only bounds the size of
+the dense score block held at once; with it the row sums in dK and dV are
+accumulated one row group after another.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .masks import dense_mask
+
+
+def to64(t) -> np.ndarray:
+    """A torch tensor or array as float64 numpy (exact for bf16 inputs)."""
+    if hasattr(t, "detach"):
+        t = t.detach().to("cpu").float().numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def _mask_vectors(bounds, b, h):
+    bounds = np.asarray(bounds)
+    Hm = bounds.shape[2]
+    hm = 0 if Hm == 1 else h
+    return tuple(bounds[t, b, hm] for t in range(4))
+
+
+def probabilities_head(q, k, mvec, scale, rows=None):
+    """Scores, lse and probabilities for one head; q [Sq][d], k [Skv][d].
+    Returns (p [R][Skv], lse [R]) for the selected rows (default all)."""
+    Sq = q.shape[0]
+    rows = np.arange(Sq) if rows is None else np.asarray(rows)
+    M = dense_mask(*mvec, Sq, rows=rows)
+    s = scale * (q[rows] @ k.T)
+    s = np.where(M, -np.inf, s)
+    m = s.max(axis=1)
+    dead = ~np.isfinite(m)                       # the row sees no key at all
+    m0 = np.where(dead, 0.0, m)
+    with np.errstate(divide="ignore"):
+        lse = np.where(dead, -np.inf, m0 + np.log(np.exp(s - m0[:, None]).sum(axis=1)))
+    p = np.where(dead[:, None], 0.0, np.exp(s - np.where(dead, 0.0, lse)[:, None]))
+    return p, lse
+
+
+def forward_head(q, k, v, mvec, scale, rows=None, slice_rows=None):
+    """O rows and LSE for one head (fully hidden row: o = 0, lse = -inf)."""
+    Sq = q.shape[0]
+    rows = np.arange(Sq) if rows is None else np.asarray(rows)
+    step = len(rows) if not slice_rows else slice_rows
+    o = np.zeros((len(rows), v.shape[1]))
+    lse = np.zeros(len(rows))
+    for a in range(0, len(rows), max(step, 1)):
+        r = rows[a:a + step]
+        p, l = probabilities_head(q, k, mvec, scale, rows=r)
+        o[a:a + len(r)] = p @ v
+        lse[a:a + len(r)] = l
+    return o, lse
+
+
+def backward_head(q, k, v, do, mvec, scale, slice_rows=None):
+    """dQ, dK, dV (and O, LSE, D) for one head, from the definitions above."""
+    Sq, Skv = q.shape[0], k.shape[0]
+    step = Sq if not slice_rows else slice_rows
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    o = np.zeros((Sq, v.shape[1]))
+    lse = np.zeros(Sq)
+    D = np.zeros(Sq)
+    for a in range(0, Sq, max(step, 1)):
+        r = np.arange(a, min(Sq, a + step))
+        p, l = probabilities_head(q, k, mvec, scale, rows=r)
+        o[r] = p @ v
+        lse[r] = l
+        dP = do[r] @ v.T
+        Dr = (p * dP).sum(axis=1)
+        dS = p * (dP - Dr[:, None])
+        dq[r] = scale * (dS @ k)
+        dk += scale * (dS.T @ q[r])
+        dv += p.T @ do[r]
+        D[r] = Dr
+    return dq, dk, dv, o, lse, D
+
+
+def forward(q, k, v, bounds, scale, slice_rows=None):
+    """O [B][Sq][H][d] and LSE [B][H][Sq] for BSHD float64 inputs."""
+    B, Sq, H, d = q.shape
+    o = np.zeros((B, Sq, H, v.shape[3]))
+    lse = np.zeros((B, H, Sq))
+    for b in range(B):
+        for h in range(H):
+            ob, lb = forward_head(q[b, :, h], k[b, :, h], v[b, :, h],
+                                  _mask_vectors(bounds, b, h), scale, slice_rows=slice_rows)
+            o[b, :, h] = ob
+            lse[b, h] = lb
+    return o, lse
+
+
+def backward(q, k, v, do, bounds, scale, slice_rows=None):
+    """(dq, dk, dv, o, lse, D) for BSHD float64 inputs; D is [B][H][Sq]."""
+    B, Sq, H, d = q.shape
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    o = np.zeros((B, Sq, H, v.shape[3]))
+    lse = np.zeros((B, H, Sq))
+    D = np.zeros((B, H, Sq))
+    for b in range(B):
+        for h in range(H):
+            r = backward_head(q[b, :, h], k[b, :, h], v[b, :, h], do[b, :, h],
+                              _mask_vectors(bounds, b, h), scale, slice_rows=slice_rows)
+            dq[b, :, h], dk[b, :, h], dv[b, :, h], o[b, :, h], lse[b, h], D[b, h] = r
+    return dq, dk, dv, o, lse, D
