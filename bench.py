@@ -1,0 +1,358 @@
+"""Benchmark: masked attention forward + backward on one GB300 per rank.
+
+Workload (one step = the whole hot path once): the 32K causal-document
+configuration, B=1, H=32, S=32768, d=128, bf16 Q/K/V/dO ~ N(0,1) seed 0,
+documents U[256, 2048], scale 1/sqrt(d).  A step runs fm_fwd (bound summary,
+tile classification, longest-first order, forward kernel) and fm_bwd (the
+same analysis over k-tiles, D / LSE preprocessing, backward kernel, dQ
+conversion) on inputs already resident in HBM.
+
+Metric: effective fwd+bwd TFLOP/s counting only visible score entries:
+14 * d * N_u per (batch, head), N_u = number of visible (row, key) pairs.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (it is the baseline: there is no other implementation to run).
+Under torchrun every rank runs its own replica of the workload (the heads of
+independent problems; no data-path collective) and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(name="suite_32k/causal_document", B=1, H=32, S=32768, d=128, mask="causal_document")
+METRIC = "effective fwd+bwd TFLOP/s on visible score entries (causal-document mask, 32K, hd128)"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return j, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        sm = [float(r[1]) for r in self.rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            if len(r) >= 9:
+                for n, v in zip(names, r[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _visible_entries(bounds_np, S, H):
+    from oracle import masks as om  # exact integer count of the visible pairs (not timed)
+    return om.visible_count_all(bounds_np, S, H)
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import masked_attention_bound_gb300 as fm
+    from fm_inputs.tensors import mask_bounds, qkv_do
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    W = WORKLOAD
+    B, H, S, d = W["B"], W["H"], W["S"], W["d"]
+    scale = d ** -0.5
+    q, k, v, do = qkv_do(B, S, S, H, d, seed=0, device="cuda")
+    bounds = mask_bounds(W["mask"], B, S, device="cuda")
+    n_vis = _visible_entries(bounds.cpu().numpy(), S, H)
+    flop_fwd, flop_bwd = 4.0 * d * n_vis, 10.0 * d * n_vis
+    flop_step = flop_fwd + flop_bwd
+
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, S, dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    desc = fm.make_desc(q, k, v, o)
+    ws_f = fm.workspace(desc, False)
+    ws_b = fm.workspace(desc, True)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fm.forward(q, k, v, bounds, scale, o=o, lse=lse, ws=ws_f, stream=stream)
+        fm.backward(q, k, v, o, lse, do, bounds, scale, dq=dq, dk=dk, dv=dv, ws=ws_b, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fm.device_status(ws_f) != 0 or fm.device_status(ws_b) != 0:
+        raise RuntimeError("device status not OK after warm-up")
+
+    # ---- timed region: K steps, inputs (1 GiB of Q/K/V/dO) larger than L2
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    fm.profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    fm.profile_enable(False)
+    prof = fm.profile_read()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end through the public API, host buffers, copies timed
+    hq, hk, hv, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
+    hb = bounds.cpu().pin_memory()
+    ho, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, dq, dk, dv))
+    hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    dq_in, dk_in, dv_in, ddo_in = (torch.empty_like(x) for x in (q, k, v, do))
+    db = torch.empty_like(bounds)
+
+    def e2e_step():
+        dq_in.copy_(hq, non_blocking=True)
+        dk_in.copy_(hk, non_blocking=True)
+        dv_in.copy_(hv, non_blocking=True)
+        ddo_in.copy_(hdo, non_blocking=True)
+        db.copy_(hb, non_blocking=True)
+        fm.forward(dq_in, dk_in, dv_in, db, scale, o=o, lse=lse, ws=ws_f, stream=stream)
+        fm.backward(dq_in, dk_in, dv_in, o, lse, ddo_in, db, scale, dq=dq, dk=dk, dv=dv, ws=ws_b,
+                    stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+        hdq.copy_(dq, non_blocking=True)
+        hdk.copy_(dk, non_blocking=True)
+        hdv.copy_(dv, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(1, min(args.steps, 5))
+    ev0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = ev0.elapsed_time(ev1) / e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo, hb))
+    d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdq, hdk, hdv))
+
+    if rank == 0:
+        peaks, peak_src = _peaks()
+        bwd_ms, bwd_n = prof["bwd_kernel"]
+        fwd_ms, fwd_n = prof["fwd_kernel"]
+        bwd_avg = bwd_ms / max(bwd_n, 1)
+        fwd_avg = fwd_ms / max(fwd_n, 1)
+        # the dominant kernel is the one with the larger share of device time
+        dom = "bwd_kernel" if bwd_ms >= fwd_ms else "fwd_kernel"
+        dom_flop = (flop_bwd if dom == "bwd_kernel" else flop_fwd)
+        dom_avg_ms = bwd_avg if dom == "bwd_kernel" else fwd_avg
+        achieved = dom_flop / (dom_avg_ms * 1e-3) / 1e12
+        peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+        value = world * flop_step / (ms * 1e-3) / 1e12
+        launches = sum(n for _, n in prof.values())
+        total_kernel_ms = sum(t for t, _ in prof.values())
+        out = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) Q/K/V/dO, seeded document lengths)",
+            "config": {"workload": W["name"], "B": B, "H": H, "S": S, "d": d, "mask": W["mask"],
+                       "visible_entries_per_rank": n_vis, "l2": "inputs larger than L2 "
+                       "(Q, K, V, dO 256 MiB each); no flush between steps",
+                       "parallelism": f"replicas x{world} (no collective on the data path)"},
+            "fwd_tflops": round(flop_fwd / (fwd_avg * 1e-3) / 1e12, 2),
+            "bwd_tflops": round(flop_bwd / (bwd_avg * 1e-3) / 1e12, 2),
+            "pct_bf16_peak": round(100.0 * value / world / peak, 1),
+            "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2),
+                         "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                         "peak_source": f"bf16_tflops_sustained of {peak_src}",
+                         "traffic": None},
+            "kernel_ms_per_step": {n: round(t / args.steps, 4) for n, (t, c) in prof.items() if c},
+            "kernel_launches_per_step": {n: c // args.steps for n, (t, c) in prof.items() if c},
+            "kernel_time_share": {n: round(t / total_kernel_ms, 4) for n, (t, c) in prof.items() if c},
+            "gpu_launches": launches,
+            "e2e": {"value": round(world * flop_step / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                    "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "clocks": clk,
+        }
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _oracle_sample_inputs(S, d, mask):
+    import numpy as np
+
+    from fm_inputs.tensors import mask_bounds
+    bounds_np = mask_bounds(mask, 1, S).numpy()
+    mvec = tuple(bounds_np[t, 0, 0] for t in range(4))
+    rng = np.random.default_rng(0)
+    q, k, v, do = (rng.standard_normal((S, d)).astype(np.float32).astype(np.float64)
+                   for _ in range(4))
+    return mvec, q, k, v, do
+
+
+def cpu_baseline(seconds: float = 15.0):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload: the
+    backward pass (which recomputes the forward) of the first R query rows of
+    one head, R sized from a 1024-row probe to take about ``seconds``."""
+    import numpy as np
+
+    from oracle import attention as oa
+    from oracle import masks as om
+
+    W = WORKLOAD
+    S, d = W["S"], W["d"]
+    mvec, q, k, v, do = _oracle_sample_inputs(S, d, W["mask"])
+    t0 = time.perf_counter()
+    oa.backward_head(q[:1024], k, v, do[:1024], mvec, d ** -0.5, slice_rows=1024, skip_hidden=True)
+    probe = time.perf_counter() - t0
+    R = int(min(S, max(1024, 1024 * int(seconds / max(probe, 1e-3)))))
+    t0 = time.perf_counter()
+    oa.backward_head(q[:R], k, v, do[:R], mvec, d ** -0.5, slice_rows=1024, skip_hidden=True)
+    el = time.perf_counter() - t0
+    work = int(sum((~om.dense_mask(*mvec, S, rows=np.arange(a, min(R, a + 1024)))).sum()
+                   for a in range(0, R, 1024)))
+    return {"value": round(14.0 * d * work / el / 1e12, 6), "unit": "TFLOP/s",
+            "cores": len(os.sched_getaffinity(0)), "threads": "numpy/BLAS default", "kind": "oracle",
+            "sample": f"fp64 oracle backward (with its forward) of query rows [0, {R}) of one head "
+                      f"of {W['name']}: {work} visible entries in {el:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import numpy as np
+
+    from oracle import attention as oa
+    from oracle import masks as om
+
+    W = WORKLOAD
+    S, d = W["S"], W["d"]
+    mvec, q, k, v, do = _oracle_sample_inputs(S, d, W["mask"])
+    rows = 2048  # one bounded sample per step: the backward of 2048 query rows of one head
+    n_vis = int((~om.dense_mask(*mvec, S, rows=np.arange(rows))).sum())
+
+    def one():
+        oa.backward_head(q[:rows], k, v, do[:rows], mvec, d ** -0.5, slice_rows=1024, skip_hidden=True)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    el = (time.perf_counter() - t0) / args.steps
+    value = 14.0 * d * n_vis / el / 1e12
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"fp64 oracle backward (with its forward) of query rows [0, {rows}) of one head of "
+              f"{W['name']} per step, {n_vis} visible entries")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": W["name"], "B": 1, "H": 1, "S": S, "d": d,
+                                        "mask": W["mask"], "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

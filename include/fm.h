@@ -1,0 +1,170 @@
+/*
+ * fm.h - masked scaled-dot-product attention for GB300 (sm_103a), C ABI.
+ *
+ * The mask is given in the column-wise sparse form of FlashMask (page
+ * "FlashMask-3: ядро внимания с масками для GPU Hopper и распределённого
+ * обучения", introduction and «Ключевые факты»): for every key column j four
+ * int32 bounds along the query axis, LTS[j], LTE[j], UTS[j], UTE[j].  Key j is
+ * hidden from query row i iff  LTS[j] <= i < LTE[j]  or  UTS[j] <= i < UTE[j].
+ * An interval with start >= end hides nothing.  Bound values must lie in
+ * [0, Sq]; other values are reported as FM_ERR_BOUNDS (see fm_device_status).
+ *
+ * The attention is exact (page "FlashAttention-2 ... work partitioning",
+ * «Блочная обработка сохраняет общую нормализацию»): a streaming softmax with
+ * rescaling, results equal to softmax(scale * Q K^T + mask) V up to
+ * floating-point order.  128 x 128 tiles are classified from per-block
+ * min/max of the bounds as empty (skipped), full (no mask arithmetic) or
+ * partial (element-wise mask), the "fewer non-matmul operations" step of the
+ * same page («Три способа повысить загрузку GPU»).
+ *
+ * Conventions for every entry point:
+ *  - Tensors are caller-owned DEVICE pointers.  The library allocates and
+ *    frees nothing; its only scratch is the caller's workspace `ws`.
+ *  - Q, K, V, O, dO, dQ, dK, dV are bf16 in BSHD layout: element (b, s, h, c)
+ *    at  b*stride[0] + s*stride[1] + h*stride[2] + c  (elements; the head
+ *    dimension is contiguous).  Base pointers must be 16-byte aligned and the
+ *    three strides multiples of 8 elements (16 bytes).
+ *  - Bounds are int32 arrays of shape [B][Hm][Skv], contiguous.  Query head h
+ *    reads mask head 0 if Hm == 1, else mask head h.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *    enqueued on it and the call returns without synchronising.  Errors found
+ *    on the host (bad shapes, pointers, workspace size) are returned at once
+ *    and nothing is enqueued.  Errors found on the device (bound values out of
+ *    range, an internal wait that expired) are or-ed into a status word in
+ *    `ws`; read it with fm_device_status().  No device code traps or asserts.
+ *  - No exception or C++ type crosses this interface.
+ */
+#ifndef FM_H_
+#define FM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FM_OK = 0,
+  FM_ERR_INVALID = 1,      /* bad argument: null pointer, shape, stride, alignment, chunk map */
+  FM_ERR_BOUNDS = 2,       /* a bound value outside [0, Sq] (device-detected) */
+  FM_ERR_UNSUPPORTED = 3,  /* valid but not built: head_dim other than 64 or 128 */
+  FM_ERR_WORKSPACE = 4,    /* workspace pointer null/misaligned or smaller than fm_workspace_size */
+  FM_ERR_CUDA = 5,         /* a CUDA runtime call failed */
+  FM_ERR_TIMEOUT = 6       /* a device-side wait expired; outputs are undefined */
+} fm_status;
+
+/* Problem description.  Hm is 1 or H; d (head_dim) is 64 or 128; Sq, Skv >= 1.
+ * Strides are in elements, for the (b, s, h) axes.  For the backward pass
+ * dO uses o_stride, dQ uses q_stride, dK uses k_stride and dV uses v_stride. */
+typedef struct {
+  int B, H, Hm, Sq, Skv, d;
+  int64_t q_stride[3];
+  int64_t k_stride[3];
+  int64_t v_stride[3];
+  int64_t o_stride[3];
+} fm_desc;
+
+/* Byte offsets of the regions inside a workspace (all 256-byte aligned).
+ * nQ = ceil(Sq/128), nK = ceil(Skv/128).  List entries are
+ * (tile_index << 2) | class with class 1 = PARTIAL, 2 = FULL. */
+typedef struct {
+  size_t status;     /* int32[4]: [0] device status bits, [1..3] scheduler counters  */
+  size_t summary;    /* int32 [B][Hm][nK][8]: min/max of LTS, LTE, UTS, UTE per k-block */
+  size_t table;      /* uint8 [B][Hm][nQ][nK]: 0 EMPTY, 1 PARTIAL, 2 FULL           */
+  size_t row_count;  /* int32 [B][Hm][nQ]: non-empty tiles per q-tile row             */
+  size_t row_list;   /* int32 [B][Hm][nQ][nK]: ascending k-tiles of each row          */
+  size_t col_count;  /* int32 [B][Hm][nK]: non-empty tiles per k-tile column          */
+  size_t col_list;   /* int32 [B][Hm][nK][nQ]: ascending q-tiles of each column       */
+  size_t fwd_order;  /* int32 [B*H*nQ]: forward units u=(b*H+h)*nQ+qi, longest first  */
+  size_t bwd_order;  /* int32 [B*H*nK]: backward units u=(b*H+h)*nK+kj, longest first */
+  size_t delta;      /* float [B][H][nQ*128]: D_i = dO_i . O_i, 0 past Sq (backward)  */
+  size_t lse_log2;   /* float [B][H][nQ*128]: LSE_i * log2(e), +inf for rows that see
+                        no key and past Sq (backward only)                          */
+  size_t dq_acc;     /* float [B][H][Sq][d]: fp32 dQ accumulator (backward only)      */
+  size_t total;      /* bytes needed */
+} fm_ws_layout;
+
+/* Workspace bytes needed by fm_fwd (for_bwd = 0) or fm_bwd (for_bwd = 1).
+ * Returns 0 for an invalid description. */
+size_t fm_workspace_size(const fm_desc* desc, int for_bwd);
+
+/* Fill `out` with the region offsets fm_workspace_size() accounts for. */
+fm_status fm_workspace_layout(const fm_desc* desc, int for_bwd, fm_ws_layout* out);
+
+/* Mask analysis into `ws`: validate the bounds (status word), the per-k-block
+ * summary, the tile table, the work lists (rows for for_bwd = 0, columns for
+ * for_bwd = 1) and the longest-first unit order.  fm_fwd and fm_bwd call this
+ * themselves; it is exported so the tables can be inspected. */
+fm_status fm_plan(const fm_desc* desc, const int32_t* lts, const int32_t* lte,
+                  const int32_t* uts, const int32_t* ute, void* ws, size_t ws_bytes,
+                  int for_bwd, void* stream);
+
+/* Forward pass.  q [B][Sq][H][d], k and v [B][Skv][H][d] bf16 (inputs);
+ * o [B][Sq][H][d] bf16 and lse [B][H][Sq] fp32 (outputs, natural log of the
+ * row's softmax normaliser including `scale`).  A query row that sees no key
+ * gets O = 0 and LSE = -inf.  `ws` must hold fm_workspace_size(desc, 0) bytes,
+ * 256-byte aligned.  `scale` multiplies Q K^T (1/sqrt(d) is usual). */
+fm_status fm_fwd(const fm_desc* desc, const void* q, const void* k, const void* v,
+                 const int32_t* lts, const int32_t* lte, const int32_t* uts,
+                 const int32_t* ute, float scale, void* o, float* lse, void* ws,
+                 size_t ws_bytes, void* stream);
+
+/* Backward pass.  Inputs q, k, v, o (bf16), lse (fp32, from fm_fwd with the
+ * same bounds and scale), dout = dO (bf16, o_stride); outputs dq, dk, dv
+ * (bf16).  Gradients of rows that see no key, and of columns no row sees,
+ * are 0.  `ws` must hold fm_workspace_size(desc, 1) bytes. */
+fm_status fm_bwd(const fm_desc* desc, const void* q, const void* k, const void* v,
+                 const void* o, const float* lse, const void* dout, const int32_t* lts,
+                 const int32_t* lte, const int32_t* uts, const int32_t* ute, float scale,
+                 void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
+
+/* Mask localisation ("clip, shift, max" over the bound vectors; FlashMask-3
+ * page, introduction and «Ключевые факты»).  A rank holds the query rows of
+ * n_chunks chunks of the global sequence, chunk c covering global rows
+ * [chunk_start[c], chunk_start[c] + chunk_len[c]), laid out one after the
+ * other in its local query tensor.  Every bound value x becomes
+ *     x' = max over chunks c with chunk_start[c] <= x of
+ *              (offset[c] + min(x - chunk_start[c], chunk_len[c])),   0 if none,
+ * offset[c] = sum of the lengths of the chunks before c: the number of local
+ * rows whose global row is below x.  The key axis is unchanged, so the
+ * rank runs fm_fwd / fm_bwd with Sq = sum(chunk_len), its local Q/dO and the
+ * full K/V.  No data moves between ranks.
+ *   bounds, local_bounds: DEVICE int32 [4][B][Hm][Skv] (LTS, LTE, UTS, UTE
+ *     arrays one after the other); may not overlap.
+ *   chunk_start, chunk_len: HOST int32[n_chunks], in local order, which must
+ *     be ascending in global position and non-overlapping, with positive
+ *     lengths (else FM_ERR_INVALID: the preimage of an interval would not be
+ *     an interval); 1 <= n_chunks <= 128. */
+fm_status fm_localize(const int32_t* bounds, int B, int Hm, int Skv,
+                      const int32_t* chunk_start, const int32_t* chunk_len, int n_chunks,
+                      int32_t* local_bounds, void* stream);
+
+/* Kernel timing, for benchmarks.  While enabled, every kernel the library
+ * launches is bracketed by a pair of CUDA events recorded on its own stream
+ * (event objects are created on first use and reused; no device memory is
+ * allocated).  fm_profile_read() waits for the recorded events, writes per
+ * kernel id the summed device time in milliseconds and the launch count into
+ * total_ms[0..n) and launches[0..n) (either may be NULL), and clears the
+ * record.  Kernel ids: 0 block summary, 1 classify, 2 unit order,
+ * 3 localize, 4 forward, 5 backward preprocess, 6 backward, 7 dQ convert;
+ * fm_kernel_name(id) names them.  At most 65536 launches are recorded per
+ * read; later launches are counted but not timed. */
+fm_status fm_profile_enable(int on);
+fm_status fm_profile_read(double* total_ms, int* launches, int n);
+const char* fm_kernel_name(int id);
+
+/* Synchronise `stream` and read the device status word of `ws`: FM_OK,
+ * FM_ERR_BOUNDS or FM_ERR_TIMEOUT (timeout wins if both are set). */
+fm_status fm_device_status(const void* ws, void* stream);
+
+/* Static description of a status code. */
+const char* fm_status_string(fm_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int fm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FM_H_ */

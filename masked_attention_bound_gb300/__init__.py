@@ -1,0 +1,163 @@
+"""Masked attention in FlashMask's column-wise sparse mask form, for GB300.
+
+Thin Python binding over the C ABI of ``include/fm.h`` (``libfm.so``, built
+from ``csrc/`` for sm_103a).  PyTorch provides device memory and streams; every
+step of the computation runs in the library's CUDA kernels.  If the library is
+missing, every call raises: there is no CPU or PyTorch fallback.
+
+Tensors: q/k/v/o/dO/dq/dk/dv are bf16 CUDA tensors in BSHD layout
+([batch][seq][head][head_dim], head_dim contiguous, other strides multiples of
+8 elements).  ``bounds`` is an int32 CUDA tensor [4][B][Hm][Skv] holding
+LTS, LTE, UTS, UTE; key j is hidden from query row i iff LTS[j] <= i < LTE[j]
+or UTS[j] <= i < UTE[j].
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._abi import FMError, FmDesc, FmWsLayout, check, lib  # noqa: F401
+
+__all__ = ["FMError", "make_desc", "workspace_size", "workspace_layout", "workspace", "plan",
+           "forward", "backward", "localize", "device_status", "lib", "profile_enable",
+           "profile_read"]
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _strides(t):
+    s = t.stride()
+    if s[3] != 1:
+        raise ValueError("head_dim must be the contiguous dimension")
+    return (s[0], s[1], s[2])
+
+
+def make_desc(q, k, v=None, o=None, Hm: int = 1) -> FmDesc:
+    """Problem description from BSHD tensors (v defaults to k's strides, o to q's)."""
+    B, Sq, H, d = q.shape
+    Skv = k.shape[1]
+    D = FmDesc()
+    D.B, D.H, D.Hm, D.Sq, D.Skv, D.d = B, H, Hm, Sq, Skv, d
+    D.q_stride[:] = _strides(q)
+    D.k_stride[:] = _strides(k)
+    D.v_stride[:] = _strides(v if v is not None else k)
+    D.o_stride[:] = _strides(o if o is not None else q)
+    return D
+
+
+def workspace_size(desc: FmDesc, for_bwd: bool) -> int:
+    n = lib().fm_workspace_size(ctypes.byref(desc), int(bool(for_bwd)))
+    if n == 0:
+        raise FMError(1, "fm_workspace_size")
+    return n
+
+
+def workspace_layout(desc: FmDesc, for_bwd: bool) -> FmWsLayout:
+    out = FmWsLayout()
+    check(lib().fm_workspace_layout(ctypes.byref(desc), int(bool(for_bwd)), ctypes.byref(out)),
+          "fm_workspace_layout")
+    return out
+
+
+def workspace(desc: FmDesc, for_bwd: bool, device="cuda") -> torch.Tensor:
+    """A byte tensor large enough (and 256-byte aligned) for the call."""
+    return torch.empty(workspace_size(desc, for_bwd), dtype=torch.uint8, device=device)
+
+
+def _bounds_ptrs(bounds):
+    if bounds.dtype != torch.int32 or not bounds.is_contiguous() or bounds.dim() != 4 \
+            or bounds.shape[0] != 4:
+        raise ValueError("bounds must be a contiguous int32 tensor [4][B][Hm][Skv]")
+    return [ctypes.c_void_p(bounds[t].data_ptr()) for t in range(4)]
+
+
+def plan(q, k, bounds, ws=None, for_bwd=False, stream=None):
+    """Run the mask analysis only; returns (workspace tensor, layout)."""
+    desc = make_desc(q, k, Hm=bounds.shape[2])
+    if ws is None:
+        ws = workspace(desc, for_bwd, q.device)
+    check(lib().fm_plan(ctypes.byref(desc), *_bounds_ptrs(bounds), _p(ws), ws.numel(),
+                        int(bool(for_bwd)), _stream_ptr(stream)), "fm_plan")
+    return ws, workspace_layout(desc, for_bwd)
+
+
+def forward(q, k, v, bounds, scale, o=None, lse=None, ws=None, stream=None):
+    """O [B][Sq][H][d] bf16 and LSE [B][H][Sq] fp32 (natural log)."""
+    B, Sq, H, d = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
+    desc = make_desc(q, k, v, o, Hm=bounds.shape[2])
+    if ws is None:
+        ws = workspace(desc, False, q.device)
+    check(lib().fm_fwd(ctypes.byref(desc), _p(q), _p(k), _p(v), *_bounds_ptrs(bounds),
+                       ctypes.c_float(scale), _p(o), _p(lse), _p(ws), ws.numel(),
+                       _stream_ptr(stream)), "fm_fwd")
+    return o, lse
+
+
+def backward(q, k, v, o, lse, do, bounds, scale, dq=None, dk=None, dv=None, ws=None,
+             stream=None):
+    """dQ, dK, dV (bf16) for the loss whose gradient with respect to O is dO."""
+    if do.stride() != o.stride():
+        do = do.contiguous() if o.is_contiguous() else do
+        if do.stride() != o.stride():
+            raise ValueError("dO must have O's strides")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for a, b_ in ((dq, q), (dk, k), (dv, v)):
+        if a.stride() != b_.stride():
+            raise ValueError("gradient tensors must have the strides of their inputs")
+    desc = make_desc(q, k, v, o, Hm=bounds.shape[2])
+    if ws is None:
+        ws = workspace(desc, True, q.device)
+    check(lib().fm_bwd(ctypes.byref(desc), _p(q), _p(k), _p(v), _p(o), _p(lse), _p(do),
+                       *_bounds_ptrs(bounds), ctypes.c_float(scale), _p(dq), _p(dk), _p(dv),
+                       _p(ws), ws.numel(), _stream_ptr(stream)), "fm_bwd")
+    return dq, dk, dv
+
+
+def localize(bounds, chunks, out=None, stream=None):
+    """Bounds local to a rank holding query chunks ``chunks`` = [(global_start, length), ...]
+    (ascending, non-overlapping), for local-Q x full-KV attention."""
+    if bounds.dtype != torch.int32 or not bounds.is_contiguous() or bounds.shape[0] != 4:
+        raise ValueError("bounds must be a contiguous int32 tensor [4][B][Hm][Skv]")
+    _, B, Hm, Skv = bounds.shape
+    if out is None:
+        out = torch.empty_like(bounds)
+    n = len(chunks)
+    starts = (ctypes.c_int32 * max(n, 1))(*[int(g) for g, _ in chunks])
+    lens = (ctypes.c_int32 * max(n, 1))(*[int(c) for _, c in chunks])
+    check(lib().fm_localize(_p(bounds), B, Hm, Skv, starts, lens, n, _p(out),
+                            _stream_ptr(stream)), "fm_localize")
+    return out
+
+
+def device_status(ws, stream=None) -> int:
+    """Synchronise and return the device status code of a workspace (0 = OK)."""
+    return lib().fm_device_status(_p(ws), _stream_ptr(stream))
+
+
+def profile_enable(on: bool = True):
+    """Bracket every library kernel launch with CUDA events (see fm.h)."""
+    check(lib().fm_profile_enable(int(bool(on))), "fm_profile_enable")
+
+
+def profile_read():
+    """{kernel name: (total device ms, launches)} since the last read; clears."""
+    from ._abi import KERNEL_IDS
+    ms = (ctypes.c_double * KERNEL_IDS)()
+    n = (ctypes.c_int * KERNEL_IDS)()
+    check(lib().fm_profile_read(ms, n, KERNEL_IDS), "fm_profile_read")
+    return {lib().fm_kernel_name(i).decode(): (ms[i], n[i]) for i in range(KERNEL_IDS)}

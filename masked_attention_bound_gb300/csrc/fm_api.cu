@@ -1,0 +1,221 @@
+// The C ABI of include/fm.h: argument validation, workspace layout, and the
+// sequence of launches for each entry point.
+#include <cstring>
+
+#include "fm_internal.h"
+#include "fm_ptx.cuh"
+
+namespace fm {
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+static bool strides_ok(const int64_t* st) {
+  for (int i = 0; i < 3; ++i)
+    if (st[i] <= 0 || (st[i] % 8) != 0 || st[i] >= (int64_t(1) << 36)) return false;
+  return true;
+}
+
+fm_status make_plan(const fm_desc* desc, int for_bwd, Plan* p) {
+  if (!desc || !p) return FM_ERR_INVALID;
+  const fm_desc& D = *desc;
+  if (D.B < 1 || D.H < 1 || D.Sq < 1 || D.Skv < 1 || D.d < 1) return FM_ERR_INVALID;
+  if (D.Hm != 1 && D.Hm != D.H) return FM_ERR_INVALID;
+  if (D.d != 64 && D.d != 128) return FM_ERR_UNSUPPORTED;
+  if (!strides_ok(D.q_stride) || !strides_ok(D.k_stride) || !strides_ok(D.v_stride) ||
+      !strides_ok(D.o_stride))
+    return FM_ERR_INVALID;
+  if (D.Sq > (1 << 24) || D.Skv > (1 << 24)) return FM_ERR_UNSUPPORTED;
+  p->B = D.B; p->H = D.H; p->Hm = D.Hm; p->Sq = D.Sq; p->Skv = D.Skv; p->d = D.d;
+  p->nQ = ceil_div(D.Sq, kTile);
+  p->nK = ceil_div(D.Skv, kTile);
+  const size_t BHm = static_cast<size_t>(D.B) * D.Hm;
+  const size_t BH = static_cast<size_t>(D.B) * D.H;
+  fm_ws_layout& L = p->L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t at = off; off = align256(off + bytes); return at; };
+  L.status = take(16);
+  L.summary = take(BHm * p->nK * 8 * 4);
+  L.table = take(BHm * p->nQ * p->nK);
+  L.row_count = take(BHm * p->nQ * 4);
+  L.row_list = take(BHm * p->nQ * p->nK * 4);
+  L.col_count = take(BHm * p->nK * 4);
+  L.col_list = take(BHm * p->nK * p->nQ * 4);
+  L.fwd_order = take(BH * p->nQ * 4);
+  L.bwd_order = take(BH * p->nK * 4);
+  if (for_bwd) {
+    L.delta = take(BH * p->nQ * kTile * 4);
+    L.lse_log2 = take(BH * p->nQ * kTile * 4);
+    L.dq_acc = take(BH * D.Sq * static_cast<size_t>(D.d) * 4);
+  } else {
+    L.delta = 0;
+    L.lse_log2 = 0;
+    L.dq_acc = 0;
+  }
+  L.total = off;
+  return FM_OK;
+}
+
+static fm_status check_ws(const Plan& p, const void* ws, size_t ws_bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return FM_ERR_WORKSPACE;
+  if (ws_bytes < p.L.total) return FM_ERR_WORKSPACE;
+  return FM_OK;
+}
+
+static bool aligned16(const void* ptr) {
+  return ptr && (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0;
+}
+
+static fm_status run_plan(const Plan& p, const int32_t* lts, const int32_t* lte,
+                          const int32_t* uts, const int32_t* ute, char* ws, int for_bwd,
+                          cudaStream_t s) {
+  if (cudaMemsetAsync(ws + p.L.status, 0, 16, s) != cudaSuccess) return FM_ERR_CUDA;
+  if (launch_summary(p, lts, lte, uts, ute, ws, s) != cudaSuccess) return FM_ERR_CUDA;
+  if (launch_classify(p, ws, for_bwd, s) != cudaSuccess) return FM_ERR_CUDA;
+  if (launch_order(p, ws, for_bwd, s) != cudaSuccess) return FM_ERR_CUDA;
+  return FM_OK;
+}
+
+}  // namespace fm
+
+using namespace fm;
+
+extern "C" {
+
+size_t fm_workspace_size(const fm_desc* desc, int for_bwd) {
+  Plan p;
+  if (make_plan(desc, for_bwd, &p) != FM_OK) return 0;
+  return p.L.total;
+}
+
+fm_status fm_workspace_layout(const fm_desc* desc, int for_bwd, fm_ws_layout* out) {
+  if (!out) return FM_ERR_INVALID;
+  Plan p;
+  fm_status st = make_plan(desc, for_bwd, &p);
+  if (st != FM_OK) return st;
+  *out = p.L;
+  return FM_OK;
+}
+
+fm_status fm_plan(const fm_desc* desc, const int32_t* lts, const int32_t* lte,
+                  const int32_t* uts, const int32_t* ute, void* ws, size_t ws_bytes,
+                  int for_bwd, void* stream) {
+  Plan p;
+  fm_status st = make_plan(desc, for_bwd, &p);
+  if (st != FM_OK) return st;
+  if (!lts || !lte || !uts || !ute) return FM_ERR_INVALID;
+  if ((st = check_ws(p, ws, ws_bytes)) != FM_OK) return st;
+  return run_plan(p, lts, lte, uts, ute, static_cast<char*>(ws), for_bwd,
+                  static_cast<cudaStream_t>(stream));
+}
+
+fm_status fm_fwd(const fm_desc* desc, const void* q, const void* k, const void* v,
+                 const int32_t* lts, const int32_t* lte, const int32_t* uts,
+                 const int32_t* ute, float scale, void* o, float* lse, void* ws,
+                 size_t ws_bytes, void* stream) {
+  Plan p;
+  fm_status st = make_plan(desc, 0, &p);
+  if (st != FM_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !lse) return FM_ERR_INVALID;
+  if (!lts || !lte || !uts || !ute) return FM_ERR_INVALID;
+  if ((st = check_ws(p, ws, ws_bytes)) != FM_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  if ((st = run_plan(p, lts, lte, uts, ute, w, 0, s)) != FM_OK) return st;
+  TensorArgs t{};
+  t.q = q; t.k = k; t.v = v; t.o_out = o; t.lse_out = lse;
+  t.bounds[0] = lts; t.bounds[1] = lte; t.bounds[2] = uts; t.bounds[3] = ute;
+  t.scale = scale;
+  return launch_fwd(p, *desc, t, w, s);
+}
+
+fm_status fm_bwd(const fm_desc* desc, const void* q, const void* k, const void* v,
+                 const void* o, const float* lse, const void* dout, const int32_t* lts,
+                 const int32_t* lte, const int32_t* uts, const int32_t* ute, float scale,
+                 void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+  Plan p;
+  fm_status st = make_plan(desc, 1, &p);
+  if (st != FM_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !lse)
+    return FM_ERR_INVALID;
+  if (!lts || !lte || !uts || !ute) return FM_ERR_INVALID;
+  if ((st = check_ws(p, ws, ws_bytes)) != FM_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  if ((st = run_plan(p, lts, lte, uts, ute, w, 1, s)) != FM_OK) return st;
+  TensorArgs t{};
+  t.q = q; t.k = k; t.v = v; t.o = o; t.dout = dout; t.lse_in = lse;
+  t.dq = dq; t.dk = dk; t.dv = dv;
+  t.bounds[0] = lts; t.bounds[1] = lte; t.bounds[2] = uts; t.bounds[3] = ute;
+  t.scale = scale;
+  return launch_bwd(p, *desc, t, w, s);
+}
+
+fm_status fm_localize(const int32_t* bounds, int B, int Hm, int Skv,
+                      const int32_t* chunk_start, const int32_t* chunk_len, int n_chunks,
+                      int32_t* local_bounds, void* stream) {
+  if (!bounds || !local_bounds || !chunk_start || !chunk_len) return FM_ERR_INVALID;
+  if (B < 1 || Hm < 1 || Skv < 1 || n_chunks < 1 || n_chunks > kMaxChunks) return FM_ERR_INVALID;
+  const long long n = 4LL * B * Hm * Skv;
+  const char* a = reinterpret_cast<const char*>(bounds);
+  const char* b = reinterpret_cast<const char*>(local_bounds);
+  if (a < b + n * 4 && b < a + n * 4) return FM_ERR_INVALID;  // overlapping buffers
+  ChunkMap cm;
+  std::memset(&cm, 0, sizeof(cm));
+  cm.n = n_chunks;
+  long long off = 0, end = -1;
+  for (int c = 0; c < n_chunks; ++c) {
+    const int g = chunk_start[c], L = chunk_len[c];
+    if (g < 0 || L <= 0 || g < end) return FM_ERR_INVALID;
+    end = static_cast<long long>(g) + L;
+    if (off + L > (1LL << 30)) return FM_ERR_INVALID;
+    cm.start[c] = g;
+    cm.len[c] = L;
+    cm.offset[c] = static_cast<int>(off);
+    off += L;
+  }
+  if (launch_localize(bounds, local_bounds, n, cm, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return FM_ERR_CUDA;
+  return FM_OK;
+}
+
+fm_status fm_device_status(const void* ws, void* stream) {
+  if (!ws) return FM_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int word = 0;
+  if (cudaMemcpyAsync(&word, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FM_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FM_ERR_CUDA;
+  if (word & DEV_TIMEOUT) return FM_ERR_TIMEOUT;
+  if (word & DEV_BOUNDS) return FM_ERR_BOUNDS;
+  return FM_OK;
+}
+
+const char* fm_status_string(fm_status s) {
+  switch (s) {
+    case FM_OK: return "ok";
+    case FM_ERR_INVALID: return "invalid argument";
+    case FM_ERR_BOUNDS: return "bound value outside [0, Sq]";
+    case FM_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FM_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case FM_ERR_CUDA: return "CUDA runtime error";
+    case FM_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+int fm_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,612 @@
+// Backward pass of masked attention on sm_103a.
+//
+// Gradients of exact attention by recomputation (FlashAttention-2 page,
+// «Блочная обработка сохраняет общую нормализацию»: the probabilities are
+// rebuilt from the saved row statistics instead of being stored; results
+// match the plain definition up to floating-point order, «...поэтому выходы и
+// градиенты проверяют с допусками»).  With P = exp(scale*S - LSE):
+//   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),  D_i = dO_i . O_i,
+//   dK = scale dS^T Q,  dQ = scale dS K.
+//
+// Three kernels:
+//   bwd_pre_kernel    D_i and LSE_i*log2(e) per query row, padded to whole
+//                     128-row tiles (+inf / 0 past Sq and on rows that see no
+//                     key, so P = 0 there without a branch);
+//   bwd_kernel        one unit = one (batch, head, k-tile): K and V stay in
+//                     smem, the unit walks its column of non-empty q-tiles.
+//                     Warps 0-3: thread r owns key row r (TMEM lane r) for
+//                     S^T, dP^T, dK, dV and query row r for the dQ tile.
+//                     Warp 4: TMA loads.  Warp 5: one thread issues tcgen05:
+//                       S^T = K Q^T, dP^T = V dO^T      (SS, both K-major)
+//                       dV += P^T dO                     (P^T from TMEM, dO MN-major)
+//                       dK += dS^T Q                     (dS^T smem K-major, Q MN-major)
+//                       dQ  = dS K                       (dS smem MN-major, K MN-major)
+//                     dQ tiles are added into an fp32 accumulator with
+//                     vector atomics; dK, dV leave once per unit;
+//   dq_convert_kernel fp32 accumulator -> bf16 dQ.
+// TMEM (512 columns): [0,128) S^T then P^T (packed bf16, 64 columns);
+// [128,256) dP^T then the dQ tile; [256,256+d) dV; [384,384+d) dK.
+#include <cuda_bf16.h>
+
+#include "fm_internal.h"
+#include "fm_ptx.cuh"
+#include "fm_tmap.h"
+
+namespace fm {
+
+// ------------------------------------------------------------------ preprocess
+// One warp per (b, h, row) over nQ*128 padded rows.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
+                                                      const __nv_bfloat16* __restrict__ dout,
+                                                      int64_t os0, int64_t os1, int64_t os2,
+                                                      const float* __restrict__ lse, int B, int H,
+                                                      int Sq, int rows_pad, float* delta,
+                                                      float* lse_log2) {
+  const int lane = threadIdx.x & 31;
+  const long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long total = static_cast<long long>(B) * H * rows_pad;
+  if (w >= total) return;
+  const int i = static_cast<int>(w % rows_pad);
+  const int bh = static_cast<int>(w / rows_pad);
+  const int b = bh / H, h = bh - b * H;
+  float dsum = 0.f;
+  float l2 = INFINITY;
+  if (i < Sq) {
+    const size_t at = static_cast<size_t>(b) * os0 + static_cast<size_t>(i) * os1 +
+                      static_cast<size_t>(h) * os2;
+    constexpr int PER = D / 32;  // elements per lane: 4 (d=128) or 2 (d=64)
+    if constexpr (PER == 4) {
+      const uint2 a = *reinterpret_cast<const uint2*>(o + at + lane * 4);
+      const uint2 g = *reinterpret_cast<const uint2*>(dout + at + lane * 4);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const float2 x = __bfloat1622float2(a2[t]);
+        const float2 y = __bfloat1622float2(g2[t]);
+        dsum = fmaf(x.x, y.x, dsum);
+        dsum = fmaf(x.y, y.y, dsum);
+      }
+    } else {
+      const uint32_t a = *reinterpret_cast<const uint32_t*>(o + at + lane * 2);
+      const uint32_t g = *reinterpret_cast<const uint32_t*>(dout + at + lane * 2);
+      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
+      const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g));
+      dsum = fmaf(x.x, y.x, x.y * y.y);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+    const float L = lse[static_cast<size_t>(bh) * Sq + i];
+    l2 = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
+  }
+  if (lane == 0) {
+    delta[static_cast<size_t>(bh) * rows_pad + i] = dsum;
+    lse_log2[static_cast<size_t>(bh) * rows_pad + i] = l2;
+  }
+}
+
+// ------------------------------------------------------------------ dQ convert
+template <int D>
+__global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* dq, int64_t s0,
+                                  int64_t s1, int64_t s2, int H, int Sq, long long n_vec) {
+  // one thread per 8 consecutive elements of one row
+  for (long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; v < n_vec;
+       v += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long e = v * 8;
+    const int c = static_cast<int>(e % D);
+    const long long row = e / D;  // (b*H + h)*Sq + i
+    const int i = static_cast<int>(row % Sq);
+    const long long bh = row / Sq;
+    const int h = static_cast<int>(bh % H);
+    const int b = static_cast<int>(bh / H);
+    const float4 x = *reinterpret_cast<const float4*>(acc + e);
+    const float4 y = *reinterpret_cast<const float4*>(acc + e + 4);
+    uint4 w;
+    w.x = pack_bf16(x.x, x.y);
+    w.y = pack_bf16(x.z, x.w);
+    w.z = pack_bf16(y.x, y.y);
+    w.w = pack_bf16(y.z, y.w);
+    *reinterpret_cast<uint4*>(dq + b * s0 + static_cast<int64_t>(i) * s1 + h * s2 + c) = w;
+  }
+}
+
+// ------------------------------------------------------------------ main kernel
+template <int D>
+struct BwdCfg {
+  static constexpr int TILE = 128 * D * 2;   // one 128-row bf16 tile
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + TILE;
+  static constexpr int OFF_Q = OFF_V + TILE;          // 2 stages
+  static constexpr int OFF_DO = OFF_Q + 2 * TILE;     // 2 stages
+  static constexpr int OFF_DS = OFF_DO + 2 * TILE;    // 128 x 128 bf16, [key][q]
+  static constexpr int OFF_BAR = OFF_DS + 128 * 128 * 2;
+  static constexpr int NBAR = 20;
+  static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16 + 1024;
+  static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+  static constexpr uint32_t T_A = 0, T_B = 128, T_DV = 256, T_DK = 384, T_COLS = 512;
+};
+
+enum { C_KVFULL = 0, C_KVEMPTY, C_QFULL0, C_QFULL1, C_QEMPTY0, C_QEMPTY1, C_SFULL, C_PREADY,
+       C_DVDONE, C_DPFULL, C_DSREADY, C_DQFULL, C_DQEMPTY, C_ACCFULL, C_ACCEMPTY, C_DRAIN };
+
+struct BwdParams {
+  int B, H, Hm, Sq, Skv, nQ, nK, n_units;
+  float scale, scale_log2;
+  const int32_t* bounds[4];
+  const int32_t* col_count;
+  const int32_t* col_list;
+  const int32_t* order;
+  const float* delta;     // [B][H][nQ*128]
+  const float* lse_log2;  // [B][H][nQ*128]
+  float* dq_acc;          // [B][H][Sq][D]
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int64_t k_stride[3], v_stride[3];
+  int* status;
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    bwd_kernel(const __grid_constant__ BwdParams P, const __grid_constant__ CUtensorMap tmQ,
+               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               const __grid_constant__ CUtensorMap tmDO) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sDS = sbase + C::OFF_DS;
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    mbar_init(bar(C_KVFULL), 1);
+    mbar_init(bar(C_KVEMPTY), 1);
+    mbar_init(bar(C_QFULL0), 1);
+    mbar_init(bar(C_QFULL1), 1);
+    mbar_init(bar(C_QEMPTY0), 1);
+    mbar_init(bar(C_QEMPTY1), 1);
+    mbar_init(bar(C_SFULL), 1);
+    mbar_init(bar(C_PREADY), 128);
+    mbar_init(bar(C_DVDONE), 1);
+    mbar_init(bar(C_DPFULL), 1);
+    mbar_init(bar(C_DSREADY), 128);
+    mbar_init(bar(C_DQFULL), 1);
+    mbar_init(bar(C_DQEMPTY), 128);
+    mbar_init(bar(C_ACCFULL), 1);
+    mbar_init(bar(C_ACCEMPTY), 128);
+    mbar_init(bar(C_DRAIN), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), C::T_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmDO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  auto wait = [&](int b, uint32_t parity) -> bool {
+    if (*abort_flag) return false;
+    if (!mbar_wait(bar(b), parity, P.status)) {
+      *abort_flag = 1;
+      return false;
+    }
+    return true;
+  };
+  // for warps whose 32 lanes all take part: one answer per warp, so the
+  // warp-collective TMEM instructions after it never run diverged
+  auto wait_all = [&](int b, uint32_t parity) -> bool {
+    const bool ok = wait(b, parity);
+    return __all_sync(0xffffffffu, ok);
+  };
+  // unit u = (b*H + h)*nK + kj -> its column of q-tiles
+  auto unit_info = [&](int idx, int& b, int& h, int& kj, const int32_t*& list) {
+    const int u = P.order[idx];
+    const int bh = u / P.nK;
+    kj = u - bh * P.nK;
+    b = bh / P.H;
+    h = bh - b * P.H;
+    const int col = (b * P.Hm + (P.Hm == 1 ? 0 : h)) * P.nK + kj;
+    list = P.col_list + static_cast<size_t>(col) * P.nQ;
+    return P.col_count[col];
+  };
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it = 0, un = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; ok && idx < P.n_units; idx += gridDim.x) {
+        int b, h, kj;
+        const int32_t* list;
+        const int n = unit_info(idx, b, h, kj, list);
+        if (n == 0) continue;
+        if (un > 0 && !wait(C_KVEMPTY, (un - 1) & 1)) break;
+        ++un;
+        mbar_arrive_expect_tx(bar(C_KVFULL), 2 * C::TILE);
+#pragma unroll
+        for (int s = 0; s < D / 64; ++s) {
+          tma_load_4d(sK + s * 16384, &tmK, bar(C_KVFULL), s * 64, h, kj * kTile, b);
+          tma_load_4d(sV + s * 16384, &tmV, bar(C_KVFULL), s * 64, h, kj * kTile, b);
+        }
+        for (int t = 0; t < n; ++t, ++it) {
+          const int qi = list[t] >> 2;
+          const int st = it & 1;
+          const uint32_t use = it >> 1;
+          if (use > 0 && !wait(C_QEMPTY0 + st, (use - 1) & 1)) { ok = false; break; }
+          const uint32_t fb = bar(C_QFULL0 + st);
+          mbar_arrive_expect_tx(fb, 2 * C::TILE);
+          const uint32_t sQ = sbase + C::OFF_Q + st * C::TILE;
+          const uint32_t sDO = sbase + C::OFF_DO + st * C::TILE;
+#pragma unroll
+          for (int s = 0; s < D / 64; ++s) {
+            tma_load_4d(sQ + s * 16384, &tmQ, fb, s * 64, h, qi * kTile, b);
+            tma_load_4d(sDO + s * 16384, &tmDO, fb, s * 64, h, qi * kTile, b);
+          }
+        }
+      }
+      // drain every issued copy before exit
+      for (uint32_t k = (it > 2u ? it - 2u : 0u); k < it; ++k)
+        mbar_wait(bar(C_QFULL0 + (k & 1)), (k >> 1) & 1, P.status);
+      if (un > 0) mbar_wait(bar(C_KVFULL), (un - 1) & 1, P.status);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t idKB = idesc_bf16(128, D, false, true);     // dV, dK (B MN-major)
+      constexpr uint32_t idDQ = idesc_bf16(128, D, true, true);      // dQ (A, B MN-major)
+      uint32_t it = 0, un = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; ok && idx < P.n_units; idx += gridDim.x) {
+        int b, h, kj;
+        const int32_t* list;
+        const int n = unit_info(idx, b, h, kj, list);
+        if (n == 0) continue;
+        if (!wait(C_KVFULL, un & 1)) break;
+        for (int t = 0; t < n; ++t, ++it) {
+          const int st = it & 1;
+          const uint32_t sQ = sbase + C::OFF_Q + st * C::TILE;
+          const uint32_t sDO = sbase + C::OFF_DO + st * C::TILE;
+          if (!wait(C_QFULL0 + st, (it >> 1) & 1)) { ok = false; break; }
+          // region A holds P^T of the previous tile until its dV has run
+          if (it > 0 && !wait(C_DVDONE, (it - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_ss(tbase + C::T_A, sdesc_sw128(sK + koff, 16, 1024),
+                   sdesc_sw128(sQ + koff, 16, 1024), idSS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(C_SFULL));
+          // dV += P^T dO once P^T is in TMEM (and the previous unit's dV/dK were read)
+          if (!wait(C_PREADY, it & 1)) { ok = false; break; }
+          if (t == 0 && un > 0 && !wait(C_ACCEMPTY, (un - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tbase + C::T_DV, tbase + C::T_A + kk * 8,
+                   sdesc_sw128(sDO + kk * 2048, 16384, 1024), idKB, (t > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(C_DVDONE));
+          // dP^T = V dO^T into region B once the previous dQ tile was drained
+          if (it > 0 && !wait(C_DQEMPTY, (it - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_ss(tbase + C::T_B, sdesc_sw128(sV + koff, 16, 1024),
+                   sdesc_sw128(sDO + koff, 16, 1024), idSS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(C_DPFULL));
+          // dK += dS^T Q and dQ = dS K once dS^T is in smem
+          if (!wait(C_DSREADY, it & 1)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_ss(tbase + C::T_DK, sdesc_sw128(sDS + aoff, 16, 1024),
+                   sdesc_sw128(sQ + kk * 2048, 16384, 1024), idKB, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tbase + C::T_B, sdesc_sw128(sDS + kk * 2048, 16384, 1024),
+                   sdesc_sw128(sK + kk * 2048, 16384, 1024), idDQ, kk > 0 ? 1u : 0u);
+          mma_commit(bar(C_DQFULL));
+          mma_commit(bar(C_QEMPTY0 + st));
+        }
+        if (!ok) break;
+        mma_commit(bar(C_KVEMPTY));
+        mma_commit(bar(C_ACCFULL));
+        ++un;
+      }
+      mma_commit(bar(C_DRAIN));
+      mbar_wait(bar(C_DRAIN), 0, P.status);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ compute warps
+    const int r = tid;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int rows_pad = P.nQ * kTile;
+    uint32_t it = 0, un = 0;
+    // dQ tile drain: query row r of the tile whose dQ sits in region B
+    auto drain_dq = [&](uint32_t jt, int b, int h, int qi) -> bool {
+      if (!wait_all(C_DQFULL, jt & 1)) return false;
+      tc_fence_after();
+      const int qrow = qi * kTile + r;
+      float* dst = P.dq_acc + ((static_cast<size_t>(b) * P.H + h) * P.Sq + qrow) * D;
+      uint32_t raw[32];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        tmem_ld32(tbase + lane_off + C::T_B + c * 32, raw);
+        tmem_wait_ld();
+        if (qrow < P.Sq) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float4 v = make_float4(__uint_as_float(raw[4 * i]) * P.scale,
+                                   __uint_as_float(raw[4 * i + 1]) * P.scale,
+                                   __uint_as_float(raw[4 * i + 2]) * P.scale,
+                                   __uint_as_float(raw[4 * i + 3]) * P.scale);
+            atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + 4 * i), v);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C_DQEMPTY));
+      return true;
+    };
+    bool ok = true;
+    for (int idx = blockIdx.x; ok && idx < P.n_units; idx += gridDim.x) {
+      int b, h, kj;
+      const int32_t* list;
+      const int n = unit_info(idx, b, h, kj, list);
+      const int key = kj * kTile + r;
+      __nv_bfloat16* dk_row = P.dk + b * P.k_stride[0] + static_cast<int64_t>(key) * P.k_stride[1] +
+                              h * P.k_stride[2];
+      __nv_bfloat16* dv_row = P.dv + b * P.v_stride[0] + static_cast<int64_t>(key) * P.v_stride[1] +
+                              h * P.v_stride[2];
+      if (n == 0) {
+        if (key < P.Skv) {
+          const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) {
+            reinterpret_cast<uint4*>(dk_row)[c] = z;
+            reinterpret_cast<uint4*>(dv_row)[c] = z;
+          }
+        }
+        continue;
+      }
+      // this thread's key column bounds (beyond Skv: hidden from every row)
+      int lts = 0, lte = 0x7fffffff, uts = 0, ute = 0;
+      if (key < P.Skv) {
+        const size_t at = static_cast<size_t>(b * P.Hm + (P.Hm == 1 ? 0 : h)) * P.Skv + key;
+        lts = __ldg(P.bounds[0] + at);
+        lte = __ldg(P.bounds[1] + at);
+        uts = __ldg(P.bounds[2] + at);
+        ute = __ldg(P.bounds[3] + at);
+      }
+      const bool key_ragged = (kj == P.nK - 1) && (P.Skv & (kTile - 1));
+      const float* lse_bh = P.lse_log2 + (static_cast<size_t>(b) * P.H + h) * rows_pad;
+      const float* del_bh = P.delta + (static_cast<size_t>(b) * P.H + h) * rows_pad;
+      int prev_qi = -1;
+      for (int t = 0; t < n; ++t, ++it) {
+        const int e = list[t];
+        const int qi = e >> 2;
+        const bool partial = ((e & 3) == CLS_PARTIAL) || key_ragged;
+        const float4* l4 = reinterpret_cast<const float4*>(lse_bh + qi * kTile);
+        const float4* d4 = reinterpret_cast<const float4*>(del_bh + qi * kTile);
+        // ---- P^T row = exp2(S^T * scale*log2e - LSE*log2e), masked entries 0
+        if (!wait_all(C_SFULL, it & 1)) { ok = false; break; }
+        tc_fence_after();
+        float p[128];
+        {
+          uint32_t raw[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tbase + lane_off + C::T_A + c * 32, raw);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 L = __ldg(l4 + c * 8 + i);
+              p[c * 32 + 4 * i + 0] = ex2(fmaf(__uint_as_float(raw[4 * i + 0]), P.scale_log2, -L.x));
+              p[c * 32 + 4 * i + 1] = ex2(fmaf(__uint_as_float(raw[4 * i + 1]), P.scale_log2, -L.y));
+              p[c * 32 + 4 * i + 2] = ex2(fmaf(__uint_as_float(raw[4 * i + 2]), P.scale_log2, -L.z));
+              p[c * 32 + 4 * i + 3] = ex2(fmaf(__uint_as_float(raw[4 * i + 3]), P.scale_log2, -L.w));
+            }
+          }
+        }
+        if (partial) {
+          const int q0 = qi * kTile;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int q = q0 + c;
+            const bool hid = (lts <= q && q < lte) || (uts <= q && q < ute);
+            p[c] = hid ? 0.f : p[c];
+          }
+        }
+        {
+          uint32_t pk[32];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(p[half * 64 + 2 * c], p[half * 64 + 2 * c + 1]);
+            tmem_st32(tbase + lane_off + C::T_A + half * 32, pk);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(bar(C_PREADY));
+        // ---- drain the previous tile's dQ (region B) while dV runs
+        if (t > 0 && !drain_dq(it - 1, b, h, prev_qi)) { ok = false; break; }
+        // ---- dS^T row = P^T o (dP^T - D), to smem as bf16 [key][q]
+        if (!wait_all(C_DPFULL, it & 1)) { ok = false; break; }
+        tc_fence_after();
+        {
+          uint32_t raw[32];
+          const uint32_t row_base = sDS + r * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tbase + lane_off + C::T_B + c * 32, raw);
+            tmem_wait_ld();
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 Dv = __ldg(d4 + c * 8 + i);
+              const float s0 = p[c * 32 + 4 * i + 0] * (__uint_as_float(raw[4 * i + 0]) - Dv.x);
+              const float s1 = p[c * 32 + 4 * i + 1] * (__uint_as_float(raw[4 * i + 1]) - Dv.y);
+              const float s2 = p[c * 32 + 4 * i + 2] * (__uint_as_float(raw[4 * i + 2]) - Dv.z);
+              const float s3 = p[c * 32 + 4 * i + 3] * (__uint_as_float(raw[4 * i + 3]) - Dv.w);
+              w[2 * i] = pack_bf16(s0, s1);
+              w[2 * i + 1] = pack_bf16(s2, s3);
+            }
+            // 32 q columns = 4 chunks of 16 B in slab c/2, logical chunks (c&1)*4 .. +3
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t chunk = static_cast<uint32_t>((c & 1) * 4 + j) ^ static_cast<uint32_t>(r & 7);
+              st_shared_v4(row_base + (c >> 1) * 16384 + chunk * 16, w[4 * j], w[4 * j + 1],
+                           w[4 * j + 2], w[4 * j + 3]);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(C_DSREADY));
+        prev_qi = qi;
+      }
+      if (!ok) break;
+      if (!drain_dq(it - 1, b, h, prev_qi)) { ok = false; break; }
+      // ---- epilogue: dV and scale * dK for this key row
+      if (!wait_all(C_ACCFULL, un & 1)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t raw[32];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        tmem_ld32(tbase + lane_off + C::T_DV + c * 32, raw);
+        tmem_wait_ld();
+        if (key < P.Skv) {
+          uint4* dst = reinterpret_cast<uint4*>(dv_row + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pack_bf16(__uint_as_float(raw[8 * i + 0]), __uint_as_float(raw[8 * i + 1])),
+                                pack_bf16(__uint_as_float(raw[8 * i + 2]), __uint_as_float(raw[8 * i + 3])),
+                                pack_bf16(__uint_as_float(raw[8 * i + 4]), __uint_as_float(raw[8 * i + 5])),
+                                pack_bf16(__uint_as_float(raw[8 * i + 6]), __uint_as_float(raw[8 * i + 7])));
+        }
+        tmem_ld32(tbase + lane_off + C::T_DK + c * 32, raw);
+        tmem_wait_ld();
+        if (key < P.Skv) {
+          uint4* dst = reinterpret_cast<uint4*>(dk_row + c * 32);
+          const float sc = P.scale;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pack_bf16(__uint_as_float(raw[8 * i + 0]) * sc, __uint_as_float(raw[8 * i + 1]) * sc),
+                                pack_bf16(__uint_as_float(raw[8 * i + 2]) * sc, __uint_as_float(raw[8 * i + 3]) * sc),
+                                pack_bf16(__uint_as_float(raw[8 * i + 4]) * sc, __uint_as_float(raw[8 * i + 5]) * sc),
+                                pack_bf16(__uint_as_float(raw[8 * i + 6]) * sc, __uint_as_float(raw[8 * i + 7]) * sc));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C_ACCEMPTY));
+      ++un;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::T_COLS);
+  }
+}
+
+template <int D>
+static fm_status launch_bwd_d(const Plan& p, const fm_desc& desc, const TensorArgs& t, char* ws,
+                              cudaStream_t s) {
+  using C = BwdCfg<D>;
+  const int rows_pad = p.nQ * kTile;
+  float* delta = reinterpret_cast<float*>(ws + p.L.delta);
+  float* lse2 = reinterpret_cast<float*>(ws + p.L.lse_log2);
+  float* acc = reinterpret_cast<float*>(ws + p.L.dq_acc);
+  const size_t acc_bytes = static_cast<size_t>(p.B) * p.H * p.Sq * D * 4;
+  if (cudaMemsetAsync(acc, 0, acc_bytes, s) != cudaSuccess) return FM_ERR_CUDA;
+  {
+    const long long warps = static_cast<long long>(p.B) * p.H * rows_pad;
+    const long long blocks = (warps + 7) / 8;
+    prof_begin(K_BWD_PRE, s);
+    bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(t.o), static_cast<const __nv_bfloat16*>(t.dout),
+        desc.o_stride[0], desc.o_stride[1], desc.o_stride[2], t.lse_in, p.B, p.H, p.Sq, rows_pad,
+        delta, lse2);
+    prof_end(K_BWD_PRE, s);
+    if (cudaGetLastError() != cudaSuccess) return FM_ERR_CUDA;
+  }
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tmap_bshd(&tq, t.q, p.B, p.Sq, p.H, D, desc.q_stride, 128) ||
+      !make_tmap_bshd(&tk, t.k, p.B, p.Skv, p.H, D, desc.k_stride, 128) ||
+      !make_tmap_bshd(&tv, t.v, p.B, p.Skv, p.H, D, desc.v_stride, 128) ||
+      !make_tmap_bshd(&tdo, t.dout, p.B, p.Sq, p.H, D, desc.o_stride, 128))
+    return FM_ERR_CUDA;
+  BwdParams P{};
+  P.B = p.B; P.H = p.H; P.Hm = p.Hm; P.Sq = p.Sq; P.Skv = p.Skv; P.nQ = p.nQ; P.nK = p.nK;
+  P.n_units = p.B * p.H * p.nK;
+  P.scale = t.scale;
+  P.scale_log2 = t.scale * 1.4426950408889634f;
+  for (int i = 0; i < 4; ++i) P.bounds[i] = t.bounds[i];
+  P.col_count = reinterpret_cast<const int32_t*>(ws + p.L.col_count);
+  P.col_list = reinterpret_cast<const int32_t*>(ws + p.L.col_list);
+  P.order = reinterpret_cast<const int32_t*>(ws + p.L.bwd_order);
+  P.delta = delta;
+  P.lse_log2 = lse2;
+  P.dq_acc = acc;
+  P.dk = static_cast<__nv_bfloat16*>(t.dk);
+  P.dv = static_cast<__nv_bfloat16*>(t.dv);
+  for (int i = 0; i < 3; ++i) {
+    P.k_stride[i] = desc.k_stride[i];
+    P.v_stride[i] = desc.v_stride[i];
+  }
+  P.status = reinterpret_cast<int*>(ws + p.L.status);
+  auto kern = bwd_kernel<D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+      cudaSuccess)
+    return FM_ERR_CUDA;
+  const int grid = P.n_units < num_sms() ? P.n_units : num_sms();
+  prof_begin(K_BWD, s);
+  kern<<<grid, 192, C::SMEM, s>>>(P, tq, tk, tv, tdo);
+  prof_end(K_BWD, s);
+  if (cudaGetLastError() != cudaSuccess) return FM_ERR_CUDA;
+  {
+    const long long n_vec = static_cast<long long>(p.B) * p.H * p.Sq * (D / 8);
+    const long long want = (n_vec + 255) / 256;
+    const int blocks = static_cast<int>(want < 8192 ? want : 8192);
+    prof_begin(K_DQ_CONVERT, s);
+    dq_convert_kernel<D><<<blocks, 256, 0, s>>>(acc, static_cast<__nv_bfloat16*>(t.dq),
+                                                desc.q_stride[0], desc.q_stride[1],
+                                                desc.q_stride[2], p.H, p.Sq, n_vec);
+    prof_end(K_DQ_CONVERT, s);
+    if (cudaGetLastError() != cudaSuccess) return FM_ERR_CUDA;
+  }
+  return FM_OK;
+}
+
+fm_status launch_bwd(const Plan& p, const fm_desc& desc, const TensorArgs& t, char* ws,
+                     cudaStream_t s) {
+  if (p.d == 64) return launch_bwd_d<64>(p, desc, t, ws, s);
+  if (p.d == 128) return launch_bwd_d<128>(p, desc, t, ws, s);
+  return FM_ERR_UNSUPPORTED;
+}
+
+}  // namespace fm

@@ -1,0 +1,62 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "fm.h"
+
+namespace fm {
+
+constexpr int kTile = 128;            // q-tile and k-tile edge
+constexpr int kMaxChunks = 128;       // fm_localize chunk limit
+
+enum : int { CLS_EMPTY = 0, CLS_PARTIAL = 1, CLS_FULL = 2 };
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+struct Plan {
+  int B, H, Hm, Sq, Skv, d, nQ, nK;
+  fm_ws_layout L;
+};
+
+// Validates the description (shapes and strides) and computes the layout.
+fm_status make_plan(const fm_desc* desc, int for_bwd, Plan* p);
+
+// Mask analysis kernels (fm_mask.cu).
+cudaError_t launch_summary(const Plan& p, const int32_t* lts, const int32_t* lte,
+                           const int32_t* uts, const int32_t* ute, char* ws, cudaStream_t s);
+cudaError_t launch_classify(const Plan& p, char* ws, int for_bwd, cudaStream_t s);
+cudaError_t launch_order(const Plan& p, char* ws, int for_bwd, cudaStream_t s);
+
+struct ChunkMap {
+  int n;
+  int start[kMaxChunks];
+  int len[kMaxChunks];
+  int offset[kMaxChunks];
+};
+cudaError_t launch_localize(const int32_t* in, int32_t* out, long long n_values,
+                            const ChunkMap& cm, cudaStream_t s);
+
+// Attention kernels (fm_fwd.cu, fm_bwd.cu).
+struct TensorArgs {
+  const void* q; const void* k; const void* v; const void* o; const void* dout;
+  void* o_out; float* lse_out; const float* lse_in;
+  void* dq; void* dk; void* dv;
+  const int32_t* bounds[4];
+  float scale;
+};
+fm_status launch_fwd(const Plan& p, const fm_desc& desc, const TensorArgs& t, char* ws,
+                     cudaStream_t s);
+fm_status launch_bwd(const Plan& p, const fm_desc& desc, const TensorArgs& t, char* ws,
+                     cudaStream_t s);
+
+int num_sms();
+
+// Kernel ids for the timing hooks (fm_profile_*).
+enum KernelId : int { K_SUMMARY = 0, K_CLASSIFY, K_ORDER, K_LOCALIZE, K_FWD, K_BWD_PRE, K_BWD,
+                      K_DQ_CONVERT, K_COUNT };
+void prof_begin(int id, cudaStream_t s);
+void prof_end(int id, cudaStream_t s);
+
+}  // namespace fm

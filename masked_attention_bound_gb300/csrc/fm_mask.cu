@@ -1,0 +1,303 @@
+// Mask analysis on the device: per-k-block bound summary, tile classification
+// with compacted work lists, the longest-first unit order, and localisation of
+// the bounds to a rank's query chunks.  All integer work; bit-exact by design.
+#include <climits>
+
+#include "fm_internal.h"
+#include "fm_ptx.cuh"
+
+namespace fm {
+
+// ------------------------------------------------------------------ summary
+// One CTA per (k-block, batch*mask-head); one thread per key column.
+// summary[(bh*nK + kj)*8 + ...] = min/max of LTS, LTE, UTS, UTE over the
+// block's valid columns.  Any bound outside [0, Sq] sets DEV_BOUNDS.
+__global__ void __launch_bounds__(kTile) summary_kernel(const int32_t* __restrict__ lts,
+                                                        const int32_t* __restrict__ lte,
+                                                        const int32_t* __restrict__ uts,
+                                                        const int32_t* __restrict__ ute, int Sq,
+                                                        int Skv, int nK, int32_t* summary,
+                                                        int* status) {
+  const int kj = blockIdx.x, bh = blockIdx.y;
+  const int j = kj * kTile + threadIdx.x;
+  int mn[4], mx[4];
+  if (j < Skv) {
+    const size_t at = static_cast<size_t>(bh) * Skv + j;
+    const int v[4] = {__ldg(lts + at), __ldg(lte + at), __ldg(uts + at), __ldg(ute + at)};
+    bool bad = false;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      mn[t] = mx[t] = v[t];
+      bad |= (v[t] < 0) | (v[t] > Sq);
+    }
+    if (bad) atomicOr(status, DEV_BOUNDS);
+  } else {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      mn[t] = INT_MAX;
+      mx[t] = INT_MIN;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      mn[t] = min(mn[t], __shfl_xor_sync(0xffffffffu, mn[t], off));
+      mx[t] = max(mx[t], __shfl_xor_sync(0xffffffffu, mx[t], off));
+    }
+  }
+  __shared__ int red[kTile / 32][8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      red[warp][2 * t] = mn[t];
+      red[warp][2 * t + 1] = mx[t];
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < 8) {
+    const int t = threadIdx.x;
+    int r = red[0][t];
+    for (int w = 1; w < kTile / 32; ++w) r = (t & 1) ? max(r, red[w][t]) : min(r, red[w][t]);
+    summary[(static_cast<size_t>(bh) * nK + kj) * 8 + t] = r;
+  }
+}
+
+// ------------------------------------------------------------------ classify
+// The tile rule for rows [r0, r1), r1 = min(r0 + 128, Sq), from one k-block's
+// summary s = {minLTS, maxLTS, minLTE, maxLTE, minUTS, maxUTS, minUTE, maxUTE}.
+__device__ __forceinline__ int classify(const int* s, int r0, int r1) {
+  const bool cover_l = (s[1] <= r0) & (s[2] >= r1);
+  const bool cover_u = (s[5] <= r0) & (s[6] >= r1);
+  const bool miss_l = (s[0] >= r1) | (s[3] <= r0);
+  const bool miss_u = (s[4] >= r1) | (s[7] <= r0);
+  return (cover_l | cover_u) ? CLS_EMPTY : ((miss_l & miss_u) ? CLS_FULL : CLS_PARTIAL);
+}
+
+__device__ __forceinline__ void load_summary(const int32_t* p, int* s) {
+  const int4 a = *reinterpret_cast<const int4*>(p);
+  const int4 b = *reinterpret_cast<const int4*>(p + 4);
+  s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w;
+  s[4] = b.x; s[5] = b.y; s[6] = b.z; s[7] = b.w;
+}
+
+// One warp per (bh, q-tile): writes the table row and the ascending list of
+// non-empty k-tiles, compacted with a ballot so the order is preserved.
+__global__ void __launch_bounds__(256) classify_rows_kernel(const int32_t* __restrict__ summary,
+                                                            int nBH, int nQ, int nK, int Sq,
+                                                            uint8_t* table, int32_t* row_count,
+                                                            int32_t* row_list) {
+  const int lane = threadIdx.x & 31;
+  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (w >= nBH * nQ) return;
+  const int bh = w / nQ, qi = w - bh * nQ;
+  const int r0 = qi * kTile, r1 = min(r0 + kTile, Sq);
+  const int32_t* sm = summary + static_cast<size_t>(bh) * nK * 8;
+  uint8_t* tab = table + static_cast<size_t>(w) * nK;
+  int32_t* lst = row_list + static_cast<size_t>(w) * nK;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int cnt = 0;
+  for (int base = 0; base < nK; base += 32) {
+    const int kj = base + lane;
+    int cls = CLS_EMPTY;
+    if (kj < nK) {
+      int s[8];
+      load_summary(sm + kj * 8, s);
+      cls = classify(s, r0, r1);
+      tab[kj] = static_cast<uint8_t>(cls);
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, cls != CLS_EMPTY);
+    if (cls != CLS_EMPTY) lst[cnt + __popc(m & lt_mask)] = (kj << 2) | cls;
+    cnt += __popc(m);
+  }
+  if (lane == 0) row_count[w] = cnt;
+}
+
+// One warp per (bh, k-tile): the ascending list of non-empty q-tiles.
+__global__ void __launch_bounds__(256) classify_cols_kernel(const int32_t* __restrict__ summary,
+                                                            int nBH, int nQ, int nK, int Sq,
+                                                            uint8_t* table, int32_t* col_count,
+                                                            int32_t* col_list) {
+  const int lane = threadIdx.x & 31;
+  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (w >= nBH * nK) return;
+  const int bh = w / nK, kj = w - bh * nK;
+  int s[8];
+  load_summary(summary + static_cast<size_t>(w) * 8, s);
+  int32_t* lst = col_list + static_cast<size_t>(w) * nQ;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int cnt = 0;
+  for (int base = 0; base < nQ; base += 32) {
+    const int qi = base + lane;
+    int cls = CLS_EMPTY;
+    if (qi < nQ) {
+      const int r0 = qi * kTile;
+      cls = classify(s, r0, min(r0 + kTile, Sq));
+      table[(static_cast<size_t>(bh) * nQ + qi) * nK + kj] = static_cast<uint8_t>(cls);
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, cls != CLS_EMPTY);
+    if (cls != CLS_EMPTY) lst[cnt + __popc(m & lt_mask)] = (qi << 2) | cls;
+    cnt += __popc(m);
+  }
+  if (lane == 0) col_count[w] = cnt;
+}
+
+// ------------------------------------------------------------------ order
+// Longest-first order of the units u = (b*H + h)*nT + t by cost
+// counts[b][hm][t] in [0, maxc], ties by u ascending: a counting sort
+// (histogram, scan in descending cost, stable scatter by one warp in u
+// order).  One CTA.
+__global__ void __launch_bounds__(1024) order_kernel(const int32_t* __restrict__ counts, int B,
+                                                     int H, int Hm, int nT, int maxc,
+                                                     int cache_counts, int32_t* order) {
+  extern __shared__ int sh[];
+  int* hist = sh;                 // maxc + 1
+  int* cst = sh + maxc + 1;       // B*Hm*nT (when cached)
+  __shared__ int wsum[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int U = B * H * nT;
+  const int nC = B * Hm * nT;
+  for (int i = tid; i <= maxc; i += blockDim.x) hist[i] = 0;
+  if (cache_counts)
+    for (int i = tid; i < nC; i += blockDim.x) cst[i] = counts[i];
+  __syncthreads();
+  const int* cs = cache_counts ? cst : counts;
+  auto cost = [&](int u) {
+    const int b = u / (H * nT);
+    const int h = (u / nT) % H;
+    const int t = u % nT;
+    return cs[(b * Hm + (Hm == 1 ? 0 : h)) * nT + t];
+  };
+  for (int u = tid; u < U; u += blockDim.x) atomicAdd(&hist[cost(u)], 1);
+  __syncthreads();
+  // exclusive scan over r = maxc - c (descending cost), each thread a segment
+  const int n = maxc + 1;
+  const int seg = (n + blockDim.x - 1) / blockDim.x;
+  const int r_lo = min(n, tid * seg), r_hi = min(n, r_lo + seg);
+  int local = 0;
+  for (int r = r_lo; r < r_hi; ++r) local += hist[maxc - r];
+  int incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int x = (lane < (int)(blockDim.x >> 5)) ? wsum[lane] : 0;
+    int xi = x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, xi, off);
+      if (lane >= off) xi += y;
+    }
+    wsum[lane] = xi - x;  // exclusive prefix of warp totals
+  }
+  __syncthreads();
+  int run = wsum[warp] + incl - local;
+  for (int r = r_lo; r < r_hi; ++r) {
+    const int c = maxc - r;
+    const int h = hist[c];
+    hist[c] = run;
+    run += h;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int u0 = 0; u0 < U; u0 += 32) {
+      const int u = u0 + lane;
+      const bool valid = u < U;
+      const int c = valid ? cost(u) : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, c);
+      int base = 0;
+      if (valid) {
+        base = hist[c];
+        order[base + __popc(peers & lt_mask)] = u;
+      }
+      __syncwarp();
+      if (valid && lane == __ffs(peers) - 1) hist[c] = base + __popc(peers);
+      __syncwarp();
+    }
+  }
+}
+
+// ------------------------------------------------------------------ localize
+__global__ void localize_kernel(const int32_t* __restrict__ in, int32_t* __restrict__ out,
+                                long long n, const __grid_constant__ ChunkMap cm) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int x = in[i];
+    int best = 0;
+    for (int c = 0; c < cm.n; ++c) {
+      if (cm.start[c] <= x) best = max(best, cm.offset[c] + min(x - cm.start[c], cm.len[c]));
+    }
+    out[i] = best;
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_summary(const Plan& p, const int32_t* lts, const int32_t* lte,
+                           const int32_t* uts, const int32_t* ute, char* ws, cudaStream_t s) {
+  dim3 grid(p.nK, p.B * p.Hm);
+  prof_begin(K_SUMMARY, s);
+  summary_kernel<<<grid, kTile, 0, s>>>(lts, lte, uts, ute, p.Sq, p.Skv, p.nK,
+                                        reinterpret_cast<int32_t*>(ws + p.L.summary),
+                                        reinterpret_cast<int*>(ws + p.L.status));
+  prof_end(K_SUMMARY, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_classify(const Plan& p, char* ws, int for_bwd, cudaStream_t s) {
+  const int nBH = p.B * p.Hm;
+  const int32_t* summ = reinterpret_cast<const int32_t*>(ws + p.L.summary);
+  uint8_t* table = reinterpret_cast<uint8_t*>(ws + p.L.table);
+  prof_begin(K_CLASSIFY, s);
+  if (!for_bwd) {
+    const int warps = nBH * p.nQ;
+    classify_rows_kernel<<<ceil_div(warps, 8), 256, 0, s>>>(
+        summ, nBH, p.nQ, p.nK, p.Sq, table, reinterpret_cast<int32_t*>(ws + p.L.row_count),
+        reinterpret_cast<int32_t*>(ws + p.L.row_list));
+  } else {
+    const int warps = nBH * p.nK;
+    classify_cols_kernel<<<ceil_div(warps, 8), 256, 0, s>>>(
+        summ, nBH, p.nQ, p.nK, p.Sq, table, reinterpret_cast<int32_t*>(ws + p.L.col_count),
+        reinterpret_cast<int32_t*>(ws + p.L.col_list));
+  }
+  prof_end(K_CLASSIFY, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_order(const Plan& p, char* ws, int for_bwd, cudaStream_t s) {
+  const int nT = for_bwd ? p.nK : p.nQ;      // units per (b, h)
+  const int maxc = for_bwd ? p.nQ : p.nK;    // largest possible cost
+  const int32_t* counts =
+      reinterpret_cast<const int32_t*>(ws + (for_bwd ? p.L.col_count : p.L.row_count));
+  int32_t* order = reinterpret_cast<int32_t*>(ws + (for_bwd ? p.L.bwd_order : p.L.fwd_order));
+  const size_t hist_bytes = static_cast<size_t>(maxc + 1) * 4;
+  const size_t cache_bytes = static_cast<size_t>(p.B) * p.Hm * nT * 4;
+  const size_t limit = 200 * 1024;
+  if (hist_bytes > limit) return cudaErrorInvalidValue;
+  const int cache = hist_bytes + cache_bytes <= limit ? 1 : 0;
+  const size_t smem = hist_bytes + (cache ? cache_bytes : 0);
+  cudaError_t e = cudaFuncSetAttribute(order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(limit));
+  if (e != cudaSuccess) return e;
+  prof_begin(K_ORDER, s);
+  order_kernel<<<1, 1024, smem, s>>>(counts, p.B, p.H, p.Hm, nT, maxc, cache, order);
+  prof_end(K_ORDER, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_localize(const int32_t* in, int32_t* out, long long n_values,
+                            const ChunkMap& cm, cudaStream_t s) {
+  const long long want = (n_values + 255) / 256;
+  const int grid = static_cast<int>(want < 4096 ? (want < 1 ? 1 : want) : 4096);
+  prof_begin(K_LOCALIZE, s);
+  localize_kernel<<<grid, 256, 0, s>>>(in, out, n_values, cm);
+  prof_end(K_LOCALIZE, s);
+  return cudaGetLastError();
+}
+
+}  // namespace fm

@@ -1,0 +1,94 @@
+// Timing hooks: CUDA events around each kernel launch while enabled.
+#include <vector>
+
+#include "fm_internal.h"
+
+namespace fm {
+
+namespace {
+struct Rec {
+  int id;
+  cudaEvent_t a, b;
+};
+constexpr int kMaxRecs = 65536;
+bool g_on = false;
+std::vector<cudaEvent_t> g_pool;  // events reused across reads
+size_t g_pool_used = 0;
+std::vector<Rec> g_recs;
+int g_counts[K_COUNT] = {0};
+int g_open = -1;  // index of the record waiting for its end event
+
+cudaEvent_t take_event() {
+  if (g_pool_used == g_pool.size()) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    g_pool.push_back(e);
+  }
+  return g_pool[g_pool_used++];
+}
+}  // namespace
+
+void prof_begin(int id, cudaStream_t s) {
+  g_open = -1;
+  if (!g_on) return;
+  g_counts[id] += 1;
+  if (static_cast<int>(g_recs.size()) >= kMaxRecs) return;
+  cudaEvent_t a = take_event(), b = take_event();
+  if (!a || !b) return;
+  cudaEventRecord(a, s);
+  g_recs.push_back({id, a, b});
+  g_open = static_cast<int>(g_recs.size()) - 1;
+}
+
+void prof_end(int id, cudaStream_t s) {
+  if (!g_on || g_open < 0 || g_recs[g_open].id != id) return;
+  cudaEventRecord(g_recs[g_open].b, s);
+  g_open = -1;
+}
+
+}  // namespace fm
+
+using namespace fm;
+
+extern "C" {
+
+fm_status fm_profile_enable(int on) {
+  g_on = on != 0;
+  return FM_OK;
+}
+
+fm_status fm_profile_read(double* total_ms, int* launches, int n) {
+  if (n < 0) return FM_ERR_INVALID;
+  double ms[K_COUNT] = {0};
+  fm_status st = FM_OK;
+  for (const Rec& r : g_recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) {
+      st = FM_ERR_CUDA;
+      continue;
+    }
+    ms[r.id] += t;
+  }
+  for (int i = 0; i < n && i < K_COUNT; ++i) {
+    if (total_ms) total_ms[i] = ms[i];
+    if (launches) launches[i] = g_counts[i];
+  }
+  for (int i = K_COUNT; i < n; ++i) {
+    if (total_ms) total_ms[i] = 0;
+    if (launches) launches[i] = 0;
+  }
+  g_recs.clear();
+  g_pool_used = 0;
+  g_open = -1;
+  for (int i = 0; i < K_COUNT; ++i) g_counts[i] = 0;
+  return st;
+}
+
+const char* fm_kernel_name(int id) {
+  static const char* names[K_COUNT] = {"summary_kernel", "classify_kernel", "order_kernel",
+                                       "localize_kernel", "fwd_kernel", "bwd_pre_kernel",
+                                       "bwd_kernel", "dq_convert_kernel"};
+  return (id >= 0 && id < K_COUNT) ? names[id] : "unknown";
+}
+
+}  // extern "C"

@@ -41,13 +41,35 @@ def _mask_vectors(bounds, b, h):
     return tuple(bounds[t, b, hm] for t in range(4))
 
 
-def probabilities_head(q, k, mvec, scale, rows=None):
+def columns_seen(mvec, r0: int, r1: int) -> np.ndarray:
+    """Indices of the key columns that at least one query row of [r0, r1)
+    sees.  A column is dropped only when its two hidden intervals together
+    cover all of [r0, r1); such a column contributes exactly zero to every
+    sum of the definition for those rows, so leaving it out changes nothing."""
+    lts, lte, uts, ute = (np.asarray(x, dtype=np.int64) for x in mvec)
+    if r0 >= r1:
+        return np.zeros(0, dtype=np.int64)
+    a_cov = (lts <= r0) & (lte >= r1)
+    b_cov = (uts <= r0) & (ute >= r1)
+    a_ne = lts < lte
+    b_ne = uts < ute
+    touch = a_ne & b_ne & (np.maximum(lts, uts) <= np.minimum(lte, ute))
+    union_cov = touch & (np.minimum(lts, uts) <= r0) & (np.maximum(lte, ute) >= r1)
+    return np.nonzero(~(a_cov | b_cov | union_cov))[0]
+
+
+def probabilities_head(q, k, mvec, scale, rows=None, cols=None):
     """Scores, lse and probabilities for one head; q [Sq][d], k [Skv][d].
-    Returns (p [R][Skv], lse [R]) for the selected rows (default all)."""
+    Returns (p [R][len(cols)], lse [R]) for the selected rows (default all)
+    over the selected key columns (default all; pass ``columns_seen`` to skip
+    columns the rows cannot see)."""
     Sq = q.shape[0]
     rows = np.arange(Sq) if rows is None else np.asarray(rows)
-    M = dense_mask(*mvec, Sq, rows=rows)
-    s = scale * (q[rows] @ k.T)
+    cols = np.arange(k.shape[0]) if cols is None else np.asarray(cols)
+    if len(cols) == 0:                           # no row of the group sees any key
+        return np.zeros((len(rows), 0)), np.full(len(rows), -np.inf)
+    M = dense_mask(*(np.asarray(x)[cols] for x in mvec), Sq, rows=rows)
+    s = scale * (q[rows] @ k[cols].T)
     s = np.where(M, -np.inf, s)
     m = s.max(axis=1)
     dead = ~np.isfinite(m)                       # the row sees no key at all
@@ -58,8 +80,9 @@ def probabilities_head(q, k, mvec, scale, rows=None):
     return p, lse
 
 
-def forward_head(q, k, v, mvec, scale, rows=None, slice_rows=None):
-    """O rows and LSE for one head (fully hidden row: o = 0, lse = -inf)."""
+def forward_head(q, k, v, mvec, scale, rows=None, slice_rows=None, skip_hidden=False):
+    """O rows and LSE for one head (fully hidden row: o = 0, lse = -inf).
+    With ``skip_hidden`` each row group only touches ``columns_seen``."""
     Sq = q.shape[0]
     rows = np.arange(Sq) if rows is None else np.asarray(rows)
     step = len(rows) if not slice_rows else slice_rows
@@ -67,14 +90,16 @@ def forward_head(q, k, v, mvec, scale, rows=None, slice_rows=None):
     lse = np.zeros(len(rows))
     for a in range(0, len(rows), max(step, 1)):
         r = rows[a:a + step]
-        p, l = probabilities_head(q, k, mvec, scale, rows=r)
-        o[a:a + len(r)] = p @ v
+        cols = columns_seen(mvec, int(r.min()), int(r.max()) + 1) if skip_hidden and len(r) else None
+        p, l = probabilities_head(q, k, mvec, scale, rows=r, cols=cols)
+        o[a:a + len(r)] = p @ (v if cols is None else v[cols])
         lse[a:a + len(r)] = l
     return o, lse
 
 
-def backward_head(q, k, v, do, mvec, scale, slice_rows=None):
-    """dQ, dK, dV (and O, LSE, D) for one head, from the definitions above."""
+def backward_head(q, k, v, do, mvec, scale, slice_rows=None, skip_hidden=False):
+    """dQ, dK, dV (and O, LSE, D) for one head, from the definitions above.
+    With ``skip_hidden`` each row group only touches ``columns_seen``."""
     Sq, Skv = q.shape[0], k.shape[0]
     step = Sq if not slice_rows else slice_rows
     dq = np.zeros_like(q)
@@ -85,15 +110,17 @@ def backward_head(q, k, v, do, mvec, scale, slice_rows=None):
     D = np.zeros(Sq)
     for a in range(0, Sq, max(step, 1)):
         r = np.arange(a, min(Sq, a + step))
-        p, l = probabilities_head(q, k, mvec, scale, rows=r)
-        o[r] = p @ v
+        cols = columns_seen(mvec, a, int(r[-1]) + 1) if skip_hidden else np.arange(Skv)
+        kc, vc = k[cols], v[cols]
+        p, l = probabilities_head(q, k, mvec, scale, rows=r, cols=cols)
+        o[r] = p @ vc
         lse[r] = l
-        dP = do[r] @ v.T
+        dP = do[r] @ vc.T
         Dr = (p * dP).sum(axis=1)
         dS = p * (dP - Dr[:, None])
-        dq[r] = scale * (dS @ k)
-        dk += scale * (dS.T @ q[r])
-        dv += p.T @ do[r]
+        dq[r] = scale * (dS @ kc)
+        dk[cols] += scale * (dS.T @ q[r])
+        dv[cols] += p.T @ do[r]
         D[r] = Dr
     return dq, dk, dv, o, lse, D
 

@@ -1,0 +1,150 @@
+"""Backward parity: fm_bwd through the binding against the fp64 oracle (GPU).
+
+Gradients are compared in full for the sampled (batch, head) pairs:
+max |G - G_ref| <= 2e-2 * max |G_ref| for G in dQ, dK, dV.
+"""
+import numpy as np
+import pytest
+import torch
+
+import masked_attention_bound_gb300 as fm
+from fm_inputs import masks as gen
+from fm_inputs.configs import (LOCALIZE_64K, LOCALIZE_RANKS, LONG_128K, SUITE_32K, SWEEP_4K, TINY,
+                               TINY_DOCS, dual_chunk_map)
+from fm_inputs.tensors import bounds_tensor, mask_bounds, qkv_do
+from parity import GRAD_REL, O_TOL, compare_bwd, compare_fwd
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(q, k, v, do, bounds, scale):
+    o, lse = fm.forward(q, k, v, bounds, scale)
+    dq, dk, dv = fm.backward(q, k, v, o, lse, do, bounds, scale)
+    torch.cuda.synchronize()
+    return o, lse, dq, dk, dv
+
+
+def test_tiny_config():
+    q, k, v, do = qkv_do(TINY.B, TINY.S, TINY.S, TINY.H, TINY.d, device="cuda")
+    bounds = bounds_tensor([[gen.causal_document(TINY.S, TINY_DOCS)]], device="cuda")
+    o, lse, dq, dk, dv = _run(q, k, v, do, bounds, TINY.scale)
+    compare_fwd(q, k, v, bounds, TINY.scale, o, lse)
+    compare_bwd(q, k, v, do, bounds, TINY.scale, dq, dk, dv)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("S", [1, 77, 128, 300, 1000])
+@pytest.mark.parametrize("name", ["full", "causal", "causal_document", "qk_sparse",
+                                  "share_question", "random_eviction", "global_sliding"])
+def test_small_shapes(name, S, d):
+    B, H = 2, 2
+    q, k, v, do = qkv_do(B, S, S, H, d, seed=S + 1, device="cuda")
+    bl = [gen.make_mask(name, S, seed=b, window=max(1, S // 5), n_global=min(7, S)) for b in range(B)]
+    bounds = bounds_tensor([[x] for x in bl], device="cuda")
+    o, lse, dq, dk, dv = _run(q, k, v, do, bounds, d ** -0.5)
+    compare_bwd(q, k, v, do, bounds, d ** -0.5, dq, dk, dv)
+
+
+def test_fully_masked_rows_and_columns_are_zero():
+    S, H, d = 512, 2, 128
+    q, k, v, do = qkv_do(1, S, S, H, d, device="cuda")
+    bounds = bounds_tensor([[gen.qk_sparse(S)]], device="cuda")
+    o, lse, dq, dk, dv = _run(q, k, v, do, bounds, d ** -0.5)
+    qs, qe, ks, ke = gen.qk_sparse_ranges(S)
+    assert torch.all(dq[:, qs:qe] == 0)
+    assert torch.all(dk[:, ks:ke] == 0) and torch.all(dv[:, ks:ke] == 0)
+    assert torch.all(torch.isneginf(lse[:, :, qs:qe]))
+    compare_bwd(q, k, v, do, bounds, d ** -0.5, dq, dk, dv)
+
+
+def test_per_head_masks_strides_and_cross_lengths():
+    B, Sq, Skv, H, d = 2, 384, 640, 3, 128
+    base_q = torch.randn(B, Sq, H, 2 * d, device="cuda").bfloat16()
+    base_kv = torch.randn(B, Skv, H, 2 * d, device="cuda").bfloat16()
+    q = base_q[..., :d]
+    do = base_q[..., d:]
+    k, v = base_kv[..., :d], base_kv[..., d:]
+    rng = np.random.default_rng(3)
+    per_b = []
+    for b in range(B):
+        heads = []
+        for h in range(H):
+            a = rng.integers(0, Sq + 1, size=(4, Skv))
+            heads.append((np.minimum(a[0], a[1]), np.maximum(a[0], a[1]),
+                          np.minimum(a[2], a[3]), np.maximum(a[2], a[3])))
+        per_b.append(heads)
+    bounds = bounds_tensor(per_b, device="cuda")
+    o = torch.empty(B, Sq, H, 2 * d, device="cuda", dtype=torch.bfloat16)[..., :d]
+    o, lse = fm.forward(q, k, v, bounds, 0.1, o=o)
+    dq = torch.empty(B, Sq, H, 2 * d, device="cuda", dtype=torch.bfloat16)[..., d:]
+    dk = torch.empty(B, Skv, H, 2 * d, device="cuda", dtype=torch.bfloat16)[..., :d]
+    dv = torch.empty(B, Skv, H, 2 * d, device="cuda", dtype=torch.bfloat16)[..., d:]
+    do_o = torch.empty_like(o)
+    do_o.copy_(do)  # dO must have O's strides
+    fm.backward(q, k, v, o, lse, do_o, bounds, 0.1, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    compare_fwd(q, k, v, bounds, 0.1, o, lse)
+    compare_bwd(q, k, v, do, bounds, 0.1, dq, dk, dv)
+
+
+@pytest.mark.parametrize("name", SWEEP_4K.masks)
+def test_sweep_4k_sampled_heads(name):
+    W = SWEEP_4K
+    q, k, v, do = qkv_do(W.B, W.S, W.S, W.H, W.d, device="cuda")
+    bounds = mask_bounds(name, W.B, W.S, device="cuda")
+    o, lse, dq, dk, dv = _run(q, k, v, do, bounds, W.scale)
+    compare_bwd(q, k, v, do, bounds, W.scale, dq, dk, dv, heads=[(0, 0), (3, 15)])
+
+
+@pytest.mark.parametrize("name", ["causal_document", "share_question", "qk_sparse", "global_sliding"])
+def test_suite_32k_sampled_head(name):
+    W = SUITE_32K
+    q, k, v, do = qkv_do(W.B, W.S, W.S, W.H, W.d, device="cuda")
+    bounds = mask_bounds(name, W.B, W.S, device="cuda")
+    o, lse, dq, dk, dv = _run(q, k, v, do, bounds, W.scale)
+    compare_bwd(q, k, v, do, bounds, W.scale, dq, dk, dv, heads=[(0, 5)])
+
+
+def test_long_128k_sampled_head():
+    W = LONG_128K
+    q, k, v, do = qkv_do(W.B, W.S, W.S, W.H, W.d, device="cuda")
+    bounds = mask_bounds("causal_document_window", W.B, W.S, device="cuda", window=8192)
+    o, lse, dq, dk, dv = _run(q, k, v, do, bounds, W.scale)
+    compare_fwd(q, k, v, bounds, W.scale, o, lse, heads=[(0, 3)], rows=64)
+    compare_bwd(q, k, v, do, bounds, W.scale, dq, dk, dv, heads=[(0, 3)])
+
+
+def test_localized_ranks_match_global_run():
+    """Localisation end to end: per simulated rank, localise the bounds and run
+    local-Q x full-KV forward and backward; the concatenated O, LSE, dQ and the
+    rank sums of dK, dV match the global run (and the global run matches the
+    oracle on a sampled head)."""
+    W = LOCALIZE_64K
+    q, k, v, do = qkv_do(W.B, W.S, W.S, W.H, W.d, device="cuda")
+    bounds = mask_bounds("causal_document", W.B, W.S, device="cuda")
+    o, lse, dq, dk, dv = _run(q, k, v, do, bounds, W.scale)
+    o_l = torch.zeros_like(o)
+    lse_l = torch.zeros_like(lse)
+    dq_l = torch.zeros_like(dq)
+    dk_sum = torch.zeros(dk.shape, dtype=torch.float32, device="cuda")
+    dv_sum = torch.zeros(dv.shape, dtype=torch.float32, device="cuda")
+    for chunks in dual_chunk_map(W.S, LOCALIZE_RANKS):
+        rows = torch.cat([torch.arange(g, g + c, device="cuda") for g, c in chunks])
+        lb = fm.localize(bounds, chunks)
+        ql, dol = q[:, rows].contiguous(), do[:, rows].contiguous()
+        ol, lsel = fm.forward(ql, k, v, lb, W.scale)
+        dql, dkl, dvl = fm.backward(ql, k, v, ol, lsel, dol, lb, W.scale)
+        o_l[:, rows] = ol
+        lse_l[:, :, rows] = lsel
+        dq_l[:, rows] = dql
+        dk_sum += dkl.float()
+        dv_sum += dvl.float()
+    torch.cuda.synchronize()
+    assert (o_l.float() - o.float()).abs().max().item() <= O_TOL
+    fin = torch.isfinite(lse)
+    assert torch.equal(fin, torch.isfinite(lse_l))
+    assert (lse_l[fin] - lse[fin]).abs().max().item() <= 1e-3
+    for got, ref in ((dq_l.float(), dq.float()), (dk_sum, dk.float()), (dv_sum, dv.float())):
+        assert (got - ref).abs().max().item() <= GRAD_REL * ref.abs().max().item()
+    compare_fwd(q, k, v, bounds, W.scale, o, lse, heads=[(0, 9)], rows=64)
+    compare_bwd(q, k, v, do, bounds, W.scale, dq, dk, dv, heads=[(0, 9)])

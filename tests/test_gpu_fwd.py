@@ -1,0 +1,110 @@
+"""Forward parity: the CUDA path (fm_fwd through the binding) against the fp64
+oracle on the same seeded inputs (GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import masked_attention_bound_gb300 as fm
+from fm_inputs import masks as gen
+from fm_inputs.configs import LONG_128K, SUITE_32K, SWEEP_4K, TINY, TINY_DOCS
+from fm_inputs.tensors import bounds_tensor, mask_bounds, qkv_do
+from parity import compare_fwd
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(B, S, H, d, seed=0, Skv=None):
+    q, k, v, do = qkv_do(B, S, S if Skv is None else Skv, H, d, seed=seed, device="cuda")
+    return q, k, v, do
+
+
+def test_tiny_config():
+    q, k, v, _ = _inputs(TINY.B, TINY.S, TINY.H, TINY.d)
+    bounds = bounds_tensor([[gen.causal_document(TINY.S, TINY_DOCS)]], device="cuda")
+    o, lse = fm.forward(q, k, v, bounds, TINY.scale)
+    torch.cuda.synchronize()
+    compare_fwd(q, k, v, bounds, TINY.scale, o, lse)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("S", [1, 77, 128, 300, 1000])
+@pytest.mark.parametrize("name", ["full", "causal", "causal_document", "qk_sparse",
+                                  "share_question", "random_eviction", "global_sliding"])
+def test_small_shapes(name, S, d):
+    B, H = 2, 2
+    q, k, v, _ = _inputs(B, S, H, d, seed=S)
+    bl = [gen.make_mask(name, S, seed=b, window=max(1, S // 5), n_global=min(7, S)) for b in range(B)]
+    bounds = bounds_tensor([[x] for x in bl], device="cuda")
+    o, lse = fm.forward(q, k, v, bounds, d ** -0.5)
+    torch.cuda.synchronize()
+    compare_fwd(q, k, v, bounds, d ** -0.5, o, lse)
+
+
+def test_per_head_masks_and_strides():
+    """Hm = H, and Q/K/V/O as non-contiguous views (head-dim still contiguous)."""
+    B, S, H, d = 2, 640, 3, 128
+    base = torch.randn(B, S, H, 3 * d, device="cuda").bfloat16()
+    q, k, v = base[..., :d], base[..., d:2 * d], base[..., 2 * d:]
+    per_b = [[gen.make_mask(n, S, seed=b) for n in ("causal", "share_question", "prefix_document")]
+             for b in range(B)]
+    bounds = bounds_tensor(per_b, device="cuda")
+    o_big = torch.zeros(B, S, H, 2 * d, device="cuda", dtype=torch.bfloat16)
+    o = o_big[..., d:]
+    fm.forward(q, k, v, bounds, 0.1, o=o)
+    lse = torch.empty(B, H, S, device="cuda")
+    fm.forward(q, k, v, bounds, 0.1, o=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(o_big[..., :d] == 0)
+    compare_fwd(q, k, v, bounds, 0.1, o, lse)
+
+
+def test_cross_lengths():
+    Sq, Skv, H, d = 300, 777, 2, 64
+    q, k, v, _ = _inputs(1, Sq, H, d, Skv=Skv)
+    rng = np.random.default_rng(2)
+    a = rng.integers(0, Sq + 1, size=(4, Skv))
+    b = (np.minimum(a[0], a[1]), np.maximum(a[0], a[1]), np.minimum(a[2], a[3]), np.maximum(a[2], a[3]))
+    bounds = bounds_tensor([[b]], device="cuda")
+    o, lse = fm.forward(q, k, v, bounds, 0.125)
+    torch.cuda.synchronize()
+    compare_fwd(q, k, v, bounds, 0.125, o, lse)
+
+
+def test_repeatable():
+    """Same inputs, same schedule: the forward output is bit-identical."""
+    q, k, v, _ = _inputs(1, 2048, 4, 128)
+    bounds = mask_bounds("causal_document", 1, 2048, device="cuda")
+    o1, l1 = fm.forward(q, k, v, bounds, 0.09)
+    o2, l2 = fm.forward(q, k, v, bounds, 0.09)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("name", SWEEP_4K.masks)
+def test_sweep_4k_sampled(name):
+    W = SWEEP_4K
+    q, k, v, _ = _inputs(W.B, W.S, W.H, W.d)
+    bounds = mask_bounds(name, W.B, W.S, device="cuda")
+    o, lse = fm.forward(q, k, v, bounds, W.scale)
+    torch.cuda.synchronize()
+    heads = [(b, h) for b in range(W.B) for h in range(W.H)]
+    compare_fwd(q, k, v, bounds, W.scale, o, lse, heads=heads[::7], rows=192)
+
+
+@pytest.mark.parametrize("name", SUITE_32K.masks)
+def test_suite_32k_sampled(name):
+    W = SUITE_32K
+    q, k, v, _ = _inputs(W.B, W.S, W.H, W.d)
+    bounds = mask_bounds(name, W.B, W.S, device="cuda")
+    o, lse = fm.forward(q, k, v, bounds, W.scale)
+    torch.cuda.synchronize()
+    compare_fwd(q, k, v, bounds, W.scale, o, lse, heads=[(0, 0), (0, 13), (0, 31)], rows=96)
+
+
+def test_long_128k_sampled():
+    W = LONG_128K
+    q, k, v, _ = _inputs(W.B, W.S, W.H, W.d)
+    bounds = mask_bounds("causal_document_window", W.B, W.S, device="cuda", window=8192)
+    o, lse = fm.forward(q, k, v, bounds, W.scale)
+    torch.cuda.synchronize()
+    compare_fwd(q, k, v, bounds, W.scale, o, lse, heads=[(0, 0), (0, 7)], rows=64)

@@ -174,3 +174,27 @@ def test_per_tile_normalisation_fails_tolerance():
             z = e.sum(axis=1, keepdims=True)
             bad[0, :, h] += np.where(ok[:, None], e / np.where(z == 0, 1, z), 0) @ v[0, c, h]
     assert np.abs(bad - o).max() > 1e-2
+
+
+@pytest.mark.parametrize("name", ["causal_document", "qk_sparse", "global_sliding", "random_eviction",
+                                  "share_question", "block_sparse", "causal_blockwise"])
+def test_skip_hidden_columns_changes_nothing(name):
+    """Leaving out the columns a row group cannot see is exact: compare with
+    the plain dense path (and check the skipped columns really are hidden)."""
+    S, d = 700, 8
+    q, k, v, do = _rand(S, d, 10)
+    b = gen.make_mask(name, S, seed=3, window=50, n_global=3) if name == "global_sliding" \
+        else gen.make_mask(name, S, seed=3)
+    M = om.dense_mask(*b, S)
+    for r0, r1 in ((0, 64), (100, 228), (640, 700), (333, 334)):
+        seen = oa.columns_seen(b, r0, r1)
+        hidden = np.setdiff1d(np.arange(S), seen)
+        assert M[r0:r1][:, hidden].all()
+        assert not M[r0:r1][:, seen].all(axis=0).any()
+    a = oa.backward_head(q[0, :, 0], k[0, :, 0], v[0, :, 0], do[0, :, 0], b, 0.3, slice_rows=64)
+    c = oa.backward_head(q[0, :, 0], k[0, :, 0], v[0, :, 0], do[0, :, 0], b, 0.3, slice_rows=64,
+                         skip_hidden=True)
+    for x, y in zip(a, c):
+        assert np.allclose(x, y, rtol=0, atol=1e-12, equal_nan=True)
+    fo = oa.forward_head(q[0, :, 0], k[0, :, 0], v[0, :, 0], b, 0.3, slice_rows=50, skip_hidden=True)
+    assert np.allclose(fo[0], a[3], rtol=0, atol=1e-12)
