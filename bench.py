@@ -274,8 +274,8 @@ def _oracle_sample_inputs(S, d, mask):
 
 def cpu_baseline(seconds: float = 15.0):
     """The fp64 oracle, as it stands, on a bounded sample of the workload: the
-    backward pass (which recomputes the forward) of the first R query rows of
-    one head, R sized from a 1024-row probe to take about ``seconds``."""
+    full backward pass (which recomputes the forward) of one head at a time,
+    each head with its own seeded inputs, until about ``seconds`` have passed."""
     import numpy as np
 
     from oracle import attention as oa
@@ -283,20 +283,22 @@ def cpu_baseline(seconds: float = 15.0):
 
     W = WORKLOAD
     S, d = W["S"], W["d"]
-    mvec, q, k, v, do = _oracle_sample_inputs(S, d, W["mask"])
-    t0 = time.perf_counter()
-    oa.backward_head(q[:1024], k, v, do[:1024], mvec, d ** -0.5, slice_rows=1024, skip_hidden=True)
-    probe = time.perf_counter() - t0
-    R = int(min(S, max(1024, 1024 * int(seconds / max(probe, 1e-3)))))
-    t0 = time.perf_counter()
-    oa.backward_head(q[:R], k, v, do[:R], mvec, d ** -0.5, slice_rows=1024, skip_hidden=True)
-    el = time.perf_counter() - t0
-    work = int(sum((~om.dense_mask(*mvec, S, rows=np.arange(a, min(R, a + 1024)))).sum()
-                   for a in range(0, R, 1024)))
+    mvec, _, _, _, _ = _oracle_sample_inputs(S, d, W["mask"])
+    per_head = om.visible_count(*mvec, S)
+    heads, el = 0, 0.0
+    rng = np.random.default_rng(0)
+    while el < seconds and heads < W["H"]:
+        q, k, v, do = (rng.standard_normal((S, d)).astype(np.float32).astype(np.float64)
+                       for _ in range(4))
+        t0 = time.perf_counter()
+        oa.backward_head(q, k, v, do, mvec, d ** -0.5, slice_rows=1024, skip_hidden=True)
+        el += time.perf_counter() - t0
+        heads += 1
+    work = heads * per_head
     return {"value": round(14.0 * d * work / el / 1e12, 6), "unit": "TFLOP/s",
             "cores": len(os.sched_getaffinity(0)), "threads": "numpy/BLAS default", "kind": "oracle",
-            "sample": f"fp64 oracle backward (with its forward) of query rows [0, {R}) of one head "
-                      f"of {W['name']}: {work} visible entries in {el:.1f} s"}
+            "sample": f"fp64 oracle backward (with its forward) of {heads} of the {W['H']} heads of "
+                      f"{W['name']}: {work} visible entries in {el:.1f} s"}
 
 
 def run_reference(args):
@@ -342,7 +344,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

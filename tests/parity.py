@@ -4,7 +4,10 @@ with the oracle on the same seeded inputs.
 Tolerances (written here once, used by every parity test):
   O:     max |O - O_ref| <= 1e-2
   LSE:   max |LSE - LSE_ref| <= 1e-3 on rows that see a key, exactly -inf otherwise
-  grads: max |G - G_ref| <= 2e-2 * max |G_ref|
+  grads: max |G - G_ref| <= 2e-2 * max(max |G_ref|, 1e-4)
+         (the floor only matters when the reference gradient is identically
+         zero, e.g. a row that sees a single key: D is formed from the bf16
+         output, so dP - D is a rounding residual instead of an exact 0)
 """
 from __future__ import annotations
 
@@ -16,6 +19,7 @@ from oracle import attention as oa
 O_TOL = 1e-2
 LSE_TOL = 1e-3
 GRAD_REL = 2e-2
+GRAD_FLOOR = 1e-4
 
 
 def head_slice(t, b, h):
@@ -79,6 +83,6 @@ def compare_bwd(q, k, v, do, bounds, scale, dq, dk, dv, heads=None, slice_rows=1
             scale_ref = float(np.abs(ref).max())
             rel = err / scale_ref if scale_ref > 0 else err
             worst[name] = max(worst[name], rel)
-            assert err <= GRAD_REL * max(scale_ref, 1e-30) or (scale_ref == 0 and err == 0), \
+            assert err <= GRAD_REL * max(scale_ref, GRAD_FLOOR), \
                 f"{name} error {err} vs max|ref| {scale_ref} at (b={b}, h={h})"
     return worst

@@ -79,7 +79,7 @@ def test_per_head_masks_strides_and_cross_lengths():
     dq = torch.empty(B, Sq, H, 2 * d, device="cuda", dtype=torch.bfloat16)[..., d:]
     dk = torch.empty(B, Skv, H, 2 * d, device="cuda", dtype=torch.bfloat16)[..., :d]
     dv = torch.empty(B, Skv, H, 2 * d, device="cuda", dtype=torch.bfloat16)[..., d:]
-    do_o = torch.empty_like(o)
+    do_o = torch.empty(B, Sq, H, 2 * d, device="cuda", dtype=torch.bfloat16)[..., d:]
     do_o.copy_(do)  # dO must have O's strides
     fm.backward(q, k, v, o, lse, do_o, bounds, 0.1, dq=dq, dk=dk, dv=dv)
     torch.cuda.synchronize()
