@@ -119,6 +119,32 @@ fm_status fm_bwd(const fm_desc* desc, const void* q, const void* k, const void* 
                  const int32_t* lte, const int32_t* uts, const int32_t* ute, float scale,
                  void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
 
+/* Size of the fixed device scratch used by fm_fwd_static (8 MiB per GPU). */
+#define FM_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* Forward pass for callers that cannot allocate device memory when they call
+ * it (for instance a plugin inside a framework that owns all device memory
+ * through its own allocator, or a latency-critical path that must not call
+ * cudaMalloc/cudaFree).  The pages describe no such interface; it has no
+ * counterpart there.  Same arguments and results as fm_fwd, without `ws`:
+ * the scratch lives in a fixed array of FM_STATIC_SCRATCH_BYTES in device
+ * memory that belongs to the library image, so every GPU that loads the
+ * library keeps those bytes until the process exits.  Problems whose
+ * fm_workspace_size(desc, 0) exceeds FM_STATIC_SCRATCH_BYTES are rejected
+ * with FM_ERR_WORKSPACE before anything is enqueued.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current); make that first call before any stream capture.
+ * The function allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library call).  All calls on a device share the array: calls whose work
+ * may overlap on the GPU (other streams, other host threads) race and give
+ * undefined results, so serialise them.  Device-side findings (bound values
+ * out of range) are recorded in the shared array and cannot be read back
+ * through this entry point; check bounds with fm_plan on a caller workspace
+ * if that is needed. */
+fm_status fm_fwd_static(const fm_desc* desc, const void* q, const void* k, const void* v,
+                        const int32_t* lts, const int32_t* lte, const int32_t* uts,
+                        const int32_t* ute, float scale, void* o, float* lse, void* stream);
+
 /* Mask localisation ("clip, shift, max" over the bound vectors; FlashMask-3
  * page, introduction and «Ключевые факты»).  A rank holds the query rows of
  * n_chunks chunks of the global sequence, chunk c covering global rows
