@@ -114,7 +114,9 @@ def run_ours(args):
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    W = WORKLOAD
+    W = dict(WORKLOAD)
+    if args.heads:
+        W["H"] = args.heads
     B, H, S, d = W["B"], W["H"], W["S"], W["d"]
     scale = d ** -0.5
     q, k, v, do = qkv_do(B, S, S, H, d, seed=0, device="cuda")
@@ -166,7 +168,22 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
 
-    # ---- end to end through the public API, host buffers, copies timed
+    if args.no_e2e:
+        e2e_ms, h2d, d2h = float("nan"), 0, 0
+    else:
+        e2e_ms, h2d, d2h = run_e2e(args, fm, q, k, v, do, bounds, scale, o, lse, dq, dk, dv,
+                                   ws_f, ws_b, stream, world)
+    report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2d, d2h, clk)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, fm, q, k, v, do, bounds, scale, o, lse, dq, dk, dv, ws_f, ws_b, stream, world):
+    """Same step through the public API with pinned HOST inputs and outputs:
+    host-to-device copies of Q, K, V, dO and the bounds, and device-to-host
+    copies of O, LSE, dQ, dK, dV, all inside the timed region."""
+    import torch
+    import torch.distributed as dist
     hq, hk, hv, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
     hb = bounds.cpu().pin_memory()
     ho, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, dq, dk, dv))
@@ -204,7 +221,12 @@ def run_ours(args):
         e2e_ms = float(t.item())
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo, hb))
     d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdq, hdk, hdv))
+    return e2e_ms, h2d, d2h
 
+
+def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2d, d2h, clk):
+    B, H, S, d = W["B"], W["H"], W["S"], W["d"]
+    flop_step = flop_fwd + flop_bwd
     if rank == 0:
         peaks, peak_src = _peaks()
         bwd_ms, bwd_n = prof["bwd_kernel"]
@@ -216,7 +238,8 @@ def run_ours(args):
         dom_flop = (flop_bwd if dom == "bwd_kernel" else flop_fwd)
         dom_avg_ms = bwd_avg if dom == "bwd_kernel" else fwd_avg
         achieved = dom_flop / (dom_avg_ms * 1e-3) / 1e12
-        peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+        # the timed loop lasts well under a second: compare with the burst figure
+        peak = float(peaks["bf16_tflops"])
         value = world * flop_step / (ms * 1e-3) / 1e12
         launches = sum(n for _, n in prof.values())
         total_kernel_ms = sum(t for t, _ in prof.values())
@@ -242,22 +265,21 @@ def run_ours(args):
             "pct_bf16_peak": round(100.0 * value / world / peak, 1),
             "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2),
                          "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                         "peak_source": f"bf16_tflops_sustained of {peak_src}",
+                         "peak_source": f"bf16_tflops (burst) of {peak_src}",
                          "traffic": None},
             "kernel_ms_per_step": {n: round(t / args.steps, 4) for n, (t, c) in prof.items() if c},
             "kernel_launches_per_step": {n: c // args.steps for n, (t, c) in prof.items() if c},
             "kernel_time_share": {n: round(t / total_kernel_ms, 4) for n, (t, c) in prof.items() if c},
             "gpu_launches": launches,
-            "e2e": {"value": round(world * flop_step / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                    "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+            "e2e": None if e2e_ms != e2e_ms else {
+                "value": round(world * flop_step / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
             "clocks": clk,
         }
         if not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
         print(json.dumps(out), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
 
 
 def _oracle_sample_inputs(S, d, mask):
@@ -349,6 +371,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="override H (smaller cases for profiler captures; not a bench line)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
