@@ -181,7 +181,8 @@ fm_status fm_profile_read(double* total_ms, int* launches, int n);
 const char* fm_kernel_name(int id);
 
 /* Synchronise `stream` and read the device status word of `ws`: FM_OK,
- * FM_ERR_BOUNDS or FM_ERR_TIMEOUT (timeout wins if both are set). */
+ * FM_ERR_BOUNDS, FM_ERR_TIMEOUT, or FM_ERR_CUDA if a kernel found its shared
+ * memory misaligned and did nothing (precedence: CUDA, timeout, bounds). */
 fm_status fm_device_status(const void* ws, void* stream);
 
 /* Static description of a status code. */

@@ -198,6 +198,7 @@ fm_status fm_device_status(const void* ws, void* stream) {
   if (cudaMemcpyAsync(&word, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return FM_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return FM_ERR_CUDA;
+  if (word & DEV_LAYOUT) return FM_ERR_CUDA;
   if (word & DEV_TIMEOUT) return FM_ERR_TIMEOUT;
   if (word & DEV_BOUNDS) return FM_ERR_BOUNDS;
   return FM_OK;

@@ -120,11 +120,15 @@ struct BwdCfg {
   static constexpr int OFF_Q = OFF_V + TILE;          // 2 stages
   static constexpr int OFF_DO = OFF_Q + 2 * TILE;     // 2 stages
   static constexpr int OFF_DS = OFF_DO + 2 * TILE;    // 128 x 128 bf16, [key][q]
-  static constexpr int OFF_BAR = OFF_DS + 128 * 128 * 2;
+  static constexpr int OFF_LD = OFF_DS + 128 * 128 * 2;  // 2 stages x (LSE*log2e, D) fp32
+  static constexpr int OFF_BAR = OFF_LD + 2 * 1024;
   static constexpr int NBAR = 20;
-  static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16 + 1024;
+  static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
+  // at least 120 KB so that one CTA (which takes all 512 TMEM columns) is
+  // resident per SM
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   static constexpr uint32_t T_A = 0, T_B = 128, T_DV = 256, T_DK = 384, T_COLS = 512;
+  static constexpr int THREADS = 320;  // 8 compute warps, 1 TMA warp, 1 MMA warp
 };
 
 enum { C_KVFULL = 0, C_KVEMPTY, C_QFULL0, C_QFULL1, C_QEMPTY0, C_QEMPTY1, C_SFULL, C_PREADY,
@@ -146,15 +150,28 @@ struct BwdParams {
   int* status;
 };
 
+// Tile pipeline per q-tile t of a unit (MMA issue order on the left, compute
+// warps on the right; region A = TMEM [0,128), region B = [128,256)):
+//   S^T(t) = K Q^T -> A       [after dV(t-1) read P^T(t-1) from A]
+//                               drain dQ(t-1) from B (fp32 atomics)
+//   dP^T(t) = V dO^T -> B     [after that drain]
+//                               P^T(t) = exp2(S^T*scale*log2e - LSE*log2e) -> A
+//   dV += P^T(t) dO           [after P^T(t)]
+//                               dS^T(t) = P^T o (dP^T - D) -> smem
+//   dK += dS^T Q, dQ = dS K -> B   [after dS^T(t)]
+// so the drain, P and dS work of the compute warps overlaps S, dP and dV.
+// Compute warp w owns TMEM lane quarter (w & 3) and column half (w >> 2).
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bwd_kernel(const __grid_constant__ BwdParams P, const __grid_constant__ CUtensorMap tmQ,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __grid_constant__ CUtensorMap tmDO) {
   using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {  // swizzled tiles need a 1024-aligned base
+    if (threadIdx.x == 0) atomicOr(P.status, DEV_LAYOUT);
+    return;
+  }
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sDS = sbase + C::OFF_DS;
   const uint32_t bar0 = sbase + C::OFF_BAR;
@@ -162,6 +179,7 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int TMA_WARP = 8, MMA_WARP = 9;
 
   if (tid == 0) {
     mbar_init(bar(C_KVFULL), 1);
@@ -171,23 +189,23 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(bar(C_QEMPTY0), 1);
     mbar_init(bar(C_QEMPTY1), 1);
     mbar_init(bar(C_SFULL), 1);
-    mbar_init(bar(C_PREADY), 128);
+    mbar_init(bar(C_PREADY), 256);
     mbar_init(bar(C_DVDONE), 1);
     mbar_init(bar(C_DPFULL), 1);
-    mbar_init(bar(C_DSREADY), 128);
+    mbar_init(bar(C_DSREADY), 256);
     mbar_init(bar(C_DQFULL), 1);
-    mbar_init(bar(C_DQEMPTY), 128);
+    mbar_init(bar(C_DQEMPTY), 256);
     mbar_init(bar(C_ACCFULL), 1);
-    mbar_init(bar(C_ACCEMPTY), 128);
+    mbar_init(bar(C_ACCEMPTY), 256);
     mbar_init(bar(C_DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == MMA_WARP) {
     tmem_alloc(smem_u32(tmem_slot), C::T_COLS);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == TMA_WARP && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
@@ -197,6 +215,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  const int rows_pad = P.nQ * kTile;
 
   auto wait = [&](int b, uint32_t parity) -> bool {
     if (*abort_flag) return false;
@@ -224,7 +243,7 @@ __global__ void __launch_bounds__(192, 1)
     return P.col_count[col];
   };
 
-  if (warp == 4) {
+  if (warp == TMA_WARP) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it = 0, un = 0;
@@ -242,13 +261,14 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_4d(sK + s * 16384, &tmK, bar(C_KVFULL), s * 64, h, kj * kTile, b);
           tma_load_4d(sV + s * 16384, &tmV, bar(C_KVFULL), s * 64, h, kj * kTile, b);
         }
+        const size_t bh_row = (static_cast<size_t>(b) * P.H + h) * rows_pad;
         for (int t = 0; t < n; ++t, ++it) {
           const int qi = list[t] >> 2;
           const int st = it & 1;
           const uint32_t use = it >> 1;
           if (use > 0 && !wait(C_QEMPTY0 + st, (use - 1) & 1)) { ok = false; break; }
           const uint32_t fb = bar(C_QFULL0 + st);
-          mbar_arrive_expect_tx(fb, 2 * C::TILE);
+          mbar_arrive_expect_tx(fb, 2 * C::TILE + 1024);
           const uint32_t sQ = sbase + C::OFF_Q + st * C::TILE;
           const uint32_t sDO = sbase + C::OFF_DO + st * C::TILE;
 #pragma unroll
@@ -256,6 +276,9 @@ __global__ void __launch_bounds__(192, 1)
             tma_load_4d(sQ + s * 16384, &tmQ, fb, s * 64, h, qi * kTile, b);
             tma_load_4d(sDO + s * 16384, &tmDO, fb, s * 64, h, qi * kTile, b);
           }
+          const uint32_t sLD = sbase + C::OFF_LD + st * 1024;
+          bulk_load(sLD, P.lse_log2 + bh_row + qi * kTile, 512, fb);
+          bulk_load(sLD + 512, P.delta + bh_row + qi * kTile, 512, fb);
         }
       }
       // drain every issued copy before exit
@@ -264,7 +287,7 @@ __global__ void __launch_bounds__(192, 1)
       if (un > 0) mbar_wait(bar(C_KVFULL), (un - 1) & 1, P.status);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
@@ -283,7 +306,7 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t sQ = sbase + C::OFF_Q + st * C::TILE;
           const uint32_t sDO = sbase + C::OFF_DO + st * C::TILE;
           if (!wait(C_QFULL0 + st, (it >> 1) & 1)) { ok = false; break; }
-          // region A holds P^T of the previous tile until its dV has run
+          // S^T into region A once the previous dV has read P^T from it
           if (it > 0 && !wait(C_DVDONE, (it - 1) & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
@@ -293,16 +316,7 @@ __global__ void __launch_bounds__(192, 1)
                    sdesc_sw128(sQ + koff, 16, 1024), idSS, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(C_SFULL));
-          // dV += P^T dO once P^T is in TMEM (and the previous unit's dV/dK were read)
-          if (!wait(C_PREADY, it & 1)) { ok = false; break; }
-          if (t == 0 && un > 0 && !wait(C_ACCEMPTY, (un - 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tbase + C::T_DV, tbase + C::T_A + kk * 8,
-                   sdesc_sw128(sDO + kk * 2048, 16384, 1024), idKB, (t > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(C_DVDONE));
-          // dP^T = V dO^T into region B once the previous dQ tile was drained
+          // dP^T into region B once the previous dQ tile was drained
           if (it > 0 && !wait(C_DQEMPTY, (it - 1) & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
@@ -312,6 +326,18 @@ __global__ void __launch_bounds__(192, 1)
                    sdesc_sw128(sDO + koff, 16, 1024), idSS, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(C_DPFULL));
+          // dV += P^T dO once P^T is in TMEM (and the previous unit's dV/dK were read)
+          if (!wait(C_PREADY, it & 1)) { ok = false; break; }
+          if (t == 0 && un > 0 && !wait(C_ACCEMPTY, (un - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            // P^T of q columns 0..63 sits in TMEM columns [0,32), 64..127 in [64,96)
+            const uint32_t acol = (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+            mma_ts(tbase + C::T_DV, tbase + C::T_A + acol,
+                   sdesc_sw128(sDO + kk * 2048, 16384, 1024), idKB, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(C_DVDONE));
           // dK += dS^T Q and dQ = dS K once dS^T is in smem
           if (!wait(C_DSREADY, it & 1)) { ok = false; break; }
           tc_fence_after();
@@ -339,30 +365,30 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ compute warps
-    const int r = tid;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const int rows_pad = P.nQ * kTile;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;  // TMEM lane: key row (S^T, dP^T, dK, dV), q row (dQ)
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int c0 = half * 64;           // this thread's 64 of the 128 q columns
     uint32_t it = 0, un = 0;
-    // dQ tile drain: query row r of the tile whose dQ sits in region B
+    // dQ tile drain: q row r, columns [half*D/2, half*D/2 + D/2) of region B
     auto drain_dq = [&](uint32_t jt, int b, int h, int qi) -> bool {
       if (!wait_all(C_DQFULL, jt & 1)) return false;
       tc_fence_after();
       const int qrow = qi * kTile + r;
-      float* dst = P.dq_acc + ((static_cast<size_t>(b) * P.H + h) * P.Sq + qrow) * D;
-      uint32_t raw[32];
+      float* dst = P.dq_acc + ((static_cast<size_t>(b) * P.H + h) * P.Sq + qrow) * D + half * (D / 2);
+      // this thread's D/2 columns in one TMEM round trip
+      uint32_t raw[D / 2];
+      if constexpr (D == 128) tmem_ld64(tbase + lane_off + C::T_B + half * (D / 2), raw);
+      else tmem_ld32(tbase + lane_off + C::T_B + half * (D / 2), raw);
+      tmem_wait_ld();
+      if (qrow < P.Sq) {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(tbase + lane_off + C::T_B + c * 32, raw);
-        tmem_wait_ld();
-        if (qrow < P.Sq) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float4 v = make_float4(__uint_as_float(raw[4 * i]) * P.scale,
-                                   __uint_as_float(raw[4 * i + 1]) * P.scale,
-                                   __uint_as_float(raw[4 * i + 2]) * P.scale,
-                                   __uint_as_float(raw[4 * i + 3]) * P.scale);
-            atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + 4 * i), v);
-          }
+        for (int i = 0; i < D / 8; ++i) {
+          const float4 v = make_float4(__uint_as_float(raw[4 * i]) * P.scale,
+                                       __uint_as_float(raw[4 * i + 1]) * P.scale,
+                                       __uint_as_float(raw[4 * i + 2]) * P.scale,
+                                       __uint_as_float(raw[4 * i + 3]) * P.scale);
+          atomicAdd(reinterpret_cast<float4*>(dst + 4 * i), v);
         }
       }
       tc_fence_before();
@@ -376,14 +402,14 @@ __global__ void __launch_bounds__(192, 1)
       const int n = unit_info(idx, b, h, kj, list);
       const int key = kj * kTile + r;
       __nv_bfloat16* dk_row = P.dk + b * P.k_stride[0] + static_cast<int64_t>(key) * P.k_stride[1] +
-                              h * P.k_stride[2];
+                              h * P.k_stride[2] + half * (D / 2);
       __nv_bfloat16* dv_row = P.dv + b * P.v_stride[0] + static_cast<int64_t>(key) * P.v_stride[1] +
-                              h * P.v_stride[2];
+                              h * P.v_stride[2] + half * (D / 2);
       if (n == 0) {
         if (key < P.Skv) {
           const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) {
+          for (int c = 0; c < D / 16; ++c) {
             reinterpret_cast<uint4*>(dk_row)[c] = z;
             reinterpret_cast<uint4*>(dv_row)[c] = z;
           }
@@ -400,39 +426,39 @@ __global__ void __launch_bounds__(192, 1)
         ute = __ldg(P.bounds[3] + at);
       }
       const bool key_ragged = (kj == P.nK - 1) && (P.Skv & (kTile - 1));
-      const float* lse_bh = P.lse_log2 + (static_cast<size_t>(b) * P.H + h) * rows_pad;
-      const float* del_bh = P.delta + (static_cast<size_t>(b) * P.H + h) * rows_pad;
       int prev_qi = -1;
       for (int t = 0; t < n; ++t, ++it) {
         const int e = list[t];
         const int qi = e >> 2;
         const bool partial = ((e & 3) == CLS_PARTIAL) || key_ragged;
-        const float4* l4 = reinterpret_cast<const float4*>(lse_bh + qi * kTile);
-        const float4* d4 = reinterpret_cast<const float4*>(del_bh + qi * kTile);
-        // ---- P^T row = exp2(S^T * scale*log2e - LSE*log2e), masked entries 0
+        const int st = it & 1;
+        const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LD + st * 1024) + c0;
+        const float* del_s = lse_s + 128;
+        // ---- drain the previous tile's dQ from region B (overlaps S^T(t))
+        if (t > 0 && !drain_dq(it - 1, b, h, prev_qi)) { ok = false; break; }
+        // ---- P^T = exp2(S^T * scale*log2e - LSE*log2e), hidden entries 0
         if (!wait_all(C_SFULL, it & 1)) { ok = false; break; }
+        // the LSE/D of this stage arrived with the Q/dO tiles
+        if (!wait_all(C_QFULL0 + st, (it >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        float p[128];
+        float p[64];
         {
-          uint32_t raw[32];
+          uint32_t raw[64];
+          tmem_ld64(tbase + lane_off + C::T_A + c0, raw);
+          tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tbase + lane_off + C::T_A + c * 32, raw);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 L = __ldg(l4 + c * 8 + i);
-              p[c * 32 + 4 * i + 0] = ex2(fmaf(__uint_as_float(raw[4 * i + 0]), P.scale_log2, -L.x));
-              p[c * 32 + 4 * i + 1] = ex2(fmaf(__uint_as_float(raw[4 * i + 1]), P.scale_log2, -L.y));
-              p[c * 32 + 4 * i + 2] = ex2(fmaf(__uint_as_float(raw[4 * i + 2]), P.scale_log2, -L.z));
-              p[c * 32 + 4 * i + 3] = ex2(fmaf(__uint_as_float(raw[4 * i + 3]), P.scale_log2, -L.w));
-            }
+          for (int i = 0; i < 16; ++i) {
+            const float4 L = *reinterpret_cast<const float4*>(lse_s + 4 * i);
+            p[4 * i + 0] = ex2(fmaf(__uint_as_float(raw[4 * i + 0]), P.scale_log2, -L.x));
+            p[4 * i + 1] = ex2(fmaf(__uint_as_float(raw[4 * i + 1]), P.scale_log2, -L.y));
+            p[4 * i + 2] = ex2(fmaf(__uint_as_float(raw[4 * i + 2]), P.scale_log2, -L.z));
+            p[4 * i + 3] = ex2(fmaf(__uint_as_float(raw[4 * i + 3]), P.scale_log2, -L.w));
           }
         }
         if (partial) {
-          const int q0 = qi * kTile;
+          const int q0 = qi * kTile + c0;
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
+          for (int c = 0; c < 64; ++c) {
             const int q = q0 + c;
             const bool hid = (lts <= q && q < lte) || (uts <= q && q < ute);
             p[c] = hid ? 0.f : p[c];
@@ -441,45 +467,37 @@ __global__ void __launch_bounds__(192, 1)
         {
           uint32_t pk[32];
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(p[half * 64 + 2 * c], p[half * 64 + 2 * c + 1]);
-            tmem_st32(tbase + lane_off + C::T_A + half * 32, pk);
-          }
+          for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(p[2 * c], p[2 * c + 1]);
+          // into the TMEM columns this thread read: [c0, c0 + 32)
+          tmem_st32(tbase + lane_off + C::T_A + c0, pk);
           tmem_wait_st();
         }
         tc_fence_before();
         mbar_arrive(bar(C_PREADY));
-        // ---- drain the previous tile's dQ (region B) while dV runs
-        if (t > 0 && !drain_dq(it - 1, b, h, prev_qi)) { ok = false; break; }
-        // ---- dS^T row = P^T o (dP^T - D), to smem as bf16 [key][q]
+        // ---- dS^T = P^T o (dP^T - D), to smem as bf16 [key][q] (slab = half)
         if (!wait_all(C_DPFULL, it & 1)) { ok = false; break; }
         tc_fence_after();
         {
-          uint32_t raw[32];
-          const uint32_t row_base = sDS + r * 128;
+          uint32_t raw[64];
+          tmem_ld64(tbase + lane_off + C::T_B + c0, raw);
+          tmem_wait_ld();
+          const uint32_t row_base = sDS + half * 16384 + r * 128;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tbase + lane_off + C::T_B + c * 32, raw);
-            tmem_wait_ld();
-            uint32_t w[16];
+          for (int j = 0; j < 8; ++j) {
+            uint32_t w[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 Dv = __ldg(d4 + c * 8 + i);
-              const float s0 = p[c * 32 + 4 * i + 0] * (__uint_as_float(raw[4 * i + 0]) - Dv.x);
-              const float s1 = p[c * 32 + 4 * i + 1] * (__uint_as_float(raw[4 * i + 1]) - Dv.y);
-              const float s2 = p[c * 32 + 4 * i + 2] * (__uint_as_float(raw[4 * i + 2]) - Dv.z);
-              const float s3 = p[c * 32 + 4 * i + 3] * (__uint_as_float(raw[4 * i + 3]) - Dv.w);
+            for (int i = 0; i < 2; ++i) {
+              const float4 Dv = *reinterpret_cast<const float4*>(del_s + 8 * j + 4 * i);
+              const int c = 8 * j + 4 * i;
+              const float s0 = p[c + 0] * (__uint_as_float(raw[c + 0]) - Dv.x);
+              const float s1 = p[c + 1] * (__uint_as_float(raw[c + 1]) - Dv.y);
+              const float s2 = p[c + 2] * (__uint_as_float(raw[c + 2]) - Dv.z);
+              const float s3 = p[c + 3] * (__uint_as_float(raw[c + 3]) - Dv.w);
               w[2 * i] = pack_bf16(s0, s1);
               w[2 * i + 1] = pack_bf16(s2, s3);
             }
-            // 32 q columns = 4 chunks of 16 B in slab c/2, logical chunks (c&1)*4 .. +3
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint32_t chunk = static_cast<uint32_t>((c & 1) * 4 + j) ^ static_cast<uint32_t>(r & 7);
-              st_shared_v4(row_base + (c >> 1) * 16384 + chunk * 16, w[4 * j], w[4 * j + 1],
-                           w[4 * j + 2], w[4 * j + 3]);
-            }
+            const uint32_t chunk = static_cast<uint32_t>(j) ^ static_cast<uint32_t>(r & 7);
+            st_shared_v4(row_base + chunk * 16, w[0], w[1], w[2], w[3]);
           }
         }
         fence_proxy_async_smem();
@@ -489,14 +507,14 @@ __global__ void __launch_bounds__(192, 1)
       }
       if (!ok) break;
       if (!drain_dq(it - 1, b, h, prev_qi)) { ok = false; break; }
-      // ---- epilogue: dV and scale * dK for this key row
+      // ---- epilogue: dV and scale * dK, this thread's half of the columns
       if (!wait_all(C_ACCFULL, un & 1)) { ok = false; break; }
       tc_fence_after();
       uint32_t raw[32];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(tbase + lane_off + C::T_DV + c * 32, raw);
-        tmem_wait_ld();
+      for (int c = 0; c < D / 64; ++c) {
+        tmem_ld32(tbase + lane_off + C::T_DV + half * (D / 2) + c * 32, raw);
+        tmem_wait_ld();  // (once per unit: not on the per-tile path)
         if (key < P.Skv) {
           uint4* dst = reinterpret_cast<uint4*>(dv_row + c * 32);
 #pragma unroll
@@ -506,7 +524,7 @@ __global__ void __launch_bounds__(192, 1)
                                 pack_bf16(__uint_as_float(raw[8 * i + 4]), __uint_as_float(raw[8 * i + 5])),
                                 pack_bf16(__uint_as_float(raw[8 * i + 6]), __uint_as_float(raw[8 * i + 7])));
         }
-        tmem_ld32(tbase + lane_off + C::T_DK + c * 32, raw);
+        tmem_ld32(tbase + lane_off + C::T_DK + half * (D / 2) + c * 32, raw);
         tmem_wait_ld();
         if (key < P.Skv) {
           uint4* dst = reinterpret_cast<uint4*>(dk_row + c * 32);
@@ -527,7 +545,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tbase, C::T_COLS);
   }
@@ -585,7 +603,7 @@ static fm_status launch_bwd_d(const Plan& p, const fm_desc& desc, const TensorAr
     return FM_ERR_CUDA;
   const int grid = P.n_units < num_sms() ? P.n_units : num_sms();
   prof_begin(K_BWD, s);
-  kern<<<grid, 192, C::SMEM, s>>>(P, tq, tk, tv, tdo);
+  kern<<<grid, C::THREADS, C::SMEM, s>>>(P, tq, tk, tv, tdo);
   prof_end(K_BWD, s);
   if (cudaGetLastError() != cudaSuccess) return FM_ERR_CUDA;
   {

@@ -32,23 +32,35 @@ template <int D>
 struct FwdCfg {
   static constexpr int SLABS = D / 64;
   static constexpr int TILE = 128 * D * 2;  // bytes of one 128-row tile
-  static constexpr int NST = 2;             // K/V pipeline stages
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + TILE;
-  static constexpr int OFF_V = OFF_K + NST * TILE;
-  static constexpr int OFF_BND = OFF_V + NST * TILE;  // NST x 128 x int4
-  static constexpr int OFF_BAR = OFF_BND + NST * 128 * 16;
-  static constexpr int NBAR = 16;
-  // + alignment slack; at least 120 KB so that one CTA (which takes all 512
-  // TMEM columns) is resident per SM
-  static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16 + 1024;
+  static constexpr int OFF_Q = 0;                       // 2 slots
+  static constexpr int OFF_K = OFF_Q + 2 * TILE;        // 2 stages
+  static constexpr int OFF_V = OFF_K + 2 * TILE;        // 2 stages
+  static constexpr int OFF_BND = OFF_V + 2 * TILE;      // 2 stages x 128 x int4
+  static constexpr int OFF_BAR = OFF_BND + 2 * 128 * 16;
+  static constexpr int NBAR = 24;
+  static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
+  // at least 120 KB so that one CTA (which takes all 512 TMEM columns) is
+  // resident per SM
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
-  static constexpr uint32_t T_S = 0, T_O = 256, T_P = 384, T_COLS = 512;
+  // TMEM: S of slot s at [128 s, 128 s + 128) (P packed into its first 64
+  // columns), O of slot s at [256 + 128 s, 256 + 128 s + D)
+  static constexpr uint32_t T_COLS = 512;
+  // warpgroups 0 and 1: softmax of slot 0 / slot 1; warpgroup 2: the Q/K/
+  // bounds load warp, the MMA warp, the V load warp and one idle warp
+  static constexpr int THREADS = 384;
+  // register split (setmaxnreg): 2 x 128 x REGS_SOFTMAX + 128 x REGS_PRODUCER
+  // = 62464 <= THREADS x (compiled registers); the launch checks that the
+  // kernel was compiled with at least MIN_LAUNCH_REGS registers per thread
+  static constexpr uint32_t REGS_SOFTMAX = 216, REGS_PRODUCER = 56;
+  static constexpr int MIN_LAUNCH_REGS =
+      (2 * 128 * REGS_SOFTMAX + 128 * REGS_PRODUCER + THREADS - 1) / THREADS;
 };
 
-// barrier slots
-enum { B_QFULL = 0, B_QEMPTY, B_SFULL0, B_SFULL1, B_SEMPTY0, B_SEMPTY1, B_PFULL, B_PVDONE,
-       B_OEMPTY, B_DRAIN, B_KVFULL0, B_KVEMPTY0 = B_KVFULL0 + 2 };
+// barrier slots; "s" = q-tile slot (0/1), "st" = K/V stage (0/1)
+enum {
+  B_QFULL0 = 0, B_QEMPTY0 = 2, B_SFULL0 = 4, B_PFULL0 = 6, B_PVDONE0 = 8, B_OEMPTY0 = 10,
+  B_KFULL0 = 12, B_KEMPTY0 = 14, B_VFULL0 = 16, B_VEMPTY0 = 18, B_BEMPTY0 = 20, B_DRAIN = 22
+};
 
 struct FwdParams {
   int B, H, Hm, Sq, Skv, nQ, nK, n_units;
@@ -67,51 +79,140 @@ __device__ __forceinline__ bool tile_partial(int e, int kj, int nK, int Skv) {
   return ((e & 3) == CLS_PARTIAL) || (kj == nK - 1 && (Skv & (kTile - 1)) != 0);
 }
 
+// The CTA's units are idx = blockIdx.x + k * gridDim.x, k = 0, 1, 2, ...;
+// slot s takes the units with k % 2 == s.  A cursor walks one slot's
+// non-empty tiles; the merge interleaves the two slots' tiles (alternating
+// while both have tiles left).  The TMA warp, the MMA warp and both softmax
+// warpgroups run identical merges, so they agree on which K/V stage and
+// which barrier phase every tile uses.
+struct Cursor {
+  int k, t, n, row;
+};
+struct UnitInfo {
+  int b, h, qi, row, n;
+};
+
+__device__ __forceinline__ UnitInfo unit_of(const FwdParams& P, int idx) {
+  UnitInfo u;
+  const int id = P.order[idx];
+  const int bh = id / P.nQ;
+  u.qi = id - bh * P.nQ;
+  u.b = bh / P.H;
+  u.h = bh - u.b * P.H;
+  u.row = (u.b * P.Hm + (P.Hm == 1 ? 0 : u.h)) * P.nQ + u.qi;
+  u.n = P.row_count[u.row];
+  return u;
+}
+
+__device__ __forceinline__ void cursor_next_unit(const FwdParams& P, Cursor& c) {
+  while (true) {
+    c.k += 2;
+    const int idx = blockIdx.x + c.k * gridDim.x;
+    if (idx >= P.n_units) {
+      c.n = -1;
+      return;
+    }
+    const UnitInfo u = unit_of(P, idx);
+    if (u.n > 0) {
+      c.n = u.n;
+      c.row = u.row;
+      c.t = 0;
+      return;
+    }
+  }
+}
+
+struct Merge {
+  Cursor c0, c1;  // two scalars, not an array: no dynamically indexed local memory
+  int turn;
+  __device__ __forceinline__ void init(const FwdParams& P) {
+    c0.k = -2;
+    c0.t = 0;
+    cursor_next_unit(P, c0);
+    c1.k = -1;
+    c1.t = 0;
+    cursor_next_unit(P, c1);
+    turn = 0;
+  }
+  __device__ __forceinline__ int peek() const {
+    const bool a = c0.n > 0, b = c1.n > 0;
+    return (a && b) ? turn : (a ? 0 : (b ? 1 : -1));
+  }
+  // Take the next merged tile: its slot, unit index k, tile t and whether it
+  // is the first / last tile of its unit.
+  __device__ __forceinline__ int next(const FwdParams& P, int& k, int& t, int& row, bool& first,
+                                      bool& last) {
+    const int s = peek();
+    if (s < 0) return -1;
+    if (c0.n > 0 && c1.n > 0) turn ^= 1;
+    Cursor x = s ? c1 : c0;
+    k = x.k;
+    t = x.t;
+    row = x.row;
+    first = x.t == 0;
+    last = x.t == x.n - 1;
+    if (++x.t >= x.n) cursor_next_unit(P, x);
+    if (s) c1 = x; else c0 = x;
+    return s;
+  }
+};
+
+// Two-entry per-slot state kept in registers (selected, never indexed).
+template <typename T>
+struct Pair {
+  T v0, v1;
+  __device__ __forceinline__ T get(int s) const { return s ? v1 : v0; }
+  __device__ __forceinline__ void set(int s, T v) {
+    if (s) v1 = v; else v0 = v;
+  }
+};
+
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_kernel(const __grid_constant__ FwdParams P, const __grid_constant__ CUtensorMap tmQ,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using C = FwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {  // swizzled tiles need a 1024-aligned base
+    if (threadIdx.x == 0) atomicOr(P.status, DEV_LAYOUT);
+    return;
+  }
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase + C::OFF_Q;
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * i; };
   int4* bnd = reinterpret_cast<int4*>(smem + C::OFF_BND);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int TMA_WARP = 8, MMA_WARP = 9, V_WARP = 10;
 
   if (tid == 0) {
-    mbar_init(bar(B_QFULL), 1);
-    mbar_init(bar(B_QEMPTY), 1);
-    mbar_init(bar(B_SFULL0), 1);
-    mbar_init(bar(B_SFULL1), 1);
-    mbar_init(bar(B_SEMPTY0), 128);
-    mbar_init(bar(B_SEMPTY1), 128);
-    mbar_init(bar(B_PFULL), 128);
-    mbar_init(bar(B_PVDONE), 1);
-    mbar_init(bar(B_OEMPTY), 128);
-    mbar_init(bar(B_DRAIN), 1);
-    for (int s = 0; s < C::NST; ++s) {
-      mbar_init(bar(B_KVFULL0 + s), 1);
-      mbar_init(bar(B_KVEMPTY0 + s), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_QFULL0 + s), 1);
+      mbar_init(bar(B_QEMPTY0 + s), 1);
+      mbar_init(bar(B_SFULL0 + s), 1);
+      mbar_init(bar(B_PFULL0 + s), 128);
+      mbar_init(bar(B_PVDONE0 + s), 1);
+      mbar_init(bar(B_OEMPTY0 + s), 128);
+      mbar_init(bar(B_KFULL0 + s), 1);
+      mbar_init(bar(B_KEMPTY0 + s), 1);
+      mbar_init(bar(B_VFULL0 + s), 1);
+      mbar_init(bar(B_VEMPTY0 + s), 1);
+      mbar_init(bar(B_BEMPTY0 + s), 128);
     }
+    mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == MMA_WARP) {
     tmem_alloc(smem_u32(tmem_slot), C::T_COLS);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == TMA_WARP && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
   }
+  if (warp == V_WARP && lane == 0) tma_prefetch_desc(&tmV);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -131,266 +232,335 @@ __global__ void __launch_bounds__(192, 1)
     const bool ok = wait(b, parity);
     return __all_sync(0xffffffffu, ok);
   };
-  auto aborted_all = [&]() -> bool { return __any_sync(0xffffffffu, *abort_flag != 0); };
 
-  if (warp == 4) {
+  if (warp >= 8) {
+  // producer warpgroup: small register budget (each role branch below runs
+  // after the budget change, so the compiler allocates it within the budget)
+  regs_decrease<C::REGS_PRODUCER>();
+  if (warp == TMA_WARP) {
     // ------------------------------------------------------------ TMA producer
-    uint32_t it = 0, qn = 0;
-    for (int idx = blockIdx.x; idx < P.n_units; idx += gridDim.x) {
-      const int u = P.order[idx];
-      const int bh = u / P.nQ, qi = u - bh * P.nQ;
-      const int b = bh / P.H, h = bh - b * P.H;
-      const int row = (b * P.Hm + (P.Hm == 1 ? 0 : h)) * P.nQ + qi;
-      const int n = P.row_count[row];
-      if (n == 0) continue;
-      const int32_t* list = P.row_list + static_cast<size_t>(row) * P.nK;
-      if (lane == 0) {
-        bool ok = qn == 0 || wait(B_QEMPTY, (qn - 1) & 1);
+    Merge mg;
+    mg.init(P);
+    uint32_t i = 0;
+    Pair<uint32_t> qn{0, 0};
+    while (true) {
+      int k, t, row;
+      bool first, last;
+      const int s = mg.next(P, k, t, row, first, last);
+      if (s < 0) break;
+      const UnitInfo u = unit_of(P, blockIdx.x + k * gridDim.x);
+      if (first && lane == 0) {
+        bool ok = qn.get(s) == 0 || wait(B_QEMPTY0 + s, (qn.get(s) - 1) & 1);
         if (ok) {
-          mbar_arrive_expect_tx(bar(B_QFULL), C::TILE);
+          mbar_arrive_expect_tx(bar(B_QFULL0 + s), C::TILE);
 #pragma unroll
-          for (int s = 0; s < C::SLABS; ++s)
-            tma_load_4d(sQ + s * 16384, &tmQ, bar(B_QFULL), s * 64, h, qi * kTile, b);
+          for (int x = 0; x < C::SLABS; ++x)
+            tma_load_4d(sbase + C::OFF_Q + s * C::TILE + x * 16384, &tmQ, bar(B_QFULL0 + s),
+                        x * 64, u.h, u.qi * kTile, u.b);
         }
       }
-      ++qn;
-      for (int t = 0; t < n; ++t, ++it) {
-        if (aborted_all()) break;
-        const int e = list[t];
-        const int kj = e >> 2;
-        const int st = it % C::NST;
-        const uint32_t use = it / C::NST;
-        if (use > 0 && !wait_all(B_KVEMPTY0 + st, (use - 1) & 1)) break;
-        if (tile_partial(e, kj, P.nK, P.Skv)) {
-          const size_t base = static_cast<size_t>(b * P.Hm + (P.Hm == 1 ? 0 : h)) * P.Skv;
+      if (first) qn.set(s, qn.get(s) + 1);
+      const int e = P.row_list[static_cast<size_t>(row) * P.nK + t];
+      const int kj = e >> 2;
+      const int st = i & 1;
+      const uint32_t use = i >> 1;
+      if (use > 0 && !wait_all(B_KEMPTY0 + st, (use - 1) & 1)) break;
+      if (use > 0 && !wait_all(B_BEMPTY0 + st, (use - 1) & 1)) break;
+      if (tile_partial(e, kj, P.nK, P.Skv)) {
+        const size_t base = static_cast<size_t>(u.b * P.Hm + (P.Hm == 1 ? 0 : u.h)) * P.Skv;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int c = lane + 32 * i;
-            const int j = kj * kTile + c;
-            int4 v;
-            if (j < P.Skv) {
-              v.x = __ldg(P.bounds[0] + base + j);
-              v.y = __ldg(P.bounds[1] + base + j);
-              v.z = __ldg(P.bounds[2] + base + j);
-              v.w = __ldg(P.bounds[3] + base + j);
-            } else {
-              v = make_int4(0, 0x7fffffff, 0, 0);  // beyond the keys: hidden from every row
-            }
-            bnd[st * 128 + c] = v;
+        for (int x = 0; x < 4; ++x) {
+          const int c = lane + 32 * x;
+          const int j = kj * kTile + c;
+          int4 v;
+          if (j < P.Skv) {
+            v.x = __ldg(P.bounds[0] + base + j);
+            v.y = __ldg(P.bounds[1] + base + j);
+            v.z = __ldg(P.bounds[2] + base + j);
+            v.w = __ldg(P.bounds[3] + base + j);
+          } else {
+            v = make_int4(0, 0x7fffffff, 0, 0);  // beyond the keys: hidden from every row
           }
-        }
-        __syncwarp();
-        if (lane == 0) {
-          const uint32_t fb = bar(B_KVFULL0 + st);
-          mbar_arrive_expect_tx(fb, 2 * C::TILE);
-          const uint32_t sK = sbase + C::OFF_K + st * C::TILE;
-          const uint32_t sV = sbase + C::OFF_V + st * C::TILE;
-#pragma unroll
-          for (int s = 0; s < C::SLABS; ++s) {
-            tma_load_4d(sK + s * 16384, &tmK, fb, s * 64, h, kj * kTile, b);
-            tma_load_4d(sV + s * 16384, &tmV, fb, s * 64, h, kj * kTile, b);
-          }
+          bnd[st * 128 + c] = v;
         }
       }
-      if (aborted_all()) break;
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(B_KFULL0 + st), C::TILE);
+#pragma unroll
+        for (int x = 0; x < C::SLABS; ++x)
+          tma_load_4d(sbase + C::OFF_K + st * C::TILE + x * 16384, &tmK, bar(B_KFULL0 + st),
+                      x * 64, u.h, kj * kTile, u.b);
+      }
+      ++i;
     }
     // drain: every issued copy has landed before the CTA may exit
     if (lane == 0) {
-      for (uint32_t k = (it > (uint32_t)C::NST ? it - C::NST : 0); k < it; ++k)
-        mbar_wait(bar(B_KVFULL0 + k % C::NST), (k / C::NST) & 1, P.status);
-      if (qn > 0) mbar_wait(bar(B_QFULL), (qn - 1) & 1, P.status);
+      for (uint32_t x = (i > 2u ? i - 2u : 0u); x < i; ++x)
+        mbar_wait(bar(B_KFULL0 + (x & 1)), (x >> 1) & 1, P.status);
+      if (qn.v0 > 0) mbar_wait(bar(B_QFULL0), (qn.v0 - 1) & 1, P.status);
+      if (qn.v1 > 0) mbar_wait(bar(B_QFULL0 + 1), (qn.v1 - 1) & 1, P.status);
     }
-  } else if (warp == 5) {
+    __syncwarp();
+  } else if (warp == V_WARP) {
+    // ------------------------------------------------------------ V producer
+    // its own warp, so a V stage that is still in use never holds up K loads
+    if (lane == 0) {
+      Merge mg;
+      mg.init(P);
+      uint32_t i = 0;
+      while (true) {
+        int k, t, row;
+        bool first, last;
+        if (mg.next(P, k, t, row, first, last) < 0) break;
+        const UnitInfo u = unit_of(P, blockIdx.x + k * gridDim.x);
+        const int kj = P.row_list[static_cast<size_t>(row) * P.nK + t] >> 2;
+        const int st = i & 1;
+        const uint32_t use = i >> 1;
+        if (use > 0 && !wait(B_VEMPTY0 + st, (use - 1) & 1)) break;
+        mbar_arrive_expect_tx(bar(B_VFULL0 + st), C::TILE);
+#pragma unroll
+        for (int x = 0; x < C::SLABS; ++x)
+          tma_load_4d(sbase + C::OFF_V + st * C::TILE + x * 16384, &tmV, bar(B_VFULL0 + st),
+                      x * 64, u.h, kj * kTile, u.b);
+        ++i;
+      }
+      for (uint32_t x = (i > 2u ? i - 2u : 0u); x < i; ++x)
+        mbar_wait(bar(B_VFULL0 + (x & 1)), (x >> 1) & 1, P.status);
+    }
+    __syncwarp();
+  } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
-      uint32_t it = 0, qn = 0, un = 0;
-      auto issue_pv = [&](uint32_t jt, bool first) -> bool {
-        if (!wait(B_PFULL, jt & 1)) return false;
-        // O is overwritten by a unit's first PV: the previous epilogue must be done
-        if (first) {
-          if (un > 0 && !wait(B_OEMPTY, (un - 1) & 1)) return false;
-          ++un;
-        }
-        tc_fence_after();
-        const int st = jt % C::NST;
-        const uint32_t sV = sbase + C::OFF_V + st * C::TILE;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd = sdesc_sw128(sV + kk * 2048, 128 * 128, 1024);
-          mma_ts(tbase + C::T_O, tbase + C::T_P + kk * 8, bd, idPV, (!first || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(B_PVDONE));
-        mma_commit(bar(B_KVEMPTY0 + st));
-        return true;
-      };
-      for (int idx = blockIdx.x; idx < P.n_units; idx += gridDim.x) {
-        const int u = P.order[idx];
-        const int bh = u / P.nQ, qi = u - bh * P.nQ;
-        const int b = bh / P.H, h = bh - b * P.H;
-        const int row = (b * P.Hm + (P.Hm == 1 ? 0 : h)) * P.nQ + qi;
-        const int n = P.row_count[row];
-        if (n == 0) continue;
-        if (!wait(B_QFULL, qn & 1)) break;
-        ++qn;
-        bool ok = true;
-        for (int t = 0; t < n; ++t, ++it) {
-          const int st = it % C::NST;
-          const int sb = it & 1;
-          if (!wait(B_KVFULL0 + st, (it / C::NST) & 1)) { ok = false; break; }
-          if (it >= 2 && !wait(B_SEMPTY0 + sb, ((it >> 1) - 1) & 1)) { ok = false; break; }
+      Merge mg;
+      mg.init(P);
+      uint32_t i = 0;
+      Pair<uint32_t> js{0, 0}, jp{0, 0}, qn{0, 0}, un{0, 0}, pend_i{0, 0};
+      Pair<bool> pend{false, false}, pend_first{false, false};
+      bool ok = true;
+      // S of slot s for the next merged tile(s) of that slot; returns false on abort
+      auto issue_s_phase = [&](int want) -> bool {
+        while (true) {
+          const int s = mg.peek();
+          if (s < 0 || pend.get(s) || (want >= 0 && s != want)) return true;
+          int k, t, row;
+          bool first, last;
+          mg.next(P, k, t, row, first, last);
+          if (first) {
+            if (!wait(B_QFULL0 + s, qn.get(s) & 1)) return false;
+            qn.set(s, qn.get(s) + 1);
+          }
+          // S of this slot overwrites P of its previous tile: that PV must be done
+          if (js.get(s) > 0 && !wait(B_PVDONE0 + s, (js.get(s) - 1) & 1)) return false;
+          const int st = i & 1;
+          if (!wait(B_KFULL0 + st, (i >> 1) & 1)) return false;
           tc_fence_after();
+          const uint32_t sQ = sbase + C::OFF_Q + s * C::TILE;
           const uint32_t sK = sbase + C::OFF_K + st * C::TILE;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tbase + C::T_S + sb * 128, sdesc_sw128(sQ + koff, 16, 1024),
+            mma_ss(tbase + 128 * s, sdesc_sw128(sQ + koff, 16, 1024),
                    sdesc_sw128(sK + koff, 16, 1024), idS, kk > 0 ? 1u : 0u);
           }
-          mma_commit(bar(B_SFULL0 + sb));
-          if (t == n - 1) mma_commit(bar(B_QEMPTY));
-          if (t > 0 && !issue_pv(it - 1, t == 1)) { ok = false; break; }
+          mma_commit(bar(B_SFULL0 + s));
+          mma_commit(bar(B_KEMPTY0 + st));
+          if (last) mma_commit(bar(B_QEMPTY0 + s));
+          js.set(s, js.get(s) + 1);
+          pend.set(s, true);
+          pend_first.set(s, first);
+          pend_i.set(s, i);
+          ++i;
         }
-        if (!ok) break;
-        if (!issue_pv(it - 1, n == 1)) break;
+      };
+      auto issue_pv = [&](int s) -> bool {
+        if (!wait(B_PFULL0 + s, jp.get(s) & 1)) return false;
+        const bool first = pend_first.get(s);
+        if (first) {
+          // O of this slot is overwritten: its previous epilogue must be done
+          if (un.get(s) > 0 && !wait(B_OEMPTY0 + s, (un.get(s) - 1) & 1)) return false;
+          un.set(s, un.get(s) + 1);
+        }
+        const int st = pend_i.get(s) & 1;
+        if (!wait(B_VFULL0 + st, (pend_i.get(s) >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t sV = sbase + C::OFF_V + st * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tbase + 256 + 128 * s, tbase + 128 * s + kk * 8,
+                 sdesc_sw128(sV + kk * 2048, 128 * 128, 1024), idPV, (!first || kk > 0) ? 1u : 0u);
+        mma_commit(bar(B_PVDONE0 + s));
+        mma_commit(bar(B_VEMPTY0 + st));
+        jp.set(s, jp.get(s) + 1);
+        pend.set(s, false);
+        return true;
+      };
+      // prologue: the first S of each slot (merged order)
+      ok = issue_s_phase(-1);
+      // ping-pong: PV of slot 0 then its next S, PV of slot 1 then its next S,
+      // so one slot's softmax overlaps the other slot's MMAs
+      while (ok && (pend.v0 || pend.v1)) {
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          if (!ok) break;
+          if (pend.get(s) && !issue_pv(s)) { ok = false; break; }
+          if (!issue_s_phase(s)) { ok = false; break; }
+        }
       }
       mma_commit(bar(B_DRAIN));
       mbar_wait(bar(B_DRAIN), 0, P.status);
     }
     __syncwarp();
+  }  // warp 11: spare warp of the producer warpgroup, nothing to do
   } else {
     // ------------------------------------------------------------ softmax
-    const int r = tid;  // query row within the tile == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    uint32_t it = 0, un = 0;
-    for (int idx = blockIdx.x; idx < P.n_units; idx += gridDim.x) {
-      const int u = P.order[idx];
-      const int bh = u / P.nQ, qi = u - bh * P.nQ;
-      const int b = bh / P.H, h = bh - b * P.H;
-      const int row = (b * P.Hm + (P.Hm == 1 ? 0 : h)) * P.nQ + qi;
-      const int n = P.row_count[row];
-      const int32_t* list = P.row_list + static_cast<size_t>(row) * P.nK;
-      const int qrow = qi * kTile + r;
-      __nv_bfloat16* orow = P.o + b * P.o_stride[0] + static_cast<int64_t>(qrow) * P.o_stride[1] +
-                            h * P.o_stride[2];
-      float* lse_out = P.lse + (static_cast<size_t>(b) * P.H + h) * P.Sq + qrow;
-      if (n == 0) {
+    regs_increase<C::REGS_SOFTMAX>();
+    const int slot = warp >> 2;              // warpgroup = slot
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;       // query row within the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tbase + lane_off + 128 * slot;
+    const uint32_t tO = tbase + lane_off + 256 + 128 * slot;
+    Merge mg;
+    mg.init(P);
+    uint32_t i = 0, j = 0;  // merged tile index, this slot's tile index
+    bool ok = true;
+    for (int k = slot; ok; k += 2) {
+      const int idx = blockIdx.x + k * gridDim.x;
+      if (idx >= P.n_units) break;
+      const UnitInfo u = unit_of(P, idx);
+      const int qrow = u.qi * kTile + r;
+      __nv_bfloat16* orow = P.o + u.b * P.o_stride[0] + static_cast<int64_t>(qrow) * P.o_stride[1] +
+                            u.h * P.o_stride[2];
+      float* lse_out = P.lse + (static_cast<size_t>(u.b) * P.H + u.h) * P.Sq + qrow;
+      if (u.n == 0) {
         if (qrow < P.Sq) {
-          uint4 z = make_uint4(0, 0, 0, 0);
+          const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
           *lse_out = -INFINITY;
         }
         continue;
       }
-      float m = -INFINITY, l = 0.f;
-      bool ok = true;
-      for (int t = 0; t < n; ++t, ++it) {
-        const int e = list[t];
+      float m_used = -INFINITY, l = 0.f;  // running max (base-2 exponent domain) and sum
+      for (int t = 0; t < u.n; ++t, ++j) {
+        // the merged index of this tile: walk the merge past the other slot's tiles
+        int mk, mt, mrow;
+        bool mf, ml;
+        int ms;
+        while ((ms = mg.next(P, mk, mt, mrow, mf, ml)) != slot && ms >= 0) ++i;
+        const uint32_t mi = i++;
+        const int e = P.row_list[static_cast<size_t>(u.row) * P.nK + t];
         const int kj = e >> 2;
-        const int sb = it & 1;
-        if (!wait_all(B_SFULL0 + sb, (it >> 1) & 1)) { ok = false; break; }
+        const int st = mi & 1;
+        if (!wait_all(B_SFULL0 + slot, j & 1)) { ok = false; break; }
         tc_fence_after();
-        float s[128];
+        // the whole S row in one round trip: TMEM load latency (~670 cycles)
+        // does not depend on the width, so issue both halves, wait once
+        const bool partial = tile_partial(e, kj, P.nK, P.Skv);
+        float sv[128];
         {
-          uint32_t raw[32];
+          uint32_t* raw = reinterpret_cast<uint32_t*>(sv);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tbase + lane_off + C::T_S + sb * 128 + c * 32, raw);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(raw[i]);
-          }
+          for (int x = 0; x < 4; ++x) tmem_ld32(tS + 32 * x, raw + 32 * x);
+          if (partial && !wait_all(B_KFULL0 + st, (mi >> 1) & 1)) { ok = false; break; }
+          tmem_wait_ld();
         }
-        tc_fence_before();
-        mbar_arrive(bar(B_SEMPTY0 + sb));
-        if (tile_partial(e, kj, P.nK, P.Skv)) {
-          const int st = it % C::NST;
-          if (!wait_all(B_KVFULL0 + st, (it / C::NST) & 1)) { ok = false; break; }
+        if (partial) {
           const int4* bb = bnd + st * 128;
 #pragma unroll
           for (int c = 0; c < 128; ++c) {
             const int4 v = bb[c];
-            const bool hid = (v.x <= qrow && qrow < v.y) || (v.z <= qrow && qrow < v.w);
-            s[c] = hid ? -INFINITY : s[c];
+            const bool hd = (v.x <= qrow && qrow < v.y) || (v.z <= qrow && qrow < v.w);
+            sv[c] = hd ? -INFINITY : sv[c];
           }
         }
-        float mx = -INFINITY;
+        mbar_arrive(bar(B_BEMPTY0 + st));  // done with this stage's bounds
+        float mx8[8];
 #pragma unroll
-        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
-        const float m_new = fmaxf(m, mx * P.scale_log2);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = ex2(m - m_use);
-        float sum = 0.f;
-        uint32_t pk[64];
+        for (int x = 0; x < 8; ++x) mx8[x] = sv[x];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float p0 = ex2(fmaf(s[2 * c], P.scale_log2, -m_use));
-          const float p1 = ex2(fmaf(s[2 * c + 1], P.scale_log2, -m_use));
-          sum += p0 + p1;
-          pk[c] = pack_bf16(p0, p1);
-        }
-        l = l * alpha + sum;
-        if (t > 0) {
-          // the previous PV has finished: P may be overwritten and O is stable
-          if (!wait_all(B_PVDONE, (it - 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-          // TMEM loads/stores are warp-collective: the whole warp rescales
-          // if any of its rows needs it (alpha == 1 leaves a row unchanged)
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
-            uint32_t raw[32];
+        for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float m_tile = mx * P.scale_log2;
+        // lazy rescale: move the reference max only when it grows by more than
+        // 8 (factor 256); below that the unnormalised p stay within bf16/fp32
+        // range and the result is unchanged
+        const bool grow = m_tile > m_used + 8.f;
+        const float m_new = grow ? m_tile : m_used;
+        const float alpha = grow ? ex2(m_used - m_new) : 1.f;  // m_used = -inf gives 0
+        l *= alpha;
+        m_used = m_new;
+        const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
+        // p = exp2(s * scale*log2e - m) from the registers, packed to bf16 into
+        // the first 64 columns of S (the row was read whole above)
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              const uint32_t ta = tbase + lane_off + C::T_O + c * 32;
-              tmem_ld32(ta, raw);
-              tmem_wait_ld();
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t pk[16];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) raw[i] = __float_as_uint(__uint_as_float(raw[i]) * alpha);
-              tmem_st32(ta, raw);
-            }
+          for (int x = 0; x < 16; ++x) {
+            const float p0 = ex2(fmaf(sv[c4 * 32 + 2 * x], P.scale_log2, -m_ref));
+            const float p1 = ex2(fmaf(sv[c4 * 32 + 2 * x + 1], P.scale_log2, -m_ref));
+            sum4[x & 3] += p0 + p1;
+            pk[x] = pack_bf16(p0, p1);
           }
+          tmem_st16(tS + c4 * 16, pk);
         }
-        tmem_st32(tbase + lane_off + C::T_P, pk);
-        tmem_st32(tbase + lane_off + C::T_P + 32, pk + 32);
+        const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+        // rescale O by alpha (after P: the S registers are free by now).  O
+        // holds the PVs of the earlier tiles, all complete since S of this tile
+        // completed after them
+        if (t > 0 && __any_sync(0xffffffffu, grow)) {
+          uint32_t raw[D];
+#pragma unroll
+          for (int x = 0; x < D / 32; ++x) tmem_ld32(tO + 32 * x, raw + 32 * x);
+          tmem_wait_ld();
+#pragma unroll
+          for (int x = 0; x < D; ++x) raw[x] = __float_as_uint(__uint_as_float(raw[x]) * alpha);
+#pragma unroll
+          for (int x = 0; x < D / 32; ++x) tmem_st32(tO + 32 * x, raw + 32 * x);
+        }
+        l += sum;
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(B_PFULL));
-        m = m_new;
+        mbar_arrive(bar(B_PFULL0 + slot));
       }
       if (!ok) break;
-      // epilogue: O / l and LSE
-      if (!wait_all(B_PVDONE, (it - 1) & 1)) break;
+      // epilogue: O / l and LSE, after this unit's last PV
+      if (!wait_all(B_PVDONE0 + slot, (j - 1) & 1)) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint32_t raw[32];
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(tbase + lane_off + C::T_O + c * 32, raw);
+        tmem_ld32(tO + c * 32, raw);
         tmem_wait_ld();
         if (qrow < P.Sq) {
           uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = pack_bf16(__uint_as_float(raw[2 * i]) * inv, __uint_as_float(raw[2 * i + 1]) * inv);
+          for (int x = 0; x < 16; ++x)
+            w[x] = pack_bf16(__uint_as_float(raw[2 * x]) * inv, __uint_as_float(raw[2 * x + 1]) * inv);
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int x = 0; x < 4; ++x) dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
         }
       }
       if (qrow < P.Sq) {
-        const float m_use = (m == -INFINITY) ? 0.f : m;
-        *lse_out = l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
+        const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
+        *lse_out = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
       }
       tc_fence_before();
-      mbar_arrive(bar(B_OEMPTY));
-      ++un;
+      mbar_arrive(bar(B_OEMPTY0 + slot));
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tbase, C::T_COLS);
   }
@@ -421,9 +591,15 @@ static fm_status launch_fwd_d(const Plan& p, const fm_desc& desc, const TensorAr
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)
     return FM_ERR_CUDA;
+  {
+    // the setmaxnreg split must fit in the registers the block launches with
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return FM_ERR_CUDA;
+    if (fa.numRegs < C::MIN_LAUNCH_REGS) return FM_ERR_UNSUPPORTED;
+  }
   const int grid = P.n_units < num_sms() ? P.n_units : num_sms();
   prof_begin(K_FWD, s);
-  kern<<<grid, 192, C::SMEM, s>>>(P, tq, tk, tv);
+  kern<<<grid, C::THREADS, C::SMEM, s>>>(P, tq, tk, tv);
   prof_end(K_FWD, s);
   return cudaGetLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }

@@ -144,32 +144,24 @@ __global__ void __launch_bounds__(256) classify_cols_kernel(const int32_t* __res
 }
 
 // ------------------------------------------------------------------ order
-// Longest-first order of the units u = (b*H + h)*nT + t by cost
-// counts[b][hm][t] in [0, maxc], ties by u ascending: a counting sort
-// (histogram, scan in descending cost, stable scatter by one warp in u
-// order).  One CTA.
-__global__ void __launch_bounds__(1024) order_kernel(const int32_t* __restrict__ counts, int B,
-                                                     int H, int Hm, int nT, int maxc,
-                                                     int cache_counts, int32_t* order) {
+// Unit order: (b, h) ascending; within one (b, h) the nT units t by cost
+// counts[b][hm][t] in [0, maxc] descending, ties by t ascending (longest
+// first).  One CTA per (b, h): histogram, scan in descending cost, stable
+// scatter by one warp in t order.
+__global__ void __launch_bounds__(256) order_kernel(const int32_t* __restrict__ counts, int H,
+                                                    int Hm, int nT, int maxc, int32_t* order) {
   extern __shared__ int sh[];
-  int* hist = sh;                 // maxc + 1
-  int* cst = sh + maxc + 1;       // B*Hm*nT (when cached)
-  __shared__ int wsum[32];
+  int* hist = sh;             // maxc + 1
+  int* cst = sh + maxc + 1;   // nT costs of this (b, h)
+  __shared__ int wsum[8];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int U = B * H * nT;
-  const int nC = B * Hm * nT;
+  const int bh = blockIdx.x;
+  const int b = bh / H, h = bh - b * H;
+  const int32_t* src = counts + static_cast<size_t>(b * Hm + (Hm == 1 ? 0 : h)) * nT;
   for (int i = tid; i <= maxc; i += blockDim.x) hist[i] = 0;
-  if (cache_counts)
-    for (int i = tid; i < nC; i += blockDim.x) cst[i] = counts[i];
+  for (int t = tid; t < nT; t += blockDim.x) cst[t] = src[t];
   __syncthreads();
-  const int* cs = cache_counts ? cst : counts;
-  auto cost = [&](int u) {
-    const int b = u / (H * nT);
-    const int h = (u / nT) % H;
-    const int t = u % nT;
-    return cs[(b * Hm + (Hm == 1 ? 0 : h)) * nT + t];
-  };
-  for (int u = tid; u < U; u += blockDim.x) atomicAdd(&hist[cost(u)], 1);
+  for (int t = tid; t < nT; t += blockDim.x) atomicAdd(&hist[cst[t]], 1);
   __syncthreads();
   // exclusive scan over r = maxc - c (descending cost), each thread a segment
   const int n = maxc + 1;
@@ -186,35 +178,37 @@ __global__ void __launch_bounds__(1024) order_kernel(const int32_t* __restrict__
   if (lane == 31) wsum[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int x = (lane < (int)(blockDim.x >> 5)) ? wsum[lane] : 0;
+    const int nw = blockDim.x >> 5;
+    int x = lane < nw ? wsum[lane] : 0;
     int xi = x;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, xi, off);
       if (lane >= off) xi += y;
     }
-    wsum[lane] = xi - x;  // exclusive prefix of warp totals
+    if (lane < nw) wsum[lane] = xi - x;  // exclusive prefix of warp totals
   }
   __syncthreads();
   int run = wsum[warp] + incl - local;
   for (int r = r_lo; r < r_hi; ++r) {
     const int c = maxc - r;
-    const int h = hist[c];
+    const int hc = hist[c];
     hist[c] = run;
-    run += h;
+    run += hc;
   }
   __syncthreads();
   if (warp == 0) {
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int u0 = 0; u0 < U; u0 += 32) {
-      const int u = u0 + lane;
-      const bool valid = u < U;
-      const int c = valid ? cost(u) : -1;
+    int32_t* out = order + static_cast<size_t>(bh) * nT;
+    for (int t0 = 0; t0 < nT; t0 += 32) {
+      const int t = t0 + lane;
+      const bool valid = t < nT;
+      const int c = valid ? cst[t] : -1;
       const unsigned peers = __match_any_sync(0xffffffffu, c);
       int base = 0;
       if (valid) {
         base = hist[c];
-        order[base + __popc(peers & lt_mask)] = u;
+        out[base + __popc(peers & lt_mask)] = bh * nT + t;
       }
       __syncwarp();
       if (valid && lane == __ffs(peers) - 1) hist[c] = base + __popc(peers);
@@ -275,17 +269,14 @@ cudaError_t launch_order(const Plan& p, char* ws, int for_bwd, cudaStream_t s) {
   const int32_t* counts =
       reinterpret_cast<const int32_t*>(ws + (for_bwd ? p.L.col_count : p.L.row_count));
   int32_t* order = reinterpret_cast<int32_t*>(ws + (for_bwd ? p.L.bwd_order : p.L.fwd_order));
-  const size_t hist_bytes = static_cast<size_t>(maxc + 1) * 4;
-  const size_t cache_bytes = static_cast<size_t>(p.B) * p.Hm * nT * 4;
+  const size_t smem = static_cast<size_t>(maxc + 1 + nT) * 4;
   const size_t limit = 200 * 1024;
-  if (hist_bytes > limit) return cudaErrorInvalidValue;
-  const int cache = hist_bytes + cache_bytes <= limit ? 1 : 0;
-  const size_t smem = hist_bytes + (cache ? cache_bytes : 0);
+  if (smem > limit) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(limit));
   if (e != cudaSuccess) return e;
   prof_begin(K_ORDER, s);
-  order_kernel<<<1, 1024, smem, s>>>(counts, p.B, p.H, p.Hm, nT, maxc, cache, order);
+  order_kernel<<<p.B * p.H, 256, smem, s>>>(counts, p.H, p.Hm, nT, maxc, order);
   prof_end(K_ORDER, s);
   return cudaGetLastError();
 }

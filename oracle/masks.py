@@ -137,10 +137,12 @@ def col_lists(table: np.ndarray):
 
 def unit_order(counts: np.ndarray, H: int) -> np.ndarray:
     """Work units (b, h, tile), numbered u = (b*H + h)*nT + tile, ordered by
-    cost (non-empty tiles of the unit's row or column) descending, ties by u
-    ascending: the longest-processing-time-first order that balances units by
-    work rather than by position (the sparsity-aware balancing named on the
-    FlashMask-3 page, «Ключевые факты», applied to one GPU's work units).
+    (b, h) ascending and, within one (b, h), by cost (non-empty tiles of the
+    unit's row or column) descending, ties by tile ascending.  Within a head
+    this is the longest-processing-time-first order that balances units by
+    work rather than by position (the sparsity-aware balancing the FlashMask-3
+    page names in «Ключевые факты», applied to one GPU's work units); keeping
+    heads in order makes the units that run at the same time share one head.
     ``counts`` is [B][Hm][nT]; head h reads mask head 0 if Hm == 1 else h."""
     B, Hm, nT = counts.shape
     units = []
@@ -149,9 +151,9 @@ def unit_order(counts: np.ndarray, H: int) -> np.ndarray:
             hm = 0 if Hm == 1 else h
             for t in range(nT):
                 u = (b * H + h) * nT + t
-                units.append((-int(counts[b, hm, t]), u))
+                units.append(((b, h), -int(counts[b, hm, t]), u))
     units.sort()
-    return np.array([u for _, u in units], dtype=np.int32)
+    return np.array([u for _, _, u in units], dtype=np.int32)
 
 
 # --------------------------------------------------------------------------

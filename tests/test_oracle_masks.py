@@ -236,10 +236,13 @@ def test_lists_and_unit_order():
         assert ks == sorted(ks)
         assert all(t[bb, hm, qi, k] == c for k, c in lst)
     order = om.unit_order(rc, H)
-    assert sorted(order.tolist()) == list(range(H * rc.shape[2]))
-    cost = [rc[0, 0, u % rc.shape[2]] for u in order]
+    nT = rc.shape[2]
+    assert sorted(order.tolist()) == list(range(H * nT))
+    cost = [rc[0, 0, u % nT] for u in order]
+    head = [u // nT for u in order]
     for a in range(len(order) - 1):
-        assert cost[a] > cost[a + 1] or (cost[a] == cost[a + 1] and order[a] < order[a + 1])
+        assert head[a] < head[a + 1] or (head[a] == head[a + 1] and (
+            cost[a] > cost[a + 1] or (cost[a] == cost[a + 1] and order[a] < order[a + 1])))
 
 
 # ---------------------------------------------------------------- localisation
