@@ -306,8 +306,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           const uint32_t sQ = sbase + C::OFF_Q + st * C::TILE;
           const uint32_t sDO = sbase + C::OFF_DO + st * C::TILE;
           if (!wait(C_QFULL0 + st, (it >> 1) & 1)) { ok = false; break; }
-          // S^T into region A once the previous dV has read P^T from it
-          if (it > 0 && !wait(C_DVDONE, (it - 1) & 1)) { ok = false; break; }
+          // S^T overwrites P^T of the previous tile in region A: the dV that
+          // reads it was issued earlier, and MMAs issued by this thread run in
+          // issue order
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -337,7 +338,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             mma_ts(tbase + C::T_DV, tbase + C::T_A + acol,
                    sdesc_sw128(sDO + kk * 2048, 16384, 1024), idKB, (t > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(bar(C_DVDONE));
           // dK += dS^T Q and dQ = dS K once dS^T is in smem
           if (!wait(C_DSREADY, it & 1)) { ok = false; break; }
           tc_fence_after();
@@ -381,6 +381,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if constexpr (D == 128) tmem_ld64(tbase + lane_off + C::T_B + half * (D / 2), raw);
       else tmem_ld32(tbase + lane_off + C::T_B + half * (D / 2), raw);
       tmem_wait_ld();
+      // region B may be reused (by the next dP^T) as soon as it has been read
+      tc_fence_before();
+      mbar_arrive(bar(C_DQEMPTY));
       if (qrow < P.Sq) {
 #pragma unroll
         for (int i = 0; i < D / 8; ++i) {
@@ -391,8 +394,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           atomicAdd(reinterpret_cast<float4*>(dst + 4 * i), v);
         }
       }
-      tc_fence_before();
-      mbar_arrive(bar(C_DQEMPTY));
       return true;
     };
     bool ok = true;
@@ -507,38 +508,35 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
       if (!ok) break;
       if (!drain_dq(it - 1, b, h, prev_qi)) { ok = false; break; }
-      // ---- epilogue: dV and scale * dK, this thread's half of the columns
+      // ---- epilogue: dV and scale * dK, this thread's half of the columns;
+      // both are read from TMEM first so the next unit's MMAs may start
       if (!wait_all(C_ACCFULL, un & 1)) { ok = false; break; }
       tc_fence_after();
-      uint32_t raw[32];
+      uint32_t rv[D / 2], rk[D / 2];
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        tmem_ld32(tbase + lane_off + C::T_DV + half * (D / 2) + c * 32, raw);
-        tmem_wait_ld();  // (once per unit: not on the per-tile path)
-        if (key < P.Skv) {
-          uint4* dst = reinterpret_cast<uint4*>(dv_row + c * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(pack_bf16(__uint_as_float(raw[8 * i + 0]), __uint_as_float(raw[8 * i + 1])),
-                                pack_bf16(__uint_as_float(raw[8 * i + 2]), __uint_as_float(raw[8 * i + 3])),
-                                pack_bf16(__uint_as_float(raw[8 * i + 4]), __uint_as_float(raw[8 * i + 5])),
-                                pack_bf16(__uint_as_float(raw[8 * i + 6]), __uint_as_float(raw[8 * i + 7])));
-        }
-        tmem_ld32(tbase + lane_off + C::T_DK + half * (D / 2) + c * 32, raw);
-        tmem_wait_ld();
-        if (key < P.Skv) {
-          uint4* dst = reinterpret_cast<uint4*>(dk_row + c * 32);
-          const float sc = P.scale;
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(pack_bf16(__uint_as_float(raw[8 * i + 0]) * sc, __uint_as_float(raw[8 * i + 1]) * sc),
-                                pack_bf16(__uint_as_float(raw[8 * i + 2]) * sc, __uint_as_float(raw[8 * i + 3]) * sc),
-                                pack_bf16(__uint_as_float(raw[8 * i + 4]) * sc, __uint_as_float(raw[8 * i + 5]) * sc),
-                                pack_bf16(__uint_as_float(raw[8 * i + 6]) * sc, __uint_as_float(raw[8 * i + 7]) * sc));
-        }
+        tmem_ld32(tbase + lane_off + C::T_DV + half * (D / 2) + c * 32, rv + 32 * c);
+        tmem_ld32(tbase + lane_off + C::T_DK + half * (D / 2) + c * 32, rk + 32 * c);
       }
+      tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(bar(C_ACCEMPTY));
+      if (key < P.Skv) {
+        const float sc = P.scale;
+        uint4* dv_dst = reinterpret_cast<uint4*>(dv_row);
+        uint4* dk_dst = reinterpret_cast<uint4*>(dk_row);
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) {
+          dv_dst[i] = make_uint4(pack_bf16(__uint_as_float(rv[8 * i + 0]), __uint_as_float(rv[8 * i + 1])),
+                                 pack_bf16(__uint_as_float(rv[8 * i + 2]), __uint_as_float(rv[8 * i + 3])),
+                                 pack_bf16(__uint_as_float(rv[8 * i + 4]), __uint_as_float(rv[8 * i + 5])),
+                                 pack_bf16(__uint_as_float(rv[8 * i + 6]), __uint_as_float(rv[8 * i + 7])));
+          dk_dst[i] = make_uint4(pack_bf16(__uint_as_float(rk[8 * i + 0]) * sc, __uint_as_float(rk[8 * i + 1]) * sc),
+                                 pack_bf16(__uint_as_float(rk[8 * i + 2]) * sc, __uint_as_float(rk[8 * i + 3]) * sc),
+                                 pack_bf16(__uint_as_float(rk[8 * i + 4]) * sc, __uint_as_float(rk[8 * i + 5]) * sc),
+                                 pack_bf16(__uint_as_float(rk[8 * i + 6]) * sc, __uint_as_float(rk[8 * i + 7]) * sc));
+        }
+      }
       ++un;
     }
   }

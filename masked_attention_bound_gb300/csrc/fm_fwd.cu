@@ -352,8 +352,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             if (!wait(B_QFULL0 + s, qn.get(s) & 1)) return false;
             qn.set(s, qn.get(s) + 1);
           }
-          // S of this slot overwrites P of its previous tile: that PV must be done
-          if (js.get(s) > 0 && !wait(B_PVDONE0 + s, (js.get(s) - 1) & 1)) return false;
+          // S of this slot overwrites P of its previous tile; MMAs issued by this
+          // thread run in issue order, so the PV that reads P is done with it first
           const int st = i & 1;
           if (!wait(B_KFULL0 + st, (i >> 1) & 1)) return false;
           tc_fence_after();
@@ -403,11 +403,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       // so one slot's softmax overlaps the other slot's MMAs
       while (ok && (pend.v0 || pend.v1)) {
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          if (!ok) break;
-          if (pend.get(s) && !issue_pv(s)) { ok = false; break; }
-          if (!issue_s_phase(s)) { ok = false; break; }
-        }
+        for (int s = 0; s < 2; ++s)
+          if (ok && pend.get(s) && !issue_pv(s)) ok = false;
+        if (ok && !issue_s_phase(-1)) ok = false;
       }
       mma_commit(bar(B_DRAIN));
       mbar_wait(bar(B_DRAIN), 0, P.status);
@@ -530,31 +528,28 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         mbar_arrive(bar(B_PFULL0 + slot));
       }
       if (!ok) break;
-      // epilogue: O / l and LSE, after this unit's last PV
+      // epilogue: O / l and LSE, after this unit's last PV.  O is read from
+      // TMEM first and released, so the slot's next unit may overwrite it
       if (!wait_all(B_PVDONE0 + slot, (j - 1) & 1)) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint32_t raw[32];
+      uint32_t ro[D];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(tO + c * 32, raw);
-        tmem_wait_ld();
-        if (qrow < P.Sq) {
-          uint32_t w[16];
-#pragma unroll
-          for (int x = 0; x < 16; ++x)
-            w[x] = pack_bf16(__uint_as_float(raw[2 * x]) * inv, __uint_as_float(raw[2 * x + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int x = 0; x < 4; ++x) dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
-        }
-      }
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + c * 32, ro + 32 * c);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(B_OEMPTY0 + slot));
       if (qrow < P.Sq) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int x = 0; x < D / 8; ++x)
+          dst[x] = make_uint4(pack_bf16(__uint_as_float(ro[8 * x + 0]) * inv, __uint_as_float(ro[8 * x + 1]) * inv),
+                              pack_bf16(__uint_as_float(ro[8 * x + 2]) * inv, __uint_as_float(ro[8 * x + 3]) * inv),
+                              pack_bf16(__uint_as_float(ro[8 * x + 4]) * inv, __uint_as_float(ro[8 * x + 5]) * inv),
+                              pack_bf16(__uint_as_float(ro[8 * x + 6]) * inv, __uint_as_float(ro[8 * x + 7]) * inv));
         const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
         *lse_out = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
       }
-      tc_fence_before();
-      mbar_arrive(bar(B_OEMPTY0 + slot));
     }
   }
 
