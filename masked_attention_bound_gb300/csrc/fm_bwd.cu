@@ -370,12 +370,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int c0 = half * 64;           // this thread's 64 of the 128 q columns
     uint32_t it = 0, un = 0;
-    // dQ tile drain: q row r, columns [half*D/2, half*D/2 + D/2) of region B
+    // dQ tile drain.  Thread r holds q row r, columns [half*D/2, +D/2) of the
+    // tile in region B.  Straight from TMEM each fp32 atomic of a warp would
+    // touch 32 different rows (16 bytes each); instead the warp transposes
+    // 32 x 32 blocks through a 4 KB patch of the dS^T buffer so that every
+    // reduction instruction covers four rows x 128 contiguous bytes.  The
+    // patch is the one this warp later fills with its own dS^T rows, and the
+    // buffer is idle here (the tile's dK/dQ MMAs have finished with it), so
+    // no other warp is involved.
+    const uint32_t patch = sDS + half * 16384 + quarter * 4096;
     auto drain_dq = [&](uint32_t jt, int b, int h, int qi) -> bool {
       if (!wait_all(C_DQFULL, jt & 1)) return false;
       tc_fence_after();
-      const int qrow = qi * kTile + r;
-      float* dst = P.dq_acc + ((static_cast<size_t>(b) * P.H + h) * P.Sq + qrow) * D + half * (D / 2);
       // this thread's D/2 columns in one TMEM round trip
       uint32_t raw[D / 2];
       if constexpr (D == 128) tmem_ld64(tbase + lane_off + C::T_B + half * (D / 2), raw);
@@ -384,15 +390,36 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       // region B may be reused (by the next dP^T) as soon as it has been read
       tc_fence_before();
       mbar_arrive(bar(C_DQEMPTY));
-      if (qrow < P.Sq) {
+      const int row0 = qi * kTile + quarter * 32;  // first q row of this warp
+      float* acc_bh = P.dq_acc + (static_cast<size_t>(b) * P.H + h) * P.Sq * D + half * (D / 2);
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-          const float4 v = make_float4(__uint_as_float(raw[4 * i]) * P.scale,
-                                       __uint_as_float(raw[4 * i + 1]) * P.scale,
-                                       __uint_as_float(raw[4 * i + 2]) * P.scale,
-                                       __uint_as_float(raw[4 * i + 3]) * P.scale);
-          atomicAdd(reinterpret_cast<float4*>(dst + 4 * i), v);
+      for (int c = 0; c < D / 64; ++c) {  // 32-column blocks
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t chunk = static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7);
+          const int e = c * 32 + j * 4;
+          st_shared_v4(patch + lane * 128 + chunk * 16,
+                       __float_as_uint(__uint_as_float(raw[e]) * P.scale),
+                       __float_as_uint(__uint_as_float(raw[e + 1]) * P.scale),
+                       __float_as_uint(__uint_as_float(raw[e + 2]) * P.scale),
+                       __float_as_uint(__uint_as_float(raw[e + 3]) * P.scale));
         }
+        __syncwarp();
+        const int j = lane & 7;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rl = i * 4 + (lane >> 3);  // row within the warp's 32
+          const uint32_t chunk = static_cast<uint32_t>(j) ^ static_cast<uint32_t>(rl & 7);
+          float4 v;
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                       : "r"(patch + rl * 128 + chunk * 16));
+          if (row0 + rl < P.Sq)
+            atomicAdd(reinterpret_cast<float4*>(acc_bh + static_cast<size_t>(row0 + rl) * D +
+                                                c * 32 + j * 4),
+                      v);
+        }
+        __syncwarp();
       }
       return true;
     };
