@@ -69,7 +69,8 @@ typedef struct {
  * nQ = ceil(Sq/128), nK = ceil(Skv/128).  List entries are
  * (tile_index << 2) | class with class 1 = PARTIAL, 2 = FULL. */
 typedef struct {
-  size_t status;     /* int32[4]: [0] device status bits, [1..3] scheduler counters  */
+  size_t status;     /* int32[4]: [0] device status bits, [1] unused, [2..3] uint64
+                        count of mask slots asked for (forward)                    */
   size_t summary;    /* int32 [B][Hm][nK][8]: min/max of LTS, LTE, UTS, UTE per k-block */
   size_t table;      /* uint8 [B][Hm][nQ][nK]: 0 EMPTY, 1 PARTIAL, 2 FULL           */
   size_t row_count;  /* int32 [B][Hm][nQ]: non-empty tiles per q-tile row             */
@@ -78,6 +79,13 @@ typedef struct {
   size_t col_list;   /* int32 [B][Hm][nK][nQ]: ascending q-tiles of each column       */
   size_t fwd_order;  /* int32 [B*H*nQ]: forward units u=(b*H+h)*nQ+qi, longest first  */
   size_t bwd_order;  /* int32 [B*H*nK]: backward units u=(b*H+h)*nK+kj, longest first */
+  size_t row_mask;   /* int32 [B][Hm][nQ]: first visibility-mask slot of the row's partial
+                        tiles (consecutive in list order), -1 if none (forward only)  */
+  size_t masks;      /* uint8 [cap][128][16], cap = min(B*Hm*nQ*nK, 65536): per partial
+                        tile (and the ragged last k-tile) 128 rows of 128 column bits,
+                        bit c of 32-bit word w = column 32w+c, set = hidden (forward
+                        only).  Rows whose tiles do not fit get row_mask -1 and the
+                        forward kernel builds their bits itself                    */
   size_t delta;      /* float [B][H][nQ*128]: D_i = dO_i . O_i, 0 past Sq (backward)  */
   size_t lse_log2;   /* float [B][H][nQ*128]: LSE_i * log2(e), +inf for rows that see
                         no key and past Sq (backward only)                          */
@@ -129,9 +137,12 @@ fm_status fm_bwd(const fm_desc* desc, const void* q, const void* k, const void* 
  * counterpart there.  Same arguments and results as fm_fwd, without `ws`:
  * the scratch lives in a fixed array of FM_STATIC_SCRATCH_BYTES in device
  * memory that belongs to the library image, so every GPU that loads the
- * library keeps those bytes until the process exits.  Problems whose
- * fm_workspace_size(desc, 0) exceeds FM_STATIC_SCRATCH_BYTES are rejected
- * with FM_ERR_WORKSPACE before anything is enqueued.  The first call on a
+ * library keeps those bytes until the process exits.  The visibility-mask
+ * region gets what the other regions leave of the array (possibly nothing;
+ * the forward kernel then builds the partial tiles' bits itself: slower,
+ * same results); problems whose other regions alone exceed
+ * FM_STATIC_SCRATCH_BYTES are rejected with FM_ERR_WORKSPACE before anything
+ * is enqueued.  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress, with
  * that device current); make that first call before any stream capture.
  * The function allocates nothing (no cudaMalloc, cudaFree or allocating
@@ -173,7 +184,8 @@ fm_status fm_localize(const int32_t* bounds, int B, int Hm, int Skv,
  * kernel id the summed device time in milliseconds and the launch count into
  * total_ms[0..n) and launches[0..n) (either may be NULL), and clears the
  * record.  Kernel ids: 0 block summary, 1 classify, 2 unit order,
- * 3 localize, 4 forward, 5 backward preprocess, 6 backward, 7 dQ convert;
+ * 3 localize, 4 forward, 5 backward preprocess, 6 backward, 7 dQ convert,
+ * 8 partial-tile visibility masks;
  * fm_kernel_name(id) names them.  At most 65536 launches are recorded per
  * read; later launches are counted but not timed. */
 fm_status fm_profile_enable(int on);

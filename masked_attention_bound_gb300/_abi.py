@@ -28,7 +28,7 @@ class FmDesc(ctypes.Structure):
 class FmWsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status", "summary", "table", "row_count", "row_list", "col_count", "col_list",
-        "fwd_order", "bwd_order", "delta", "lse_log2", "dq_acc", "total")]
+        "fwd_order", "bwd_order", "row_mask", "masks", "delta", "lse_log2", "dq_acc", "total")]
 
 
 class FMError(RuntimeError):
@@ -66,7 +66,7 @@ SIGNATURES = {
     "fm_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
-KERNEL_IDS = 8
+KERNEL_IDS = 9
 
 
 def lib():

@@ -26,7 +26,7 @@ static bool strides_ok(const int64_t* st) {
   return true;
 }
 
-fm_status make_plan(const fm_desc* desc, int for_bwd, Plan* p) {
+fm_status make_plan(const fm_desc* desc, int for_bwd, Plan* p, size_t limit) {
   if (!desc || !p) return FM_ERR_INVALID;
   const fm_desc& D = *desc;
   if (D.B < 1 || D.H < 1 || D.Sq < 1 || D.Skv < 1 || D.d < 1) return FM_ERR_INVALID;
@@ -53,6 +53,21 @@ fm_status make_plan(const fm_desc* desc, int for_bwd, Plan* p) {
   L.col_list = take(BHm * p->nK * p->nQ * 4);
   L.fwd_order = take(BH * p->nQ * 4);
   L.bwd_order = take(BH * p->nK * 4);
+  if (!for_bwd) {
+    // the mask region comes last and takes what the limit leaves, up to one
+    // slot per tile and kMaxMaskTiles slots
+    L.row_mask = take(BHm * p->nQ * 4);
+    size_t cap = BHm * p->nQ * p->nK;
+    if (cap > static_cast<size_t>(kMaxMaskTiles)) cap = kMaxMaskTiles;
+    const size_t room = limit > off ? (limit - off) / kMaskBytes : 0;
+    if (cap > room) cap = room;
+    p->mask_cap = static_cast<int>(cap);
+    L.masks = take(cap * kMaskBytes);
+  } else {
+    p->mask_cap = 0;
+    L.row_mask = 0;
+    L.masks = 0;
+  }
   if (for_bwd) {
     L.delta = take(BH * p->nQ * kTile * 4);
     L.lse_log2 = take(BH * p->nQ * kTile * 4);
@@ -82,6 +97,8 @@ static fm_status run_plan(const Plan& p, const int32_t* lts, const int32_t* lte,
   if (cudaMemsetAsync(ws + p.L.status, 0, 16, s) != cudaSuccess) return FM_ERR_CUDA;
   if (launch_summary(p, lts, lte, uts, ute, ws, s) != cudaSuccess) return FM_ERR_CUDA;
   if (launch_classify(p, ws, for_bwd, s) != cudaSuccess) return FM_ERR_CUDA;
+  if (!for_bwd && launch_tile_masks(p, lts, lte, uts, ute, ws, s) != cudaSuccess)
+    return FM_ERR_CUDA;
   if (launch_order(p, ws, for_bwd, s) != cudaSuccess) return FM_ERR_CUDA;
   return FM_OK;
 }

@@ -69,6 +69,8 @@ struct FwdParams {
   const int32_t* row_count;
   const int32_t* row_list;
   const int32_t* order;
+  const int32_t* row_mask;  // first visibility-mask slot of a row's partial tiles, -1: none
+  const uint8_t* masks;     // 2 KB per slot: 128 rows x 128 column bits, set = hidden
   __nv_bfloat16* o;
   int64_t o_stride[3];
   float* lse;
@@ -243,6 +245,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     mg.init(P);
     uint32_t i = 0;
     Pair<uint32_t> qn{0, 0};
+    Pair<int> mbase{-1, -1}, mord{0, 0};  // per slot: the unit's first mask slot, partials so far
     while (true) {
       int k, t, row;
       bool first, last;
@@ -259,34 +262,62 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                         x * 64, u.h, u.qi * kTile, u.b);
         }
       }
-      if (first) qn.set(s, qn.get(s) + 1);
+      if (first) {
+        qn.set(s, qn.get(s) + 1);
+        mbase.set(s, P.row_mask[u.row]);
+        mord.set(s, 0);
+      }
       const int e = P.row_list[static_cast<size_t>(row) * P.nK + t];
       const int kj = e >> 2;
       const int st = i & 1;
       const uint32_t use = i >> 1;
       if (use > 0 && !wait_all(B_KEMPTY0 + st, (use - 1) & 1)) break;
       if (use > 0 && !wait_all(B_BEMPTY0 + st, (use - 1) & 1)) break;
-      if (tile_partial(e, kj, P.nK, P.Skv)) {
+      const bool partial = tile_partial(e, kj, P.nK, P.Skv);
+      int mslot = -1;  // precomputed bit mask of this tile, if any
+      if (partial && mbase.get(s) >= 0) {
+        mslot = mbase.get(s) + mord.get(s);
+        mord.set(s, mord.get(s) + 1);
+      }
+      if (partial && mslot < 0) {
+        // no precomputed mask for this tile: build its bits here from the
+        // bounds. Lane l holds columns l, l+32, l+64, l+96, so ballot x over
+        // the lanes is word x of a row; lane (r mod 32) keeps row r's words.
         const size_t base = static_cast<size_t>(u.b * P.Hm + (P.Hm == 1 ? 0 : u.h)) * P.Skv;
+        int4 v[4];
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
-          const int c = lane + 32 * x;
-          const int j = kj * kTile + c;
-          int4 v;
+          const int j = kj * kTile + lane + 32 * x;
           if (j < P.Skv) {
-            v.x = __ldg(P.bounds[0] + base + j);
-            v.y = __ldg(P.bounds[1] + base + j);
-            v.z = __ldg(P.bounds[2] + base + j);
-            v.w = __ldg(P.bounds[3] + base + j);
+            v[x].x = __ldg(P.bounds[0] + base + j);
+            v[x].y = __ldg(P.bounds[1] + base + j);
+            v[x].z = __ldg(P.bounds[2] + base + j);
+            v[x].w = __ldg(P.bounds[3] + base + j);
           } else {
-            v = make_int4(0, 0x7fffffff, 0, 0);  // beyond the keys: hidden from every row
+            v[x] = make_int4(0, 0x7fffffff, 0, 0);  // beyond the keys: hidden from every row
           }
-          bnd[st * 128 + c] = v;
+        }
+        uint4* rows = reinterpret_cast<uint4*>(bnd + st * 128);
+        for (int g = 0; g < 4; ++g) {
+          uint4 mine = make_uint4(0u, 0u, 0u, 0u);
+          for (int rr = 0; rr < 32; ++rr) {
+            const int qrow = u.qi * kTile + g * 32 + rr;
+            uint32_t w[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+              w[x] = __ballot_sync(0xffffffffu, (v[x].x <= qrow && qrow < v[x].y) ||
+                                                    (v[x].z <= qrow && qrow < v[x].w));
+            if (lane == rr) mine = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          rows[g * 32 + lane] = mine;
         }
       }
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(B_KFULL0 + st), C::TILE);
+        mbar_arrive_expect_tx(bar(B_KFULL0 + st), C::TILE + (mslot >= 0 ? kMaskBytes : 0));
+        if (mslot >= 0)
+          bulk_load(smem_u32(bnd + st * 128), P.masks + static_cast<size_t>(mslot) * kMaskBytes,
+                    kMaskBytes, bar(B_KFULL0 + st));
 #pragma unroll
         for (int x = 0; x < C::SLABS; ++x)
           tma_load_4d(sbase + C::OFF_K + st * C::TILE + x * 16384, &tmK, bar(B_KFULL0 + st),
@@ -467,15 +498,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           tmem_wait_ld();
         }
         if (partial) {
-          const int4* bb = bnd + st * 128;
+          // this row's 128 column bits (set = hidden), one 16-byte load
+          const uint4 mw = reinterpret_cast<const uint4*>(bnd + st * 128)[r];
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const int4 v = bb[c];
-            const bool hd = (v.x <= qrow && qrow < v.y) || (v.z <= qrow && qrow < v.w);
-            sv[c] = hd ? -INFINITY : sv[c];
+          for (int c = 0; c < 32; ++c) {
+            sv[c] = ((mw.x >> c) & 1u) ? -INFINITY : sv[c];
+            sv[c + 32] = ((mw.y >> c) & 1u) ? -INFINITY : sv[c + 32];
+            sv[c + 64] = ((mw.z >> c) & 1u) ? -INFINITY : sv[c + 64];
+            sv[c + 96] = ((mw.w >> c) & 1u) ? -INFINITY : sv[c + 96];
           }
         }
-        mbar_arrive(bar(B_BEMPTY0 + st));  // done with this stage's bounds
+        mbar_arrive(bar(B_BEMPTY0 + st));  // done with this stage's mask bits
         float mx8[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) mx8[x] = sv[x];
@@ -578,6 +611,8 @@ static fm_status launch_fwd_d(const Plan& p, const fm_desc& desc, const TensorAr
   P.row_count = reinterpret_cast<const int32_t*>(ws + p.L.row_count);
   P.row_list = reinterpret_cast<const int32_t*>(ws + p.L.row_list);
   P.order = reinterpret_cast<const int32_t*>(ws + p.L.fwd_order);
+  P.row_mask = reinterpret_cast<const int32_t*>(ws + p.L.row_mask);
+  P.masks = reinterpret_cast<const uint8_t*>(ws + p.L.masks);
   P.o = static_cast<__nv_bfloat16*>(t.o_out);
   for (int i = 0; i < 3; ++i) P.o_stride[i] = desc.o_stride[i];
   P.lse = t.lse_out;

@@ -10,6 +10,8 @@ namespace fm {
 
 constexpr int kTile = 128;            // q-tile and k-tile edge
 constexpr int kMaxChunks = 128;       // fm_localize chunk limit
+constexpr int kMaxMaskTiles = 65536;  // partial tiles with a precomputed bit mask
+constexpr int kMaskBytes = 128 * 16;  // 128 rows x 128 column bits
 
 enum : int { CLS_EMPTY = 0, CLS_PARTIAL = 1, CLS_FULL = 2 };
 
@@ -17,17 +19,23 @@ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 struct Plan {
   int B, H, Hm, Sq, Skv, d, nQ, nK;
+  int mask_cap;  // forward: slots in the visibility-mask region
   fm_ws_layout L;
 };
 
 // Validates the description (shapes and strides) and computes the layout.
-fm_status make_plan(const fm_desc* desc, int for_bwd, Plan* p);
+// limit: the most bytes the forward layout may take; the visibility-mask
+// region shrinks to fit (rows without slots fall back to bits built in the
+// forward kernel).  Other regions do not shrink.
+fm_status make_plan(const fm_desc* desc, int for_bwd, Plan* p, size_t limit = SIZE_MAX);
 
 // Mask analysis kernels (fm_mask.cu).
 cudaError_t launch_summary(const Plan& p, const int32_t* lts, const int32_t* lte,
                            const int32_t* uts, const int32_t* ute, char* ws, cudaStream_t s);
 cudaError_t launch_classify(const Plan& p, char* ws, int for_bwd, cudaStream_t s);
 cudaError_t launch_order(const Plan& p, char* ws, int for_bwd, cudaStream_t s);
+cudaError_t launch_tile_masks(const Plan& p, const int32_t* lts, const int32_t* lte,
+                              const int32_t* uts, const int32_t* ute, char* ws, cudaStream_t s);
 
 struct ChunkMap {
   int n;
@@ -55,7 +63,7 @@ int num_sms();
 
 // Kernel ids for the timing hooks (fm_profile_*).
 enum KernelId : int { K_SUMMARY = 0, K_CLASSIFY, K_ORDER, K_LOCALIZE, K_FWD, K_BWD_PRE, K_BWD,
-                      K_DQ_CONVERT, K_COUNT };
+                      K_DQ_CONVERT, K_TILE_MASKS, K_COUNT };
 void prof_begin(int id, cudaStream_t s);
 void prof_end(int id, cudaStream_t s);
 

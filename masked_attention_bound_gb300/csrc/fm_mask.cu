@@ -84,10 +84,17 @@ __device__ __forceinline__ void load_summary(const int32_t* p, int* s) {
 
 // One warp per (bh, q-tile): writes the table row and the ascending list of
 // non-empty k-tiles, compacted with a ballot so the order is preserved.
+// It also counts the row's tiles that take the element-wise path (class
+// PARTIAL, or the ragged last key tile) and reserves that many consecutive
+// slots of the visibility-mask region (row_mask = first slot, -1 if none or
+// if the region is full: the forward then builds those tiles' bits itself).
 __global__ void __launch_bounds__(256) classify_rows_kernel(const int32_t* __restrict__ summary,
                                                             int nBH, int nQ, int nK, int Sq,
-                                                            uint8_t* table, int32_t* row_count,
-                                                            int32_t* row_list) {
+                                                            int Skv, uint8_t* table,
+                                                            int32_t* row_count,
+                                                            int32_t* row_list, int32_t* row_mask,
+                                                            unsigned long long* slot_counter,
+                                                            int mask_cap) {
   const int lane = threadIdx.x & 31;
   const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (w >= nBH * nQ) return;
@@ -97,7 +104,8 @@ __global__ void __launch_bounds__(256) classify_rows_kernel(const int32_t* __res
   uint8_t* tab = table + static_cast<size_t>(w) * nK;
   int32_t* lst = row_list + static_cast<size_t>(w) * nK;
   const unsigned lt_mask = (1u << lane) - 1u;
-  int cnt = 0;
+  const bool ragged = (Skv & (kTile - 1)) != 0;
+  int cnt = 0, npart = 0;
   for (int base = 0; base < nK; base += 32) {
     const int kj = base + lane;
     int cls = CLS_EMPTY;
@@ -110,8 +118,62 @@ __global__ void __launch_bounds__(256) classify_rows_kernel(const int32_t* __res
     const unsigned m = __ballot_sync(0xffffffffu, cls != CLS_EMPTY);
     if (cls != CLS_EMPTY) lst[cnt + __popc(m & lt_mask)] = (kj << 2) | cls;
     cnt += __popc(m);
+    npart += __popc(__ballot_sync(0xffffffffu, cls == CLS_PARTIAL ||
+                                                   (cls != CLS_EMPTY && ragged && kj == nK - 1)));
   }
-  if (lane == 0) row_count[w] = cnt;
+  if (lane == 0) {
+    row_count[w] = cnt;
+    int first = -1;
+    if (npart > 0 && mask_cap > 0) {
+      const unsigned long long at = atomicAdd(slot_counter, static_cast<unsigned long long>(npart));
+      if (at + static_cast<unsigned long long>(npart) <= static_cast<unsigned long long>(mask_cap))
+        first = static_cast<int>(at);
+    }
+    row_mask[w] = first;
+  }
+}
+
+// Visibility bit masks of the partial tiles of one q-tile row (one CTA per
+// row, thread r = query row r0 + r of the tile): bit c of row r is set when
+// key column kj*128 + c is hidden from that row (or lies past Skv).  The
+// masks depend only on (batch, mask head), so every query head reuses them.
+__global__ void __launch_bounds__(kTile) tile_mask_kernel(
+    const int32_t* __restrict__ lts, const int32_t* __restrict__ lte,
+    const int32_t* __restrict__ uts, const int32_t* __restrict__ ute, int nQ, int nK, int Skv,
+    const int32_t* __restrict__ row_count, const int32_t* __restrict__ row_list,
+    const int32_t* __restrict__ row_mask, uint4* masks) {
+  __shared__ int4 sb[kTile];
+  const int row = blockIdx.x;
+  const int first = row_mask[row];
+  if (first < 0) return;
+  const int bh = row / nQ, qi = row - bh * nQ;
+  const int n = row_count[row];
+  const int32_t* lst = row_list + static_cast<size_t>(row) * nK;
+  const size_t bbase = static_cast<size_t>(bh) * Skv;
+  const int r = threadIdx.x;
+  const int R = qi * kTile + r;
+  const bool ragged = (Skv & (kTile - 1)) != 0;
+  int ord = 0;
+  for (int t = 0; t < n; ++t) {
+    const int e = lst[t];
+    const int kj = e >> 2;
+    if ((e & 3) != CLS_PARTIAL && !(ragged && kj == nK - 1)) continue;
+    __syncthreads();  // previous tile's bounds no longer read
+    const int j = kj * kTile + r;
+    sb[r] = j < Skv ? make_int4(__ldg(lts + bbase + j), __ldg(lte + bbase + j),
+                                __ldg(uts + bbase + j), __ldg(ute + bbase + j))
+                    : make_int4(0, 0x7fffffff, 0, 0);
+    __syncthreads();
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int c = 0; c < kTile; ++c) {
+      const int4 v = sb[c];
+      const bool hid = (v.x <= R && R < v.y) || (v.z <= R && R < v.w);
+      w[c >> 5] |= (hid ? 1u : 0u) << (c & 31);
+    }
+    masks[(static_cast<size_t>(first + ord) * kTile + r)] = make_uint4(w[0], w[1], w[2], w[3]);
+    ++ord;
+  }
 }
 
 // One warp per (bh, k-tile): the ascending list of non-empty q-tiles.
@@ -251,8 +313,11 @@ cudaError_t launch_classify(const Plan& p, char* ws, int for_bwd, cudaStream_t s
   if (!for_bwd) {
     const int warps = nBH * p.nQ;
     classify_rows_kernel<<<ceil_div(warps, 8), 256, 0, s>>>(
-        summ, nBH, p.nQ, p.nK, p.Sq, table, reinterpret_cast<int32_t*>(ws + p.L.row_count),
-        reinterpret_cast<int32_t*>(ws + p.L.row_list));
+        summ, nBH, p.nQ, p.nK, p.Sq, p.Skv, table,
+        reinterpret_cast<int32_t*>(ws + p.L.row_count),
+        reinterpret_cast<int32_t*>(ws + p.L.row_list),
+        reinterpret_cast<int32_t*>(ws + p.L.row_mask),
+        reinterpret_cast<unsigned long long*>(ws + p.L.status + 8), p.mask_cap);
   } else {
     const int warps = nBH * p.nK;
     classify_cols_kernel<<<ceil_div(warps, 8), 256, 0, s>>>(
@@ -260,6 +325,17 @@ cudaError_t launch_classify(const Plan& p, char* ws, int for_bwd, cudaStream_t s
         reinterpret_cast<int32_t*>(ws + p.L.col_list));
   }
   prof_end(K_CLASSIFY, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tile_masks(const Plan& p, const int32_t* lts, const int32_t* lte,
+                              const int32_t* uts, const int32_t* ute, char* ws, cudaStream_t s) {
+  prof_begin(K_TILE_MASKS, s);
+  tile_mask_kernel<<<p.B * p.Hm * p.nQ, kTile, 0, s>>>(
+      lts, lte, uts, ute, p.nQ, p.nK, p.Skv, reinterpret_cast<const int32_t*>(ws + p.L.row_count),
+      reinterpret_cast<const int32_t*>(ws + p.L.row_list),
+      reinterpret_cast<const int32_t*>(ws + p.L.row_mask), reinterpret_cast<uint4*>(ws + p.L.masks));
+  prof_end(K_TILE_MASKS, s);
   return cudaGetLastError();
 }
 

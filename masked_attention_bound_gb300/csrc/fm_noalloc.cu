@@ -52,7 +52,7 @@ extern "C" fm_status fm_fwd_static(const fm_desc* desc, const void* q, const voi
                                    const int32_t* uts, const int32_t* ute, float scale, void* o,
                                    float* lse, void* stream) {
   Plan p;
-  fm_status st = make_plan(desc, 0, &p);
+  fm_status st = make_plan(desc, 0, &p, FM_STATIC_SCRATCH_BYTES);
   if (st != FM_OK) return st;
   if (p.L.total > FM_STATIC_SCRATCH_BYTES) return FM_ERR_WORKSPACE;
   auto a16 = [](const void* x) { return x && (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
@@ -64,6 +64,7 @@ extern "C" fm_status fm_fwd_static(const fm_desc* desc, const void* q, const voi
   if (cudaMemsetAsync(ws + p.L.status, 0, 16, s) != cudaSuccess) return FM_ERR_CUDA;
   if (launch_summary(p, lts, lte, uts, ute, ws, s) != cudaSuccess) return FM_ERR_CUDA;
   if (launch_classify(p, ws, 0, s) != cudaSuccess) return FM_ERR_CUDA;
+  if (launch_tile_masks(p, lts, lte, uts, ute, ws, s) != cudaSuccess) return FM_ERR_CUDA;
   if (launch_order(p, ws, 0, s) != cudaSuccess) return FM_ERR_CUDA;
   TensorArgs t{};
   t.q = q; t.k = k; t.v = v; t.o_out = o; t.lse_out = lse;

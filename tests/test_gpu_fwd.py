@@ -8,6 +8,7 @@ import masked_attention_bound_gb300 as fm
 from fm_inputs import masks as gen
 from fm_inputs.configs import LONG_128K, SUITE_32K, SWEEP_4K, TINY, TINY_DOCS
 from fm_inputs.tensors import bounds_tensor, mask_bounds, qkv_do
+from oracle import masks as om
 from parity import compare_fwd
 
 pytestmark = pytest.mark.gpu
@@ -68,6 +69,22 @@ def test_cross_lengths():
     o, lse = fm.forward(q, k, v, bounds, 0.125)
     torch.cuda.synchronize()
     compare_fwd(q, k, v, bounds, 0.125, o, lse)
+
+
+def test_more_partial_tiles_than_mask_slots():
+    """Three 32K random-eviction masks hold more partial tiles than the
+    visibility-mask region has slots, so some rows go without precomputed bits
+    and the forward kernel builds theirs itself; every row must still match."""
+    B, S, H, d = 3, 32768, 2, 64
+    q, k, v, _ = _inputs(B, S, H, d, seed=5)
+    bounds = mask_bounds("random_eviction", B, S, device="cuda")
+    _, L = fm.plan(q, k, bounds)
+    cap = (L.total - L.masks) // 2048
+    n_partial = int((om.tile_table(bounds.cpu().numpy(), S) == 1).sum())
+    assert n_partial > cap
+    o, lse = fm.forward(q, k, v, bounds, d ** -0.5)
+    torch.cuda.synchronize()
+    compare_fwd(q, k, v, bounds, d ** -0.5, o, lse, heads=[(0, 0), (1, 1), (2, 0), (2, 1)], rows=96)
 
 
 def test_repeatable():

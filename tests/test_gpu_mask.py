@@ -1,7 +1,8 @@
 """Mask-analysis kernels against the oracle, bit for bit (GPU).
 
-Block summary + tile classification + work lists + longest-first order
-(fm_plan), bound validation, and localisation (fm_localize).
+Block summary + tile classification + work lists + longest-first order +
+the partial tiles' visibility bit masks (fm_plan), bound validation, and
+localisation (fm_localize).
 """
 import numpy as np
 import pytest
@@ -23,6 +24,54 @@ def _bounds_from(b_list, Hm=1):
 def _ws_view(ws, off, n, dtype):
     itemsize = torch.tensor([], dtype=dtype).element_size()
     return ws[off:off + n * itemsize].view(dtype)
+
+
+def _check_tile_masks(ws, L, bounds, Sq, ref_rl, sample=40, seed=0):
+    """The forward plan's visibility bit masks: every row with partial tiles
+    (class PARTIAL, or the ragged last k-tile) owns consecutive slots, one per
+    such tile in list order, disjoint from other rows' and inside the region
+    (rows may go without when the region is full); sampled tiles match the
+    oracle's dense mask bit for bit (rows below Sq; columns past Skv set)."""
+    _, B, Hm, Skv = bounds.shape
+    nQ, nK = -(-Sq // 128), -(-Skv // 128)
+    cap = (L.total - L.masks) // 2048
+    rowm = _ws_view(ws, L.row_mask, B * Hm * nQ, torch.int32).view(B, Hm, nQ).cpu().numpy()
+    ragged = Skv % 128 != 0
+    parts = {}
+    for key, ent in ref_rl.items():
+        p = [kj for kj, c in ent if c == 1 or (ragged and kj == nK - 1)]
+        if p:
+            parts[key] = p
+    for b in range(B):
+        for hm in range(Hm):
+            for qi in range(nQ):
+                if (b, hm, qi) not in parts:
+                    assert rowm[b, hm, qi] == -1
+    spans = sorted((int(rowm[key]), len(p)) for key, p in parts.items() if rowm[key] >= 0)
+    for (f0, n0), (f1, _) in zip(spans, spans[1:]):
+        assert f0 + n0 <= f1
+    if spans:
+        assert spans[0][0] >= 0 and spans[-1][0] + spans[-1][1] <= cap
+    if sum(len(p) for p in parts.values()) <= cap:
+        assert len(spans) == len(parts)
+    owned = [(key, o) for key, p in parts.items() if rowm[key] >= 0 for o in range(len(p))]
+    if not owned:
+        return
+    words = _ws_view(ws, L.masks, cap * 512, torch.int32).cpu().numpy().view(np.uint32).reshape(cap, 128, 4)
+    bnp = bounds.cpu().numpy()
+    rng = np.random.default_rng(seed)
+    pick = rng.choice(len(owned), size=min(sample, len(owned)), replace=False)
+    shifts = np.arange(32, dtype=np.uint32)
+    for n in pick:
+        (b, hm, qi), o = owned[n]
+        kj = parts[(b, hm, qi)][o]
+        got = ((words[rowm[b, hm, qi] + o][:, :, None] >> shifts) & 1).reshape(128, 128).astype(bool)
+        rows = np.arange(qi * 128, min(qi * 128 + 128, Sq))
+        cols = np.arange(kj * 128, kj * 128 + 128)
+        want = np.ones((len(rows), 128), dtype=bool)
+        live = cols < Skv
+        want[:, live] = om.dense_mask(*(bnp[t, b, hm, cols[live]] for t in range(4)), Sq, rows=rows)
+        assert np.array_equal(got[:len(rows)], want), ((b, hm, qi), kj)
 
 
 def _check_plan(bounds, Sq, H=2, d=64):
@@ -48,6 +97,7 @@ def _check_plan(bounds, Sq, H=2, d=64):
                 assert lst[b, hm, qi, :len(want)].tolist() == want
             order = _ws_view(ws, L.fwd_order, B * H * nQ, torch.int32).cpu().numpy()
             assert np.array_equal(order, om.unit_order(ref_rc, H))
+            _check_tile_masks(ws, L, bounds, Sq, ref_rl)
         else:
             cnt = _ws_view(ws, L.col_count, B * Hm * nK, torch.int32).view(B, Hm, nK).cpu().numpy()
             lst = _ws_view(ws, L.col_list, B * Hm * nK * nQ, torch.int32).view(B, Hm, nK, nQ).cpu().numpy()

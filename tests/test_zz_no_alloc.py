@@ -50,6 +50,21 @@ def test_static_scratch_forward_matches_workspace_forward():
         assert (lse_s[fin] - lse_w[fin]).abs().max().item() <= LSE_TOL
 
 
+def test_static_scratch_without_room_for_every_tile_mask():
+    """At 32K random eviction the fixed scratch holds the bit masks of only a
+    few thousand of the ~33K partial tiles; the forward kernel builds the rest
+    from the bounds.  Same bits, same schedule: O and LSE equal fm_fwd's."""
+    B, S, H, d = 1, 32768, 2, 64
+    q, k, v, _ = qkv_do(B, S, S, H, d, seed=9, device="cuda")
+    bounds = mask_bounds("random_eviction", B, S, device="cuda")
+    rc, o_s, lse_s = _static_fwd(q, k, v, bounds, d ** -0.5)
+    assert rc == _abi.FM_OK
+    o_w, lse_w = fm.forward(q, k, v, bounds, d ** -0.5)
+    torch.cuda.synchronize()
+    assert torch.equal(o_s, o_w)
+    assert torch.equal(lse_s, lse_w)
+
+
 def test_static_scratch_rejects_problems_beyond_its_size():
     B, S, H, d = 1, 1 << 17, 1, 64
     q = torch.empty(B, S, H, d, dtype=torch.bfloat16, device="cuda")
