@@ -161,6 +161,15 @@ struct BwdParams {
 //   dK += dS^T Q, dQ = dS K -> B   [after dS^T(t)]
 // so the drain, P and dS work of the compute warps overlaps S, dP and dV.
 // Compute warp w owns TMEM lane quarter (w & 3) and column half (w >> 2).
+// Bits [a, b) of a 64-bit word, with a and b clipped to [0, 64].
+__device__ __forceinline__ uint64_t row_span(int a, int b) {
+  a = min(max(a, 0), 64);
+  b = min(max(b, 0), 64);
+  if (a >= b) return 0ull;
+  const uint64_t below_b = b == 64 ? ~0ull : ((1ull << b) - 1ull);
+  return below_b & ~((1ull << a) - 1ull);
+}
+
 template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bwd_kernel(const __grid_constant__ BwdParams P, const __grid_constant__ CUtensorMap tmQ,
@@ -484,12 +493,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           }
         }
         if (partial) {
+          // the rows q0 .. q0+63 hidden from this key form at most two
+          // intervals: one 64-bit mask, then a bit test per entry
           const int q0 = qi * kTile + c0;
+          const uint64_t hm = row_span(lts - q0, lte - q0) | row_span(uts - q0, ute - q0);
+          if (hm != 0) {
+            const uint32_t m0 = static_cast<uint32_t>(hm), m1 = static_cast<uint32_t>(hm >> 32);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const int q = q0 + c;
-            const bool hid = (lts <= q && q < lte) || (uts <= q && q < ute);
-            p[c] = hid ? 0.f : p[c];
+            for (int c = 0; c < 32; ++c) {
+              p[c] = ((m0 >> c) & 1u) ? 0.f : p[c];
+              p[c + 32] = ((m1 >> c) & 1u) ? 0.f : p[c + 32];
+            }
           }
         }
         {
