@@ -135,10 +135,47 @@ def col_lists(table: np.ndarray):
     return counts, lists
 
 
+def pair_lists(table: np.ndarray, Skv: int, Bk: int = 128):
+    """Forward work units of two q-tiles: rows 2p and 2p+1 of one (b, hm) (the
+    second absent when nQ is odd) walk their k-tiles together, so that each
+    K/V tile is loaded once for both; the forward pass gives each warp group
+    its own queries and shares K and V (FlashAttention-2 page, «Три способа
+    повысить загрузку GPU», third point).  A pair's list is the union of the
+    two rows' non-empty k-tiles, ascending, each entry carrying the tile's
+    class in row 2p and in row 2p+1 (EMPTY where that row skips it).  A
+    non-empty last k-tile that is ragged (Skv not a multiple of Bk) is given
+    the class PARTIAL: its columns past Skv are masked element by element.
+    Returns (counts [B][Hm][nP] = entries, costs [B][Hm][nP] = non-empty tiles
+    of both rows, dict (b, hm, p) -> [(kj, class_a, class_b), ...])."""
+    B, Hm, nQ, nK = table.shape
+    nP = -(-nQ // 2)
+    ragged = Skv % Bk != 0
+    counts = np.zeros((B, Hm, nP), dtype=np.int32)
+    costs = np.zeros((B, Hm, nP), dtype=np.int32)
+    lists = {}
+    for b in range(B):
+        for hm in range(Hm):
+            for p in range(nP):
+                ent = []
+                for kj in range(nK):
+                    cls = []
+                    for qi in (2 * p, 2 * p + 1):
+                        c = int(table[b, hm, qi, kj]) if qi < nQ else EMPTY
+                        if c != EMPTY and ragged and kj == nK - 1:
+                            c = PARTIAL
+                        cls.append(c)
+                    if cls[0] != EMPTY or cls[1] != EMPTY:
+                        ent.append((kj, cls[0], cls[1]))
+                counts[b, hm, p] = len(ent)
+                costs[b, hm, p] = sum((ca != EMPTY) + (cb != EMPTY) for _, ca, cb in ent)
+                lists[(b, hm, p)] = ent
+    return counts, costs, lists
+
+
 def unit_order(counts: np.ndarray, H: int) -> np.ndarray:
     """Work units (b, h, tile), numbered u = (b*H + h)*nT + tile, ordered by
     (b, h) ascending and, within one (b, h), by cost (non-empty tiles of the
-    unit's row or column) descending, ties by tile ascending.  Within a head
+    unit's q-tile pair or k-tile column) descending, ties by tile ascending.  Within a head
     this is the longest-processing-time-first order that balances units by
     work rather than by position (the sparsity-aware balancing the FlashMask-3
     page names in «Ключевые факты», applied to one GPU's work units); keeping

@@ -245,6 +245,48 @@ def test_lists_and_unit_order():
             cost[a] > cost[a + 1] or (cost[a] == cost[a + 1] and order[a] < order[a + 1])))
 
 
+def _table_of(b, S):
+    bounds = np.stack([np.stack([np.asarray(x)[None]]) for x in b])  # [4][1][1][S]
+    return om.tile_table(bounds, S)
+
+
+def test_pair_lists_by_hand():
+    """Causal, S = 384: tile (qi, kj) is FULL below the diagonal, PARTIAL on
+    it, EMPTY above.  Pair 0 = rows 0, 1; pair 1 = row 2 alone (nQ = 3).
+    Full mask, S = 300: every tile FULL, but the ragged last k-tile is PARTIAL."""
+    P, F, E = om.PARTIAL, om.FULL, om.EMPTY
+    n, c, lst = om.pair_lists(_table_of(gen.causal(384), 384), 384)
+    assert lst[(0, 0, 0)] == [(0, P, F), (1, E, P)]
+    assert lst[(0, 0, 1)] == [(0, F, E), (1, F, E), (2, P, E)]
+    assert n.tolist() == [[[2, 3]]] and c.tolist() == [[[3, 3]]]
+    n, c, lst = om.pair_lists(_table_of(gen.full(300), 300), 300)
+    assert lst[(0, 0, 0)] == [(0, F, F), (1, F, F), (2, P, P)]
+    assert lst[(0, 0, 1)] == [(0, F, E), (1, F, E), (2, P, E)]
+    assert c.tolist() == [[[6, 3]]]
+
+
+@pytest.mark.parametrize("name", ["causal_document", "qk_sparse", "random_eviction", "share_question"])
+def test_pair_lists_are_unions_of_rows(name):
+    S = 1100  # nQ = 9: the last pair has one row; the last k-tile is ragged
+    t = _table_of(gen.make_mask(name, S, seed=2), S)
+    nQ, nK = t.shape[2], t.shape[3]
+    rc, rl = om.row_lists(t)
+    n, c, pl = om.pair_lists(t, S)
+    assert n.shape == (1, 1, (nQ + 1) // 2)
+    for p in range((nQ + 1) // 2):
+        rows = [q for q in (2 * p, 2 * p + 1) if q < nQ]
+        want = sorted(set(k for q in rows for k, _ in rl[(0, 0, q)]))
+        got = pl[(0, 0, p)]
+        assert [k for k, _, _ in got] == want
+        assert c[0, 0, p] == sum(rc[0, 0, q] for q in rows)
+        for k, ca, cb in got:
+            for q, cls in zip((2 * p, 2 * p + 1), (ca, cb)):
+                tab = int(t[0, 0, q, k]) if q < nQ else om.EMPTY
+                if tab != om.EMPTY and k == nK - 1:
+                    tab = om.PARTIAL
+                assert cls == tab
+
+
 # ---------------------------------------------------------------- localisation
 
 def test_localize_golden(golden_dir):
