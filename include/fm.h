@@ -77,7 +77,8 @@ typedef struct {
   size_t row_list;   /* int32 [B][Hm][nQ][nK]: ascending k-tiles of each row          */
   size_t col_count;  /* int32 [B][Hm][nK]: non-empty tiles per k-tile column          */
   size_t col_list;   /* int32 [B][Hm][nK][nQ]: ascending q-tiles of each column       */
-  size_t fwd_order;  /* int32 [B*H*nQ]: forward units u=(b*H+h)*nQ+qi, longest first  */
+  size_t fwd_order;  /* int32 [B*H*nP], nP = ceil(nQ/2): forward units u=(b*H+h)*nP+p
+                        (q-tiles 2p and 2p+1), longest first                       */
   size_t bwd_order;  /* int32 [B*H*nK]: backward units u=(b*H+h)*nK+kj, longest first */
   size_t row_mask;   /* int32 [B][Hm][nQ]: first visibility-mask slot of the row's partial
                         tiles (consecutive in list order), -1 if none (forward only)  */
@@ -86,6 +87,11 @@ typedef struct {
                         bit c of 32-bit word w = column 32w+c, set = hidden (forward
                         only).  Rows whose tiles do not fit get row_mask -1 and the
                         forward kernel builds their bits itself                    */
+  size_t pair_info;  /* int32 [B][Hm][nP][4]: entries of the pair list, non-empty tiles
+                        of q-tile 2p, of q-tile 2p+1, and their sum (forward only) */
+  size_t pair_list;  /* int32 [B][Hm][nP][nK]: union of the two q-tiles' non-empty
+                        k-tiles, ascending, (kj << 4) | (class_2p << 2) | class_2p+1,
+                        a non-empty ragged last k-tile as PARTIAL (forward only)   */
   size_t delta;      /* float [B][H][nQ*128]: D_i = dO_i . O_i, 0 past Sq (backward)  */
   size_t lse_log2;   /* float [B][H][nQ*128]: LSE_i * log2(e), +inf for rows that see
                         no key and past Sq (backward only)                          */

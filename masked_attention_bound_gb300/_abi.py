@@ -28,7 +28,8 @@ class FmDesc(ctypes.Structure):
 class FmWsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status", "summary", "table", "row_count", "row_list", "col_count", "col_list",
-        "fwd_order", "bwd_order", "row_mask", "masks", "delta", "lse_log2", "dq_acc", "total")]
+        "fwd_order", "bwd_order", "row_mask", "masks", "pair_info", "pair_list", "delta",
+        "lse_log2", "dq_acc", "total")]
 
 
 class FMError(RuntimeError):

@@ -39,6 +39,7 @@ fm_status make_plan(const fm_desc* desc, int for_bwd, Plan* p, size_t limit) {
   p->B = D.B; p->H = D.H; p->Hm = D.Hm; p->Sq = D.Sq; p->Skv = D.Skv; p->d = D.d;
   p->nQ = ceil_div(D.Sq, kTile);
   p->nK = ceil_div(D.Skv, kTile);
+  p->nP = ceil_div(p->nQ, 2);
   const size_t BHm = static_cast<size_t>(D.B) * D.Hm;
   const size_t BH = static_cast<size_t>(D.B) * D.H;
   fm_ws_layout& L = p->L;
@@ -57,6 +58,8 @@ fm_status make_plan(const fm_desc* desc, int for_bwd, Plan* p, size_t limit) {
     // the mask region comes last and takes what the limit leaves, up to one
     // slot per tile and kMaxMaskTiles slots
     L.row_mask = take(BHm * p->nQ * 4);
+    L.pair_info = take(BHm * p->nP * 16);
+    L.pair_list = take(BHm * p->nP * p->nK * 4);
     size_t cap = BHm * p->nQ * p->nK;
     if (cap > static_cast<size_t>(kMaxMaskTiles)) cap = kMaxMaskTiles;
     const size_t room = limit > off ? (limit - off) / kMaskBytes : 0;
@@ -67,6 +70,8 @@ fm_status make_plan(const fm_desc* desc, int for_bwd, Plan* p, size_t limit) {
     p->mask_cap = 0;
     L.row_mask = 0;
     L.masks = 0;
+    L.pair_info = 0;
+    L.pair_list = 0;
   }
   if (for_bwd) {
     L.delta = take(BH * p->nQ * kTile * 4);

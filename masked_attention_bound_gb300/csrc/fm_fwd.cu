@@ -6,20 +6,28 @@
 // partial outputs rescaled, normalisation over the whole row), and the
 // empty/full/partial tile classes of the column-wise mask (FlashMask-3 page,
 // introduction): empty tiles never reach this kernel, full tiles skip the
-// mask arithmetic, partial tiles test every (row, column).
+// mask arithmetic, partial tiles apply a 128 x 128 visibility bit mask.
 //
-// Work unit: one (batch, head, q-tile), 128 query rows.  A persistent grid of
-// one CTA per SM walks the longest-first unit list.  Six warps per CTA:
-//   warps 0-3  softmax: thread r owns query row r = TMEM lane r.  Reads S from
-//              TMEM, masks partial tiles, keeps the running max m and sum l
-//              (base-2 exponent domain), writes P (bf16) to TMEM, rescales O
-//              in TMEM when the max moves, and writes O / LSE at the end;
-//   warp 4     loads Q, K, V tiles with TMA into 128B-swizzled smem and, for
-//              partial tiles, the 128 columns' bounds into smem;
-//   warp 5     one thread issues tcgen05 MMAs: S = Q K^T (both K-major, smem),
-//              O += P V (P from TMEM, V MN-major from smem).
-// TMEM (512 columns): S double buffer [0,128) [128,256), O [256,256+D),
-// P [384,448) as packed bf16 pairs.
+// Work unit: one (batch, head) and two adjacent q-tiles 2p, 2p+1 (slots a
+// and b, 256 query rows) that walk the union of their non-empty k-tiles, so
+// each K/V tile is loaded once for both; the FlashAttention-2 page («Три
+// способа повысить загрузку GPU», third point) gives each group of warps its
+// own queries and shares K and V.  A persistent grid of one CTA per SM walks
+// the longest-first unit list.  Twelve warps per CTA:
+//   warps 0-3 / 4-7   softmax of slot a / b: thread r owns query row r =
+//              TMEM lane r.  Reads S from TMEM, masks partial tiles, keeps
+//              the running max m and sum l (base-2 exponent domain), writes
+//              P (bf16) over S in TMEM, rescales O in TMEM when the max moves
+//              by more than 2^8, and writes O / LSE at the end of the unit;
+//   warp 8     loads Q (per slot), K and the partial tiles' bit masks; passes
+//              each entry's classes and unit boundaries to the MMA warp;
+//   warp 9     one thread issues tcgen05 MMAs: S = Q K^T (both K-major,
+//              smem), O += P V (P from TMEM, V MN-major from smem), in the
+//              order PV_a(e), S_a(e+1), PV_b(e), S_b(e+1), so one slot's
+//              softmax runs while the other slot's MMAs do;
+//   warp 10    loads V;  warp 11 idle.
+// TMEM (512 columns): S/P of slot s at [128 s, 128 s + 128), O of slot s at
+// [256 + 128 s, 256 + 128 s + D).
 #include <cuda_bf16.h>
 
 #include "fm_internal.h"
@@ -32,21 +40,20 @@ template <int D>
 struct FwdCfg {
   static constexpr int SLABS = D / 64;
   static constexpr int TILE = 128 * D * 2;  // bytes of one 128-row tile
-  static constexpr int OFF_Q = 0;                       // 2 slots
-  static constexpr int OFF_K = OFF_Q + 2 * TILE;        // 2 stages
-  static constexpr int OFF_V = OFF_K + 2 * TILE;        // 2 stages
-  static constexpr int OFF_BND = OFF_V + 2 * TILE;      // 2 stages x 128 x int4
-  static constexpr int OFF_BAR = OFF_BND + 2 * 128 * 16;
+  static constexpr int OFF_Q = 0;                              // slots a, b
+  static constexpr int OFF_K = OFF_Q + 2 * TILE;               // 2 stages
+  static constexpr int OFF_V = OFF_K + 2 * TILE;               // 2 stages
+  static constexpr int OFF_MSK = OFF_V + 2 * TILE;             // [stage][slot] bit masks
+  static constexpr int OFF_DESC = OFF_MSK + 4 * kMaskBytes;    // [stage] entry word
+  static constexpr int OFF_BAR = OFF_DESC + 16;
   static constexpr int NBAR = 24;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
   // at least 120 KB so that one CTA (which takes all 512 TMEM columns) is
   // resident per SM
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
-  // TMEM: S of slot s at [128 s, 128 s + 128) (P packed into its first 64
-  // columns), O of slot s at [256 + 128 s, 256 + 128 s + D)
   static constexpr uint32_t T_COLS = 512;
-  // warpgroups 0 and 1: softmax of slot 0 / slot 1; warpgroup 2: the Q/K/
-  // bounds load warp, the MMA warp, the V load warp and one idle warp
+  // warpgroups 0 and 1: softmax of slot a / b; warpgroup 2: the Q/K/mask
+  // load warp, the MMA warp, the V load warp and one idle warp
   static constexpr int THREADS = 384;
   // register split (setmaxnreg): 2 x 128 x REGS_SOFTMAX + 128 x REGS_PRODUCER
   // = 62464 <= THREADS x (compiled registers); the launch checks that the
@@ -56,20 +63,27 @@ struct FwdCfg {
       (2 * 128 * REGS_SOFTMAX + 128 * REGS_PRODUCER + THREADS - 1) / THREADS;
 };
 
-// barrier slots; "s" = q-tile slot (0/1), "st" = K/V stage (0/1)
+// barrier slots; "s" = q-tile slot (0 = a, 1 = b), "st" = K/V stage (0/1)
 enum {
   B_QFULL0 = 0, B_QEMPTY0 = 2, B_SFULL0 = 4, B_PFULL0 = 6, B_PVDONE0 = 8, B_OEMPTY0 = 10,
-  B_KFULL0 = 12, B_KEMPTY0 = 14, B_VFULL0 = 16, B_VEMPTY0 = 18, B_BEMPTY0 = 20, B_DRAIN = 22
+  B_KFULL0 = 12, B_KEMPTY0 = 14, B_VFULL0 = 16, B_VEMPTY0 = 18, B_MEMPTY0 = 20, B_DRAIN = 22
 };
 
+// entry word the load warp hands to the MMA warp: the pair-list classes in
+// bits 0-3 (class_b bits 0-1, class_a bits 2-3), then whether this entry is
+// the first / last non-empty tile of slot a (bits 4, 5) and of slot b (6, 7)
+// within its unit
+constexpr uint32_t E_A = 12u, E_B = 3u, E_FIRST_A = 16u, E_LAST_A = 32u, E_FIRST_B = 64u,
+                   E_LAST_B = 128u;
+
 struct FwdParams {
-  int B, H, Hm, Sq, Skv, nQ, nK, n_units;
+  int B, H, Hm, Sq, Skv, nQ, nK, nP, n_units;
   float scale_log2;  // scale * log2(e)
   const int32_t* bounds[4];
-  const int32_t* row_count;
-  const int32_t* row_list;
+  const int4* pair_info;    // per pair row: entries, tiles of 2p, tiles of 2p+1, sum
+  const int32_t* pair_list;
   const int32_t* order;
-  const int32_t* row_mask;  // first visibility-mask slot of a row's partial tiles, -1: none
+  const int32_t* row_mask;  // first visibility-mask slot of a q-tile row's partial tiles, -1: none
   const uint8_t* masks;     // 2 KB per slot: 128 rows x 128 column bits, set = hidden
   __nv_bfloat16* o;
   int64_t o_stride[3];
@@ -77,87 +91,30 @@ struct FwdParams {
   int* status;
 };
 
-__device__ __forceinline__ bool tile_partial(int e, int kj, int nK, int Skv) {
-  return ((e & 3) == CLS_PARTIAL) || (kj == nK - 1 && (Skv & (kTile - 1)) != 0);
-}
-
 // The CTA's units are idx = blockIdx.x + k * gridDim.x, k = 0, 1, 2, ...;
-// slot s takes the units with k % 2 == s.  A cursor walks one slot's
-// non-empty tiles; the merge interleaves the two slots' tiles (alternating
-// while both have tiles left).  The TMA warp, the MMA warp and both softmax
-// warpgroups run identical merges, so they agree on which K/V stage and
-// which barrier phase every tile uses.
-struct Cursor {
-  int k, t, n, row;
-};
-struct UnitInfo {
-  int b, h, qi, row, n;
+// every role walks them in that order and their entries one by one, so all
+// agree on the K/V stage (entry count mod 2) and the barrier phases.
+struct PairUnit {
+  int b, h, qa, prow, row_a, n, na, nb;
 };
 
-__device__ __forceinline__ UnitInfo unit_of(const FwdParams& P, int idx) {
-  UnitInfo u;
+__device__ __forceinline__ PairUnit unit_of(const FwdParams& P, int idx) {
+  PairUnit u;
   const int id = P.order[idx];
-  const int bh = id / P.nQ;
-  u.qi = id - bh * P.nQ;
+  const int bh = id / P.nP;
+  const int p = id - bh * P.nP;
   u.b = bh / P.H;
   u.h = bh - u.b * P.H;
-  u.row = (u.b * P.Hm + (P.Hm == 1 ? 0 : u.h)) * P.nQ + u.qi;
-  u.n = P.row_count[u.row];
+  const int bm = u.b * P.Hm + (P.Hm == 1 ? 0 : u.h);
+  u.prow = bm * P.nP + p;
+  u.row_a = bm * P.nQ + 2 * p;
+  u.qa = 2 * p;
+  const int4 inf = P.pair_info[u.prow];
+  u.n = inf.x;
+  u.na = inf.y;
+  u.nb = inf.z;
   return u;
 }
-
-__device__ __forceinline__ void cursor_next_unit(const FwdParams& P, Cursor& c) {
-  while (true) {
-    c.k += 2;
-    const int idx = blockIdx.x + c.k * gridDim.x;
-    if (idx >= P.n_units) {
-      c.n = -1;
-      return;
-    }
-    const UnitInfo u = unit_of(P, idx);
-    if (u.n > 0) {
-      c.n = u.n;
-      c.row = u.row;
-      c.t = 0;
-      return;
-    }
-  }
-}
-
-struct Merge {
-  Cursor c0, c1;  // two scalars, not an array: no dynamically indexed local memory
-  int turn;
-  __device__ __forceinline__ void init(const FwdParams& P) {
-    c0.k = -2;
-    c0.t = 0;
-    cursor_next_unit(P, c0);
-    c1.k = -1;
-    c1.t = 0;
-    cursor_next_unit(P, c1);
-    turn = 0;
-  }
-  __device__ __forceinline__ int peek() const {
-    const bool a = c0.n > 0, b = c1.n > 0;
-    return (a && b) ? turn : (a ? 0 : (b ? 1 : -1));
-  }
-  // Take the next merged tile: its slot, unit index k, tile t and whether it
-  // is the first / last tile of its unit.
-  __device__ __forceinline__ int next(const FwdParams& P, int& k, int& t, int& row, bool& first,
-                                      bool& last) {
-    const int s = peek();
-    if (s < 0) return -1;
-    if (c0.n > 0 && c1.n > 0) turn ^= 1;
-    Cursor x = s ? c1 : c0;
-    k = x.k;
-    t = x.t;
-    row = x.row;
-    first = x.t == 0;
-    last = x.t == x.n - 1;
-    if (++x.t >= x.n) cursor_next_unit(P, x);
-    if (s) c1 = x; else c0 = x;
-    return s;
-  }
-};
 
 // Two-entry per-slot state kept in registers (selected, never indexed).
 template <typename T>
@@ -182,7 +139,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * i; };
-  int4* bnd = reinterpret_cast<int4*>(smem + C::OFF_BND);
+  uint4* msk = reinterpret_cast<uint4*>(smem + C::OFF_MSK);  // [stage * 2 + slot][128 rows]
+  volatile uint32_t* desc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_DESC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -200,7 +158,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       mbar_init(bar(B_KEMPTY0 + s), 1);
       mbar_init(bar(B_VFULL0 + s), 1);
       mbar_init(bar(B_VEMPTY0 + s), 1);
-      mbar_init(bar(B_BEMPTY0 + s), 128);
+      // per stage: 128 arrivals for each slot, from its softmax threads when
+      // the slot's tile there is partial (they read the bits), else from the
+      // load warp on the slot's behalf
+      mbar_init(bar(B_MEMPTY0 + s), 256);
     }
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
@@ -240,182 +201,204 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   // after the budget change, so the compiler allocates it within the budget)
   regs_decrease<C::REGS_PRODUCER>();
   if (warp == TMA_WARP) {
-    // ------------------------------------------------------------ TMA producer
-    Merge mg;
-    mg.init(P);
-    uint32_t i = 0;
+    // ------------------------------------------------------------ Q / K / mask loads
+    // Bits of a partial tile without a precomputed mask, built from the
+    // bounds: lane l holds columns l, l+32, l+64, l+96, so ballot x over the
+    // lanes is word x of a row; lane (r mod 32) keeps row r's words.
+    auto build_bits = [&](const PairUnit& u, int kj, int qt, uint4* rows) {
+      const size_t base = static_cast<size_t>(u.b * P.Hm + (P.Hm == 1 ? 0 : u.h)) * P.Skv;
+      int4 v[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int j = kj * kTile + lane + 32 * x;
+        if (j < P.Skv) {
+          v[x].x = __ldg(P.bounds[0] + base + j);
+          v[x].y = __ldg(P.bounds[1] + base + j);
+          v[x].z = __ldg(P.bounds[2] + base + j);
+          v[x].w = __ldg(P.bounds[3] + base + j);
+        } else {
+          v[x] = make_int4(0, 0x7fffffff, 0, 0);  // beyond the keys: hidden from every row
+        }
+      }
+      for (int g = 0; g < 4; ++g) {
+        uint4 mine = make_uint4(0u, 0u, 0u, 0u);
+        for (int rr = 0; rr < 32; ++rr) {
+          const int qrow = qt * kTile + g * 32 + rr;
+          uint32_t w[4];
+#pragma unroll
+          for (int x = 0; x < 4; ++x)
+            w[x] = __ballot_sync(0xffffffffu, (v[x].x <= qrow && qrow < v[x].y) ||
+                                                  (v[x].z <= qrow && qrow < v[x].w));
+          if (lane == rr) mine = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        rows[g * 32 + lane] = mine;
+      }
+    };
+    uint32_t e = 0;
     Pair<uint32_t> qn{0, 0};
-    Pair<int> mbase{-1, -1}, mord{0, 0};  // per slot: the unit's first mask slot, partials so far
-    while (true) {
-      int k, t, row;
-      bool first, last;
-      const int s = mg.next(P, k, t, row, first, last);
-      if (s < 0) break;
-      const UnitInfo u = unit_of(P, blockIdx.x + k * gridDim.x);
-      if (first && lane == 0) {
-        bool ok = qn.get(s) == 0 || wait(B_QEMPTY0 + s, (qn.get(s) - 1) & 1);
-        if (ok) {
-          mbar_arrive_expect_tx(bar(B_QFULL0 + s), C::TILE);
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int idx = blockIdx.x + k * gridDim.x;
+      if (idx >= P.n_units) break;
+      const PairUnit u = unit_of(P, idx);
+      if (u.n == 0) continue;
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        if ((s ? u.nb : u.na) == 0) continue;  // no tile of this slot: no Q
+        if (lane == 0) {
+          if (qn.get(s) > 0 && !wait(B_QEMPTY0 + s, (qn.get(s) - 1) & 1)) ok = false;
+          if (ok) {
+            mbar_arrive_expect_tx(bar(B_QFULL0 + s), C::TILE);
+#pragma unroll
+            for (int x = 0; x < C::SLABS; ++x)
+              tma_load_4d(sbase + C::OFF_Q + s * C::TILE + x * 16384, &tmQ, bar(B_QFULL0 + s),
+                          x * 64, u.h, (u.qa + s) * kTile, u.b);
+          }
+        }
+        qn.set(s, qn.get(s) + 1);
+      }
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const int mb0 = P.row_mask[u.row_a];
+      const int mb1 = u.nb > 0 ? P.row_mask[u.row_a + 1] : -1;
+      int mo0 = 0, mo1 = 0;      // partial tiles of each slot so far in this unit
+      int seen0 = 0, seen1 = 0;  // non-empty tiles of each slot so far in this unit
+      for (int t = 0; t < u.n; ++t, ++e) {
+        const int ent = P.pair_list[static_cast<size_t>(u.prow) * P.nK + t];
+        const int kj = ent >> 4, ca = (ent >> 2) & 3, cb = ent & 3;
+        const int st = e & 1;
+        const uint32_t use = e >> 1;
+        if (use > 0 && !wait_all(B_KEMPTY0 + st, (use - 1) & 1)) { ok = false; break; }
+        if (use > 0 && !wait_all(B_MEMPTY0 + st, (use - 1) & 1)) { ok = false; break; }
+        int ms0 = -1, ms1 = -1;  // precomputed mask slots (bulk-copied below)
+        if (ca == CLS_PARTIAL) {
+          if (mb0 >= 0) ms0 = mb0 + mo0;
+          else build_bits(u, kj, u.qa, msk + (st * 2 + 0) * 128);
+          ++mo0;
+        }
+        if (cb == CLS_PARTIAL) {
+          if (mb1 >= 0) ms1 = mb1 + mo1;
+          else build_bits(u, kj, u.qa + 1, msk + (st * 2 + 1) * 128);
+          ++mo1;
+        }
+        uint32_t flags = static_cast<uint32_t>(ent & 15);
+        if (ca != CLS_EMPTY) {
+          flags |= (seen0 == 0 ? E_FIRST_A : 0u) | (seen0 == u.na - 1 ? E_LAST_A : 0u);
+          ++seen0;
+        }
+        if (cb != CLS_EMPTY) {
+          flags |= (seen1 == 0 ? E_FIRST_B : 0u) | (seen1 == u.nb - 1 ? E_LAST_B : 0u);
+          ++seen1;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          desc[st] = flags;
+          const uint32_t bytes =
+              C::TILE + (ms0 >= 0 ? kMaskBytes : 0u) + (ms1 >= 0 ? kMaskBytes : 0u);
+          mbar_arrive_expect_tx(bar(B_KFULL0 + st), bytes);
+          if (ms0 >= 0)
+            bulk_load(smem_u32(msk + (st * 2 + 0) * 128),
+                      P.masks + static_cast<size_t>(ms0) * kMaskBytes, kMaskBytes,
+                      bar(B_KFULL0 + st));
+          if (ms1 >= 0)
+            bulk_load(smem_u32(msk + (st * 2 + 1) * 128),
+                      P.masks + static_cast<size_t>(ms1) * kMaskBytes, kMaskBytes,
+                      bar(B_KFULL0 + st));
 #pragma unroll
           for (int x = 0; x < C::SLABS; ++x)
-            tma_load_4d(sbase + C::OFF_Q + s * C::TILE + x * 16384, &tmQ, bar(B_QFULL0 + s),
-                        x * 64, u.h, u.qi * kTile, u.b);
+            tma_load_4d(sbase + C::OFF_K + st * C::TILE + x * 16384, &tmK, bar(B_KFULL0 + st),
+                        x * 64, u.h, kj * kTile, u.b);
+          // a slot whose tile here is not partial never reads this stage's bits
+          if (ca != CLS_PARTIAL) mbar_arrive_count(bar(B_MEMPTY0 + st), 128);
+          if (cb != CLS_PARTIAL) mbar_arrive_count(bar(B_MEMPTY0 + st), 128);
         }
       }
-      if (first) {
-        qn.set(s, qn.get(s) + 1);
-        mbase.set(s, P.row_mask[u.row]);
-        mord.set(s, 0);
-      }
-      const int e = P.row_list[static_cast<size_t>(row) * P.nK + t];
-      const int kj = e >> 2;
-      const int st = i & 1;
-      const uint32_t use = i >> 1;
-      if (use > 0 && !wait_all(B_KEMPTY0 + st, (use - 1) & 1)) break;
-      if (use > 0 && !wait_all(B_BEMPTY0 + st, (use - 1) & 1)) break;
-      const bool partial = tile_partial(e, kj, P.nK, P.Skv);
-      int mslot = -1;  // precomputed bit mask of this tile, if any
-      if (partial && mbase.get(s) >= 0) {
-        mslot = mbase.get(s) + mord.get(s);
-        mord.set(s, mord.get(s) + 1);
-      }
-      if (partial && mslot < 0) {
-        // no precomputed mask for this tile: build its bits here from the
-        // bounds. Lane l holds columns l, l+32, l+64, l+96, so ballot x over
-        // the lanes is word x of a row; lane (r mod 32) keeps row r's words.
-        const size_t base = static_cast<size_t>(u.b * P.Hm + (P.Hm == 1 ? 0 : u.h)) * P.Skv;
-        int4 v[4];
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const int j = kj * kTile + lane + 32 * x;
-          if (j < P.Skv) {
-            v[x].x = __ldg(P.bounds[0] + base + j);
-            v[x].y = __ldg(P.bounds[1] + base + j);
-            v[x].z = __ldg(P.bounds[2] + base + j);
-            v[x].w = __ldg(P.bounds[3] + base + j);
-          } else {
-            v[x] = make_int4(0, 0x7fffffff, 0, 0);  // beyond the keys: hidden from every row
-          }
-        }
-        uint4* rows = reinterpret_cast<uint4*>(bnd + st * 128);
-        for (int g = 0; g < 4; ++g) {
-          uint4 mine = make_uint4(0u, 0u, 0u, 0u);
-          for (int rr = 0; rr < 32; ++rr) {
-            const int qrow = u.qi * kTile + g * 32 + rr;
-            uint32_t w[4];
-#pragma unroll
-            for (int x = 0; x < 4; ++x)
-              w[x] = __ballot_sync(0xffffffffu, (v[x].x <= qrow && qrow < v[x].y) ||
-                                                    (v[x].z <= qrow && qrow < v[x].w));
-            if (lane == rr) mine = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-          rows[g * 32 + lane] = mine;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(B_KFULL0 + st), C::TILE + (mslot >= 0 ? kMaskBytes : 0));
-        if (mslot >= 0)
-          bulk_load(smem_u32(bnd + st * 128), P.masks + static_cast<size_t>(mslot) * kMaskBytes,
-                    kMaskBytes, bar(B_KFULL0 + st));
-#pragma unroll
-        for (int x = 0; x < C::SLABS; ++x)
-          tma_load_4d(sbase + C::OFF_K + st * C::TILE + x * 16384, &tmK, bar(B_KFULL0 + st),
-                      x * 64, u.h, kj * kTile, u.b);
-      }
-      ++i;
     }
     // drain: every issued copy has landed before the CTA may exit
     if (lane == 0) {
-      for (uint32_t x = (i > 2u ? i - 2u : 0u); x < i; ++x)
+      for (uint32_t x = (e > 2u ? e - 2u : 0u); x < e; ++x)
         mbar_wait(bar(B_KFULL0 + (x & 1)), (x >> 1) & 1, P.status);
       if (qn.v0 > 0) mbar_wait(bar(B_QFULL0), (qn.v0 - 1) & 1, P.status);
       if (qn.v1 > 0) mbar_wait(bar(B_QFULL0 + 1), (qn.v1 - 1) & 1, P.status);
     }
     __syncwarp();
   } else if (warp == V_WARP) {
-    // ------------------------------------------------------------ V producer
+    // ------------------------------------------------------------ V loads
     // its own warp, so a V stage that is still in use never holds up K loads
     if (lane == 0) {
-      Merge mg;
-      mg.init(P);
-      uint32_t i = 0;
-      while (true) {
-        int k, t, row;
-        bool first, last;
-        if (mg.next(P, k, t, row, first, last) < 0) break;
-        const UnitInfo u = unit_of(P, blockIdx.x + k * gridDim.x);
-        const int kj = P.row_list[static_cast<size_t>(row) * P.nK + t] >> 2;
-        const int st = i & 1;
-        const uint32_t use = i >> 1;
-        if (use > 0 && !wait(B_VEMPTY0 + st, (use - 1) & 1)) break;
-        mbar_arrive_expect_tx(bar(B_VFULL0 + st), C::TILE);
+      uint32_t e = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int idx = blockIdx.x + k * gridDim.x;
+        if (idx >= P.n_units) break;
+        const PairUnit u = unit_of(P, idx);
+        for (int t = 0; t < u.n; ++t, ++e) {
+          const int kj = P.pair_list[static_cast<size_t>(u.prow) * P.nK + t] >> 4;
+          const int st = e & 1;
+          const uint32_t use = e >> 1;
+          if (use > 0 && !wait(B_VEMPTY0 + st, (use - 1) & 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(B_VFULL0 + st), C::TILE);
 #pragma unroll
-        for (int x = 0; x < C::SLABS; ++x)
-          tma_load_4d(sbase + C::OFF_V + st * C::TILE + x * 16384, &tmV, bar(B_VFULL0 + st),
-                      x * 64, u.h, kj * kTile, u.b);
-        ++i;
+          for (int x = 0; x < C::SLABS; ++x)
+            tma_load_4d(sbase + C::OFF_V + st * C::TILE + x * 16384, &tmV, bar(B_VFULL0 + st),
+                        x * 64, u.h, kj * kTile, u.b);
+        }
       }
-      for (uint32_t x = (i > 2u ? i - 2u : 0u); x < i; ++x)
+      for (uint32_t x = (e > 2u ? e - 2u : 0u); x < e; ++x)
         mbar_wait(bar(B_VFULL0 + (x & 1)), (x >> 1) & 1, P.status);
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
+    // entries this CTA walks: the lanes sum the units' counts
+    uint32_t total = 0;
+    for (long long k0 = 0;; k0 += 32) {
+      if (blockIdx.x + k0 * gridDim.x >= P.n_units) break;
+      const long long idx = blockIdx.x + (k0 + lane) * gridDim.x;
+      const int n = idx < P.n_units ? unit_of(P, static_cast<int>(idx)).n : 0;
+      total += static_cast<uint32_t>(__reduce_add_sync(0xffffffffu, n));
+    }
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
-      Merge mg;
-      mg.init(P);
-      uint32_t i = 0;
-      Pair<uint32_t> js{0, 0}, jp{0, 0}, qn{0, 0}, un{0, 0}, pend_i{0, 0};
-      Pair<bool> pend{false, false}, pend_first{false, false};
-      bool ok = true;
-      // S of slot s for the next merged tile(s) of that slot; returns false on abort
-      auto issue_s_phase = [&](int want) -> bool {
-        while (true) {
-          const int s = mg.peek();
-          if (s < 0 || pend.get(s) || (want >= 0 && s != want)) return true;
-          int k, t, row;
-          bool first, last;
-          mg.next(P, k, t, row, first, last);
-          if (first) {
-            if (!wait(B_QFULL0 + s, qn.get(s) & 1)) return false;
-            qn.set(s, qn.get(s) + 1);
-          }
-          // S of this slot overwrites P of its previous tile; MMAs issued by this
-          // thread run in issue order, so the PV that reads P is done with it first
-          const int st = i & 1;
-          if (!wait(B_KFULL0 + st, (i >> 1) & 1)) return false;
-          tc_fence_after();
-          const uint32_t sQ = sbase + C::OFF_Q + s * C::TILE;
-          const uint32_t sK = sbase + C::OFF_K + st * C::TILE;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tbase + 128 * s, sdesc_sw128(sQ + koff, 16, 1024),
-                   sdesc_sw128(sK + koff, 16, 1024), idS, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(B_SFULL0 + s));
-          mma_commit(bar(B_KEMPTY0 + st));
-          if (last) mma_commit(bar(B_QEMPTY0 + s));
-          js.set(s, js.get(s) + 1);
-          pend.set(s, true);
-          pend_first.set(s, first);
-          pend_i.set(s, i);
-          ++i;
-        }
+      Pair<uint32_t> qn{0, 0}, np{0, 0}, un{0, 0};
+      // entry word of entry e, once its K tile (and bits) have landed
+      auto entry = [&](uint32_t e, uint32_t& f) -> bool {
+        if (!wait(B_KFULL0 + (e & 1), (e >> 1) & 1)) return false;
+        f = desc[e & 1];
+        return true;
       };
-      auto issue_pv = [&](int s) -> bool {
-        if (!wait(B_PFULL0 + s, jp.get(s) & 1)) return false;
-        const bool first = pend_first.get(s);
+      // S of slot s for entry e.  It overwrites the slot's P of its previous
+      // tile; MMAs issued by this thread run in issue order, so the PV that
+      // reads that P (issued before) is done with it first.
+      auto issue_s = [&](int s, uint32_t e, uint32_t f) -> bool {
+        if (f & (s ? E_FIRST_B : E_FIRST_A)) {
+          if (!wait(B_QFULL0 + s, qn.get(s) & 1)) return false;
+          qn.set(s, qn.get(s) + 1);
+        }
+        tc_fence_after();
+        const uint32_t sQ = sbase + C::OFF_Q + s * C::TILE;
+        const uint32_t sK = sbase + C::OFF_K + (e & 1) * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tbase + 128 * s, sdesc_sw128(sQ + koff, 16, 1024),
+                 sdesc_sw128(sK + koff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(B_SFULL0 + s));
+        if (f & (s ? E_LAST_B : E_LAST_A)) mma_commit(bar(B_QEMPTY0 + s));
+        return true;
+      };
+      auto issue_pv = [&](int s, uint32_t e, uint32_t f) -> bool {
+        if (!wait(B_PFULL0 + s, np.get(s) & 1)) return false;
+        np.set(s, np.get(s) + 1);
+        const bool first = (f & (s ? E_FIRST_B : E_FIRST_A)) != 0;
         if (first) {
           // O of this slot is overwritten: its previous epilogue must be done
           if (un.get(s) > 0 && !wait(B_OEMPTY0 + s, (un.get(s) - 1) & 1)) return false;
           un.set(s, un.get(s) + 1);
         }
-        const int st = pend_i.get(s) & 1;
-        if (!wait(B_VFULL0 + st, (pend_i.get(s) >> 1) & 1)) return false;
+        const int st = e & 1;
+        if (!wait(B_VFULL0 + st, (e >> 1) & 1)) return false;
         tc_fence_after();
         const uint32_t sV = sbase + C::OFF_V + st * C::TILE;
 #pragma unroll
@@ -423,20 +406,27 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           mma_ts(tbase + 256 + 128 * s, tbase + 128 * s + kk * 8,
                  sdesc_sw128(sV + kk * 2048, 128 * 128, 1024), idPV, (!first || kk > 0) ? 1u : 0u);
         mma_commit(bar(B_PVDONE0 + s));
-        mma_commit(bar(B_VEMPTY0 + st));
-        jp.set(s, jp.get(s) + 1);
-        pend.set(s, false);
         return true;
       };
-      // prologue: the first S of each slot (merged order)
-      ok = issue_s_phase(-1);
-      // ping-pong: PV of slot 0 then its next S, PV of slot 1 then its next S,
-      // so one slot's softmax overlaps the other slot's MMAs
-      while (ok && (pend.v0 || pend.v1)) {
-#pragma unroll
-        for (int s = 0; s < 2; ++s)
-          if (ok && pend.get(s) && !issue_pv(s)) ok = false;
-        if (ok && !issue_s_phase(-1)) ok = false;
+      bool ok = true;
+      if (total > 0) {
+        uint32_t fc = 0;
+        ok = entry(0, fc);
+        if (ok && (fc & E_A)) ok = issue_s(0, 0, fc);
+        if (ok && (fc & E_B)) ok = issue_s(1, 0, fc);
+        if (ok) mma_commit(bar(B_KEMPTY0));
+        for (uint32_t j = 0; ok && j < total; ++j) {
+          const bool more = j + 1 < total;
+          uint32_t fn = 0;
+          if ((fc & E_A) && !issue_pv(0, j, fc)) { ok = false; break; }
+          if (more && !entry(j + 1, fn)) { ok = false; break; }
+          if (more && (fn & E_A) && !issue_s(0, j + 1, fn)) { ok = false; break; }
+          if ((fc & E_B) && !issue_pv(1, j, fc)) { ok = false; break; }
+          mma_commit(bar(B_VEMPTY0 + (j & 1)));
+          if (more && (fn & E_B) && !issue_s(1, j + 1, fn)) { ok = false; break; }
+          if (more) mma_commit(bar(B_KEMPTY0 + ((j + 1) & 1)));
+          fc = fn;
+        }
       }
       mma_commit(bar(B_DRAIN));
       mbar_wait(bar(B_DRAIN), 0, P.status);
@@ -452,54 +442,59 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tbase + lane_off + 128 * slot;
     const uint32_t tO = tbase + lane_off + 256 + 128 * slot;
-    Merge mg;
-    mg.init(P);
-    uint32_t i = 0, j = 0;  // merged tile index, this slot's tile index
+    uint32_t e = 0, j = 0;  // entries walked, tiles of this slot done
     bool ok = true;
-    for (int k = slot; ok; k += 2) {
+    for (int k = 0; ok; ++k) {
       const int idx = blockIdx.x + k * gridDim.x;
       if (idx >= P.n_units) break;
-      const UnitInfo u = unit_of(P, idx);
-      const int qrow = u.qi * kTile + r;
+      const PairUnit u = unit_of(P, idx);
+      const int qt = u.qa + slot;
+      if (qt >= P.nQ) {  // odd nQ: the last pair has no second q-tile
+        e += u.n;
+        continue;
+      }
+      const int ns = slot ? u.nb : u.na;
+      const int qrow = qt * kTile + r;
       __nv_bfloat16* orow = P.o + u.b * P.o_stride[0] + static_cast<int64_t>(qrow) * P.o_stride[1] +
                             u.h * P.o_stride[2];
       float* lse_out = P.lse + (static_cast<size_t>(u.b) * P.H + u.h) * P.Sq + qrow;
-      if (u.n == 0) {
+      if (ns == 0) {
         if (qrow < P.Sq) {
           const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
           *lse_out = -INFINITY;
         }
+        e += u.n;
         continue;
       }
       float m_used = -INFINITY, l = 0.f;  // running max (base-2 exponent domain) and sum
-      for (int t = 0; t < u.n; ++t, ++j) {
-        // the merged index of this tile: walk the merge past the other slot's tiles
-        int mk, mt, mrow;
-        bool mf, ml;
-        int ms;
-        while ((ms = mg.next(P, mk, mt, mrow, mf, ml)) != slot && ms >= 0) ++i;
-        const uint32_t mi = i++;
-        const int e = P.row_list[static_cast<size_t>(u.row) * P.nK + t];
-        const int kj = e >> 2;
-        const int st = mi & 1;
+      int done = 0;                       // tiles of this unit done
+      for (int t = 0; t < u.n; ++t, ++e) {
+        const int ent = P.pair_list[static_cast<size_t>(u.prow) * P.nK + t];
+        const int cls = slot ? (ent & 3) : ((ent >> 2) & 3);
+        if (cls == CLS_EMPTY) continue;
+        const int st = e & 1;
+        const bool partial = cls == CLS_PARTIAL;
         if (!wait_all(B_SFULL0 + slot, j & 1)) { ok = false; break; }
         tc_fence_after();
-        // the whole S row in one round trip: TMEM load latency (~670 cycles)
-        // does not depend on the width, so issue both halves, wait once
-        const bool partial = tile_partial(e, kj, P.nK, P.Skv);
+        // the whole S row in one round trip: TMEM load latency does not
+        // depend on the width, so issue all four quarters and wait once
         float sv[128];
         {
           uint32_t* raw = reinterpret_cast<uint32_t*>(sv);
 #pragma unroll
           for (int x = 0; x < 4; ++x) tmem_ld32(tS + 32 * x, raw + 32 * x);
-          if (partial && !wait_all(B_KFULL0 + st, (mi >> 1) & 1)) { ok = false; break; }
+          if (partial && !wait_all(B_KFULL0 + st, (e >> 1) & 1)) {
+            tmem_wait_ld();
+            ok = false;
+            break;
+          }
           tmem_wait_ld();
         }
         if (partial) {
           // this row's 128 column bits (set = hidden), one 16-byte load
-          const uint4 mw = reinterpret_cast<const uint4*>(bnd + st * 128)[r];
+          const uint4 mw = msk[(st * 2 + slot) * 128 + r];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             sv[c] = ((mw.x >> c) & 1u) ? -INFINITY : sv[c];
@@ -507,8 +502,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             sv[c + 64] = ((mw.z >> c) & 1u) ? -INFINITY : sv[c + 64];
             sv[c + 96] = ((mw.w >> c) & 1u) ? -INFINITY : sv[c + 96];
           }
+          mbar_arrive(bar(B_MEMPTY0 + st));  // done with this stage's bits
         }
-        mbar_arrive(bar(B_BEMPTY0 + st));  // done with this stage's mask bits
         float mx8[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) mx8[x] = sv[x];
@@ -545,7 +540,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         // rescale O by alpha (after P: the S registers are free by now).  O
         // holds the PVs of the earlier tiles, all complete since S of this tile
         // completed after them
-        if (t > 0 && __any_sync(0xffffffffu, grow)) {
+        if (done > 0 && __any_sync(0xffffffffu, grow)) {
           uint32_t raw[D];
 #pragma unroll
           for (int x = 0; x < D / 32; ++x) tmem_ld32(tO + 32 * x, raw + 32 * x);
@@ -559,6 +554,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(B_PFULL0 + slot));
+        ++j;
+        ++done;
       }
       if (!ok) break;
       // epilogue: O / l and LSE, after this unit's last PV.  O is read from
@@ -605,11 +602,12 @@ static fm_status launch_fwd_d(const Plan& p, const fm_desc& desc, const TensorAr
     return FM_ERR_CUDA;
   FwdParams P{};
   P.B = p.B; P.H = p.H; P.Hm = p.Hm; P.Sq = p.Sq; P.Skv = p.Skv; P.nQ = p.nQ; P.nK = p.nK;
-  P.n_units = p.B * p.H * p.nQ;
+  P.nP = p.nP;
+  P.n_units = p.B * p.H * p.nP;
   P.scale_log2 = t.scale * 1.4426950408889634f;
   for (int i = 0; i < 4; ++i) P.bounds[i] = t.bounds[i];
-  P.row_count = reinterpret_cast<const int32_t*>(ws + p.L.row_count);
-  P.row_list = reinterpret_cast<const int32_t*>(ws + p.L.row_list);
+  P.pair_info = reinterpret_cast<const int4*>(ws + p.L.pair_info);
+  P.pair_list = reinterpret_cast<const int32_t*>(ws + p.L.pair_list);
   P.order = reinterpret_cast<const int32_t*>(ws + p.L.fwd_order);
   P.row_mask = reinterpret_cast<const int32_t*>(ws + p.L.row_mask);
   P.masks = reinterpret_cast<const uint8_t*>(ws + p.L.masks);

@@ -176,6 +176,46 @@ __global__ void __launch_bounds__(kTile) tile_mask_kernel(
   }
 }
 
+// One warp per (bh, q-tile pair p): the union of the non-empty k-tiles of
+// q-tiles 2p and 2p+1 (the second absent when nQ is odd), ascending, each
+// entry (kj << 4) | (class_a << 2) | class_b, a non-empty ragged last k-tile
+// as PARTIAL; info = {entries, tiles of 2p, tiles of 2p+1, their sum}.
+__global__ void __launch_bounds__(256) classify_pairs_kernel(const uint8_t* __restrict__ table,
+                                                             int nBH, int nQ, int nK, int nP,
+                                                             int Skv, int4* pair_info,
+                                                             int32_t* pair_list) {
+  const int lane = threadIdx.x & 31;
+  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (w >= nBH * nP) return;
+  const int bh = w / nP, p = w - bh * nP;
+  const uint8_t* ta = table + (static_cast<size_t>(bh) * nQ + 2 * p) * nK;
+  const bool has_b = 2 * p + 1 < nQ;
+  const uint8_t* tb = ta + nK;
+  int32_t* lst = pair_list + static_cast<size_t>(w) * nK;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const bool ragged = (Skv & (kTile - 1)) != 0;
+  int cnt = 0, na = 0, nb = 0;
+  for (int base = 0; base < nK; base += 32) {
+    const int kj = base + lane;
+    int ca = CLS_EMPTY, cb = CLS_EMPTY;
+    if (kj < nK) {
+      ca = ta[kj];
+      cb = has_b ? tb[kj] : CLS_EMPTY;
+      if (ragged && kj == nK - 1) {
+        if (ca != CLS_EMPTY) ca = CLS_PARTIAL;
+        if (cb != CLS_EMPTY) cb = CLS_PARTIAL;
+      }
+    }
+    const bool any = ca != CLS_EMPTY || cb != CLS_EMPTY;
+    const unsigned m = __ballot_sync(0xffffffffu, any);
+    if (any) lst[cnt + __popc(m & lt_mask)] = (kj << 4) | (ca << 2) | cb;
+    cnt += __popc(m);
+    na += __popc(__ballot_sync(0xffffffffu, ca != CLS_EMPTY));
+    nb += __popc(__ballot_sync(0xffffffffu, cb != CLS_EMPTY));
+  }
+  if (lane == 0) pair_info[w] = make_int4(cnt, na, nb, na + nb);
+}
+
 // One warp per (bh, k-tile): the ascending list of non-empty q-tiles.
 __global__ void __launch_bounds__(256) classify_cols_kernel(const int32_t* __restrict__ summary,
                                                             int nBH, int nQ, int nK, int Sq,
@@ -210,8 +250,9 @@ __global__ void __launch_bounds__(256) classify_cols_kernel(const int32_t* __res
 // counts[b][hm][t] in [0, maxc] descending, ties by t ascending (longest
 // first).  One CTA per (b, h): histogram, scan in descending cost, stable
 // scatter by one warp in t order.
-__global__ void __launch_bounds__(256) order_kernel(const int32_t* __restrict__ counts, int H,
-                                                    int Hm, int nT, int maxc, int32_t* order) {
+__global__ void __launch_bounds__(256) order_kernel(const int32_t* __restrict__ counts,
+                                                    int stride, int H, int Hm, int nT, int maxc,
+                                                    int32_t* order) {
   extern __shared__ int sh[];
   int* hist = sh;             // maxc + 1
   int* cst = sh + maxc + 1;   // nT costs of this (b, h)
@@ -219,9 +260,9 @@ __global__ void __launch_bounds__(256) order_kernel(const int32_t* __restrict__ 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int bh = blockIdx.x;
   const int b = bh / H, h = bh - b * H;
-  const int32_t* src = counts + static_cast<size_t>(b * Hm + (Hm == 1 ? 0 : h)) * nT;
+  const int32_t* src = counts + static_cast<size_t>(b * Hm + (Hm == 1 ? 0 : h)) * nT * stride;
   for (int i = tid; i <= maxc; i += blockDim.x) hist[i] = 0;
-  for (int t = tid; t < nT; t += blockDim.x) cst[t] = src[t];
+  for (int t = tid; t < nT; t += blockDim.x) cst[t] = src[static_cast<size_t>(t) * stride];
   __syncthreads();
   for (int t = tid; t < nT; t += blockDim.x) atomicAdd(&hist[cst[t]], 1);
   __syncthreads();
@@ -318,6 +359,10 @@ cudaError_t launch_classify(const Plan& p, char* ws, int for_bwd, cudaStream_t s
         reinterpret_cast<int32_t*>(ws + p.L.row_list),
         reinterpret_cast<int32_t*>(ws + p.L.row_mask),
         reinterpret_cast<unsigned long long*>(ws + p.L.status + 8), p.mask_cap);
+    const int pwarps = nBH * p.nP;
+    classify_pairs_kernel<<<ceil_div(pwarps, 8), 256, 0, s>>>(
+        table, nBH, p.nQ, p.nK, p.nP, p.Skv, reinterpret_cast<int4*>(ws + p.L.pair_info),
+        reinterpret_cast<int32_t*>(ws + p.L.pair_list));
   } else {
     const int warps = nBH * p.nK;
     classify_cols_kernel<<<ceil_div(warps, 8), 256, 0, s>>>(
@@ -340,10 +385,13 @@ cudaError_t launch_tile_masks(const Plan& p, const int32_t* lts, const int32_t* 
 }
 
 cudaError_t launch_order(const Plan& p, char* ws, int for_bwd, cudaStream_t s) {
-  const int nT = for_bwd ? p.nK : p.nQ;      // units per (b, h)
-  const int maxc = for_bwd ? p.nQ : p.nK;    // largest possible cost
-  const int32_t* counts =
-      reinterpret_cast<const int32_t*>(ws + (for_bwd ? p.L.col_count : p.L.row_count));
+  // backward: k-tile columns, cost = their non-empty tiles; forward: q-tile
+  // pairs, cost = the non-empty tiles of both rows (pair_info[.][3])
+  const int nT = for_bwd ? p.nK : p.nP;          // units per (b, h)
+  const int maxc = for_bwd ? p.nQ : 2 * p.nK;    // largest possible cost
+  const int stride = for_bwd ? 1 : 4;
+  const int32_t* counts = for_bwd ? reinterpret_cast<const int32_t*>(ws + p.L.col_count)
+                                  : reinterpret_cast<const int32_t*>(ws + p.L.pair_info) + 3;
   int32_t* order = reinterpret_cast<int32_t*>(ws + (for_bwd ? p.L.bwd_order : p.L.fwd_order));
   const size_t smem = static_cast<size_t>(maxc + 1 + nT) * 4;
   const size_t limit = 200 * 1024;
@@ -352,7 +400,7 @@ cudaError_t launch_order(const Plan& p, char* ws, int for_bwd, cudaStream_t s) {
                                        static_cast<int>(limit));
   if (e != cudaSuccess) return e;
   prof_begin(K_ORDER, s);
-  order_kernel<<<p.B * p.H, 256, smem, s>>>(counts, p.H, p.Hm, nT, maxc, order);
+  order_kernel<<<p.B * p.H, 256, smem, s>>>(counts, stride, p.H, p.Hm, nT, maxc, order);
   prof_end(K_ORDER, s);
   return cudaGetLastError();
 }

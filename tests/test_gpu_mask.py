@@ -1,8 +1,9 @@
 """Mask-analysis kernels against the oracle, bit for bit (GPU).
 
-Block summary + tile classification + work lists + longest-first order +
-the partial tiles' visibility bit masks (fm_plan), bound validation, and
-localisation (fm_localize).
+Block summary + tile classification + work lists (per q-tile row, per
+q-tile pair, per k-tile column) + longest-first order + the partial tiles'
+visibility bit masks (fm_plan), bound validation, and localisation
+(fm_localize).
 """
 import numpy as np
 import pytest
@@ -95,8 +96,19 @@ def _check_plan(bounds, Sq, H=2, d=64):
             for (b, hm, qi), ent in ref_rl.items():
                 want = [(kj << 2) | c for kj, c in ent]
                 assert lst[b, hm, qi, :len(want)].tolist() == want
-            order = _ws_view(ws, L.fwd_order, B * H * nQ, torch.int32).cpu().numpy()
-            assert np.array_equal(order, om.unit_order(ref_rc, H))
+            nP = (nQ + 1) // 2
+            ref_pc, ref_cost, ref_pl = om.pair_lists(ref_table, Skv)
+            info = _ws_view(ws, L.pair_info, B * Hm * nP * 4, torch.int32).view(B, Hm, nP, 4).cpu().numpy()
+            plst = _ws_view(ws, L.pair_list, B * Hm * nP * nK, torch.int32).view(B, Hm, nP, nK).cpu().numpy()
+            assert np.array_equal(info[..., 0], ref_pc)
+            assert np.array_equal(info[..., 3], ref_cost)
+            for (b, hm, p), ent in ref_pl.items():
+                want = [(kj << 4) | (ca << 2) | cb for kj, ca, cb in ent]
+                assert plst[b, hm, p, :len(want)].tolist() == want
+                assert info[b, hm, p, 1] == sum(ca != 0 for _, ca, _ in ent)
+                assert info[b, hm, p, 2] == sum(cb != 0 for _, _, cb in ent)
+            order = _ws_view(ws, L.fwd_order, B * H * nP, torch.int32).cpu().numpy()
+            assert np.array_equal(order, om.unit_order(ref_cost, H))
             _check_tile_masks(ws, L, bounds, Sq, ref_rl)
         else:
             cnt = _ws_view(ws, L.col_count, B * Hm * nK, torch.int32).view(B, Hm, nK).cpu().numpy()
