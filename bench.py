@@ -209,11 +209,17 @@ def run_e2e(args, fm, q, k, v, do, bounds, scale, o, lse, dq, dk, dv, ws_f, ws_b
     e2e_step()
     torch.cuda.synchronize()
     e_steps = max(1, min(args.steps, 5))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
     ev0.record(stream)
     for _ in range(e_steps):
         e2e_step()
     ev1.record(stream)
     torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
     e2e_ms = ev0.elapsed_time(ev1) / e_steps
     if world > 1:
         t = torch.tensor([e2e_ms], device="cuda")

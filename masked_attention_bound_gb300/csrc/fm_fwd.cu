@@ -504,13 +504,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           }
           mbar_arrive(bar(B_MEMPTY0 + st));  // done with this stage's bits
         }
+        // row maximum: eight independent chains of three-input max
         float mx8[8];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) mx8[x] = sv[x];
+        for (int x = 0; x < 8; ++x) mx8[x] = fmax3(sv[x], sv[x + 8], sv[x + 16]);
 #pragma unroll
-        for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int c = 24; c < 120; c += 16)
+#pragma unroll
+          for (int x = 0; x < 8; ++x) mx8[x] = fmax3(mx8[x], sv[c + x], sv[c + 8 + x]);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) mx8[x] = fmaxf(mx8[x], sv[120 + x]);
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7]));
         const float m_tile = mx * P.scale_log2;
         // lazy rescale: move the reference max only when it grows by more than
         // 8 (factor 256); below that the unnormalised p stay within bf16/fp32
@@ -523,15 +528,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
         // p = exp2(s * scale*log2e - m) from the registers, packed to bf16 into
         // the first 64 columns of S (the row was read whole above)
+        // two columns per packed FMA and per packed add
+        const uint64_t sc2 = splat2(P.scale_log2), nm2 = splat2(-m_ref);
         float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           uint32_t pk[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
-            const float p0 = ex2(fmaf(sv[c4 * 32 + 2 * x], P.scale_log2, -m_ref));
-            const float p1 = ex2(fmaf(sv[c4 * 32 + 2 * x + 1], P.scale_log2, -m_ref));
-            sum4[x & 3] += p0 + p1;
+            float a0, a1;
+            fma2_bc(a0, a1, sv[c4 * 32 + 2 * x], sv[c4 * 32 + 2 * x + 1], sc2, nm2);
+            const float p0 = ex2(a0);
+            const float p1 = ex2(a1);
+            if (x & 1) add2_acc(sum4[2], sum4[3], p0, p1);
+            else add2_acc(sum4[0], sum4[1], p0, p1);
             pk[x] = pack_bf16(p0, p1);
           }
           tmem_st16(tS + c4 * 16, pk);
