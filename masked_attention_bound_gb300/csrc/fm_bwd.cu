@@ -14,9 +14,12 @@
 //                     key, so P = 0 there without a branch);
 //   bwd_kernel        one unit = one (batch, head, k-tile): K and V stay in
 //                     smem, the unit walks its column of non-empty q-tiles.
-//                     Warps 0-3: thread r owns key row r (TMEM lane r) for
-//                     S^T, dP^T, dK, dV and query row r for the dQ tile.
-//                     Warp 4: TMA loads.  Warp 5: one thread issues tcgen05:
+//                     Warps 0-7 (compute): thread r owns key row r (TMEM
+//                     lane r, warp quarter w & 3) and half of the q columns
+//                     (w >> 2) of S^T and dP^T, and half of dK / dV.
+//                     Warps 8-11 (dQ): thread r owns q row r of the dQ tile
+//                     and adds it into the fp32 accumulator.
+//                     Warp 12: TMA loads.  Warp 13: one thread issues tcgen05:
 //                       S^T = K Q^T, dP^T = V dO^T      (SS, both K-major)
 //                       dV += P^T dO                     (P^T from TMEM, dO MN-major)
 //                       dK += dS^T Q                     (dS^T smem K-major, Q MN-major)
@@ -128,7 +131,14 @@ struct BwdCfg {
   // resident per SM
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   static constexpr uint32_t T_A = 0, T_B = 128, T_DV = 256, T_DK = 384, T_COLS = 512;
-  static constexpr int THREADS = 320;  // 8 compute warps, 1 TMA warp, 1 MMA warp
+  // warpgroups 0-1: compute (P^T, dS^T, the dV/dK epilogue); warpgroup 2:
+  // dQ drain; warpgroup 3: the TMA warp, the MMA warp and two idle warps
+  static constexpr int THREADS = 512;
+  // register split (setmaxnreg): 2 x 128 x REGS_COMPUTE + 128 x REGS_DQ +
+  // 128 x REGS_PRODUCER = 65536 = THREADS x 128 registers at launch
+  static constexpr uint32_t REGS_COMPUTE = 152, REGS_DQ = 152, REGS_PRODUCER = 56;
+  static constexpr int MIN_LAUNCH_REGS =
+      (2 * 128 * REGS_COMPUTE + 128 * REGS_DQ + 128 * REGS_PRODUCER + THREADS - 1) / THREADS;
 };
 
 enum { C_KVFULL = 0, C_KVEMPTY, C_QFULL0, C_QFULL1, C_QEMPTY0, C_QEMPTY1, C_SFULL, C_PREADY,
@@ -150,17 +160,17 @@ struct BwdParams {
   int* status;
 };
 
-// Tile pipeline per q-tile t of a unit (MMA issue order on the left, compute
+// Tile pipeline per q-tile t of a unit (MMA issue order on the left, other
 // warps on the right; region A = TMEM [0,128), region B = [128,256)):
 //   S^T(t) = K Q^T -> A       [after dV(t-1) read P^T(t-1) from A]
-//                               drain dQ(t-1) from B (fp32 atomics)
-//   dP^T(t) = V dO^T -> B     [after that drain]
-//                               P^T(t) = exp2(S^T*scale*log2e - LSE*log2e) -> A
+//                               dQ warps: dQ(t-1) from B to registers
+//   dP^T(t) = V dO^T -> B     [after that read]
+//                               compute: P^T(t) = exp2(S^T*scale*log2e - LSE*log2e) -> A
+//                               dQ warps: atomics of dQ(t-1)
 //   dV += P^T(t) dO           [after P^T(t)]
-//                               dS^T(t) = P^T o (dP^T - D) -> smem
+//                               compute: dS^T(t) = P^T o (dP^T - D) -> smem
 //   dK += dS^T Q, dQ = dS K -> B   [after dS^T(t)]
-// so the drain, P and dS work of the compute warps overlaps S, dP and dV.
-// Compute warp w owns TMEM lane quarter (w & 3) and column half (w >> 2).
+// so the P, dS and dQ work overlaps S, dP and dV.
 // Bits [a, b) of a 64-bit word, with a and b clipped to [0, 64].
 __device__ __forceinline__ uint64_t row_span(int a, int b) {
   a = min(max(a, 0), 64);
@@ -188,22 +198,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr int TMA_WARP = 8, MMA_WARP = 9;
+  constexpr int DQ_WARP0 = 8, TMA_WARP = 12, MMA_WARP = 13;
 
   if (tid == 0) {
     mbar_init(bar(C_KVFULL), 1);
     mbar_init(bar(C_KVEMPTY), 1);
     mbar_init(bar(C_QFULL0), 1);
     mbar_init(bar(C_QFULL1), 1);
-    mbar_init(bar(C_QEMPTY0), 1);
-    mbar_init(bar(C_QEMPTY1), 1);
+    // a Q/dO stage is free once the tile's MMAs are done (commit) and the dQ
+    // warps, which use its dO buffer as transpose scratch, are done (128)
+    mbar_init(bar(C_QEMPTY0), 1 + 128);
+    mbar_init(bar(C_QEMPTY1), 1 + 128);
     mbar_init(bar(C_SFULL), 1);
     mbar_init(bar(C_PREADY), 256);
     mbar_init(bar(C_DVDONE), 1);
     mbar_init(bar(C_DPFULL), 1);
     mbar_init(bar(C_DSREADY), 256);
     mbar_init(bar(C_DQFULL), 1);
-    mbar_init(bar(C_DQEMPTY), 256);
+    mbar_init(bar(C_DQEMPTY), 128);
     mbar_init(bar(C_ACCFULL), 1);
     mbar_init(bar(C_ACCEMPTY), 256);
     mbar_init(bar(C_DRAIN), 1);
@@ -252,6 +264,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     return P.col_count[col];
   };
 
+  if (warp >= TMA_WARP) {
+  // producer warpgroup: small register budget (each role branch below runs
+  // after the budget change, so the compiler allocates it within the budget)
+  regs_decrease<C::REGS_PRODUCER>();
   if (warp == TMA_WARP) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -372,66 +388,84 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mbar_wait(bar(C_DRAIN), 0, P.status);
     }
     __syncwarp();
+  }  // warps 14, 15: spare warps of the producer warpgroup
+  } else if (warp >= DQ_WARP0) {
+    // ------------------------------------------------------------ dQ drain
+    // Thread r holds q row r of the tile in region B (TMEM lane r): all D
+    // columns in one TMEM round trip, region B released for the next dP^T.
+    // Straight from registers each fp32 atomic of a warp would touch 32
+    // different rows; instead the warp transposes 32 x 32 blocks through a
+    // 4 KB patch so that every reduction instruction covers four rows x 128
+    // contiguous bytes.  The patch lies in the dO buffer of this tile's Q/dO
+    // stage: the tile's MMAs have finished with it (they committed before
+    // the dQ tile), and the stage is refilled only after these warps arrive
+    // on its release barrier.  These warps do nothing else, so the
+    // reductions overlap the compute warps' P^T / dS^T work and the MMAs.
+    regs_increase<C::REGS_DQ>();
+    const int quarter = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; ok && idx < P.n_units; idx += gridDim.x) {
+      int b, h, kj;
+      const int32_t* list;
+      const int n = unit_info(idx, b, h, kj, list);
+      float* acc_bh = P.dq_acc + (static_cast<size_t>(b) * P.H + h) * P.Sq * D;
+      for (int t = 0; t < n; ++t, ++it) {
+        const int qi = list[t] >> 2;
+        const int st = it & 1;
+        if (!wait_all(C_DQFULL, it & 1)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t raw[D];
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) tmem_ld64(tbase + lane_off + C::T_B + 64 * c, raw + 64 * c);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(C_DQEMPTY));
+        const uint32_t patch = sbase + C::OFF_DO + st * C::TILE + quarter * 4096;
+        const int row0 = qi * kTile + quarter * 32;  // first q row of this warp
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {  // 32-column blocks
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t chunk = static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7);
+            const int e = c * 32 + j * 4;
+            st_shared_v4(patch + lane * 128 + chunk * 16,
+                         __float_as_uint(__uint_as_float(raw[e]) * P.scale),
+                         __float_as_uint(__uint_as_float(raw[e + 1]) * P.scale),
+                         __float_as_uint(__uint_as_float(raw[e + 2]) * P.scale),
+                         __float_as_uint(__uint_as_float(raw[e + 3]) * P.scale));
+          }
+          __syncwarp();
+          const int j = lane & 7;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rl = i * 4 + (lane >> 3);  // row within the warp's 32
+            const uint32_t chunk = static_cast<uint32_t>(j) ^ static_cast<uint32_t>(rl & 7);
+            float4 v;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                         : "r"(patch + rl * 128 + chunk * 16));
+            if (row0 + rl < P.Sq)
+              atomicAdd(reinterpret_cast<float4*>(acc_bh + static_cast<size_t>(row0 + rl) * D +
+                                                  c * 32 + j * 4),
+                        v);
+          }
+          __syncwarp();
+        }
+        // the stage may be refilled by TMA (async proxy) after these accesses
+        fence_proxy_async_smem();
+        mbar_arrive(bar(C_QEMPTY0 + st));
+      }
+    }
   } else {
     // ------------------------------------------------------------ compute warps
+    regs_increase<C::REGS_COMPUTE>();
     const int quarter = warp & 3, half = warp >> 2;
     const int r = quarter * 32 + lane;  // TMEM lane: key row (S^T, dP^T, dK, dV), q row (dQ)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int c0 = half * 64;           // this thread's 64 of the 128 q columns
     uint32_t it = 0, un = 0;
-    // dQ tile drain.  Thread r holds q row r, columns [half*D/2, +D/2) of the
-    // tile in region B.  Straight from TMEM each fp32 atomic of a warp would
-    // touch 32 different rows (16 bytes each); instead the warp transposes
-    // 32 x 32 blocks through a 4 KB patch of the dS^T buffer so that every
-    // reduction instruction covers four rows x 128 contiguous bytes.  The
-    // patch is the one this warp later fills with its own dS^T rows, and the
-    // buffer is idle here (the tile's dK/dQ MMAs have finished with it), so
-    // no other warp is involved.
-    const uint32_t patch = sDS + half * 16384 + quarter * 4096;
-    auto drain_dq = [&](uint32_t jt, int b, int h, int qi) -> bool {
-      if (!wait_all(C_DQFULL, jt & 1)) return false;
-      tc_fence_after();
-      // this thread's D/2 columns in one TMEM round trip
-      uint32_t raw[D / 2];
-      if constexpr (D == 128) tmem_ld64(tbase + lane_off + C::T_B + half * (D / 2), raw);
-      else tmem_ld32(tbase + lane_off + C::T_B + half * (D / 2), raw);
-      tmem_wait_ld();
-      // region B may be reused (by the next dP^T) as soon as it has been read
-      tc_fence_before();
-      mbar_arrive(bar(C_DQEMPTY));
-      const int row0 = qi * kTile + quarter * 32;  // first q row of this warp
-      float* acc_bh = P.dq_acc + (static_cast<size_t>(b) * P.H + h) * P.Sq * D + half * (D / 2);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {  // 32-column blocks
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t chunk = static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7);
-          const int e = c * 32 + j * 4;
-          st_shared_v4(patch + lane * 128 + chunk * 16,
-                       __float_as_uint(__uint_as_float(raw[e]) * P.scale),
-                       __float_as_uint(__uint_as_float(raw[e + 1]) * P.scale),
-                       __float_as_uint(__uint_as_float(raw[e + 2]) * P.scale),
-                       __float_as_uint(__uint_as_float(raw[e + 3]) * P.scale));
-        }
-        __syncwarp();
-        const int j = lane & 7;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rl = i * 4 + (lane >> 3);  // row within the warp's 32
-          const uint32_t chunk = static_cast<uint32_t>(j) ^ static_cast<uint32_t>(rl & 7);
-          float4 v;
-          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                       : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                       : "r"(patch + rl * 128 + chunk * 16));
-          if (row0 + rl < P.Sq)
-            atomicAdd(reinterpret_cast<float4*>(acc_bh + static_cast<size_t>(row0 + rl) * D +
-                                                c * 32 + j * 4),
-                      v);
-        }
-        __syncwarp();
-      }
-      return true;
-    };
     bool ok = true;
     for (int idx = blockIdx.x; ok && idx < P.n_units; idx += gridDim.x) {
       int b, h, kj;
@@ -463,7 +497,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         ute = __ldg(P.bounds[3] + at);
       }
       const bool key_ragged = (kj == P.nK - 1) && (P.Skv & (kTile - 1));
-      int prev_qi = -1;
       for (int t = 0; t < n; ++t, ++it) {
         const int e = list[t];
         const int qi = e >> 2;
@@ -471,8 +504,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         const int st = it & 1;
         const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LD + st * 1024) + c0;
         const float* del_s = lse_s + 128;
-        // ---- drain the previous tile's dQ from region B (overlaps S^T(t))
-        if (t > 0 && !drain_dq(it - 1, b, h, prev_qi)) { ok = false; break; }
         // ---- P^T = exp2(S^T * scale*log2e - LSE*log2e), hidden entries 0
         if (!wait_all(C_SFULL, it & 1)) { ok = false; break; }
         // the LSE/D of this stage arrived with the Q/dO tiles
@@ -545,10 +576,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(C_DSREADY));
-        prev_qi = qi;
       }
       if (!ok) break;
-      if (!drain_dq(it - 1, b, h, prev_qi)) { ok = false; break; }
       // ---- epilogue: dV and scale * dK, this thread's half of the columns;
       // both are read from TMEM first so the next unit's MMAs may start
       if (!wait_all(C_ACCFULL, un & 1)) { ok = false; break; }
@@ -640,6 +669,12 @@ static fm_status launch_bwd_d(const Plan& p, const fm_desc& desc, const TensorAr
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)
     return FM_ERR_CUDA;
+  {
+    // the setmaxnreg split must fit in the registers the block launches with
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return FM_ERR_CUDA;
+    if (fa.numRegs < C::MIN_LAUNCH_REGS) return FM_ERR_UNSUPPORTED;
+  }
   const int grid = P.n_units < num_sms() ? P.n_units : num_sms();
   prof_begin(K_BWD, s);
   kern<<<grid, C::THREADS, C::SMEM, s>>>(P, tq, tk, tv, tdo);
