@@ -19,7 +19,8 @@
 //                     (w >> 2) of S^T and dP^T, and half of dK / dV.
 //                     Warps 8-11 (dQ): thread r owns q row r of the dQ tile
 //                     and adds it into the fp32 accumulator.
-//                     Warp 12: TMA loads.  Warp 13: one thread issues tcgen05:
+//                     Warp 12: K/V loads, warp 14: Q/dO/LSE/D loads (TMA).
+//                     Warp 13: one thread issues tcgen05:
 //                       S^T = K Q^T, dP^T = V dO^T      (SS, both K-major)
 //                       dV += P^T dO                     (P^T from TMEM, dO MN-major)
 //                       dK += dS^T Q                     (dS^T smem K-major, Q MN-major)
@@ -132,7 +133,8 @@ struct BwdCfg {
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   static constexpr uint32_t T_A = 0, T_B = 128, T_DV = 256, T_DK = 384, T_COLS = 512;
   // warpgroups 0-1: compute (P^T, dS^T, the dV/dK epilogue); warpgroup 2:
-  // dQ drain; warpgroup 3: the TMA warp, the MMA warp and two idle warps
+  // dQ drain; warpgroup 3: the K/V load warp, the MMA warp, the Q/dO load
+  // warp and one idle warp
   static constexpr int THREADS = 512;
   // register split (setmaxnreg): 2 x 128 x REGS_COMPUTE + 128 x REGS_DQ +
   // 128 x REGS_PRODUCER = 65536 = THREADS x 128 registers at launch
@@ -198,7 +200,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr int DQ_WARP0 = 8, TMA_WARP = 12, MMA_WARP = 13;
+  constexpr int DQ_WARP0 = 8, TMA_WARP = 12, MMA_WARP = 13, QTMA_WARP = 14;
 
   if (tid == 0) {
     mbar_init(bar(C_KVFULL), 1);
@@ -227,9 +229,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     tmem_relinquish();
   }
   if (warp == TMA_WARP && lane == 0) {
-    tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+  }
+  if (warp == QTMA_WARP && lane == 0) {
+    tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmDO);
   }
   tc_fence_before();
@@ -269,11 +273,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   // after the budget change, so the compiler allocates it within the budget)
   regs_decrease<C::REGS_PRODUCER>();
   if (warp == TMA_WARP) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ K / V loads
+    // once per unit, after the previous unit's MMAs are done with K and V
     if (lane == 0) {
-      uint32_t it = 0, un = 0;
-      bool ok = true;
-      for (int idx = blockIdx.x; ok && idx < P.n_units; idx += gridDim.x) {
+      uint32_t un = 0;
+      for (int idx = blockIdx.x; idx < P.n_units; idx += gridDim.x) {
         int b, h, kj;
         const int32_t* list;
         const int n = unit_info(idx, b, h, kj, list);
@@ -286,6 +290,22 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tma_load_4d(sK + s * 16384, &tmK, bar(C_KVFULL), s * 64, h, kj * kTile, b);
           tma_load_4d(sV + s * 16384, &tmV, bar(C_KVFULL), s * 64, h, kj * kTile, b);
         }
+      }
+      // drain every issued copy before exit
+      if (un > 0) mbar_wait(bar(C_KVFULL), (un - 1) & 1, P.status);
+    }
+    __syncwarp();
+  } else if (warp == QTMA_WARP) {
+    // ------------------------------------------------------------ Q / dO / LSE / D loads
+    // its own warp, so the next unit's first tiles load as soon as a stage
+    // is free, without waiting for the unit's K and V
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; ok && idx < P.n_units; idx += gridDim.x) {
+        int b, h, kj;
+        const int32_t* list;
+        const int n = unit_info(idx, b, h, kj, list);
         const size_t bh_row = (static_cast<size_t>(b) * P.H + h) * rows_pad;
         for (int t = 0; t < n; ++t, ++it) {
           const int qi = list[t] >> 2;
@@ -309,7 +329,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       // drain every issued copy before exit
       for (uint32_t k = (it > 2u ? it - 2u : 0u); k < it; ++k)
         mbar_wait(bar(C_QFULL0 + (k & 1)), (k >> 1) & 1, P.status);
-      if (un > 0) mbar_wait(bar(C_KVFULL), (un - 1) & 1, P.status);
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
@@ -388,7 +407,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mbar_wait(bar(C_DRAIN), 0, P.status);
     }
     __syncwarp();
-  }  // warps 14, 15: spare warps of the producer warpgroup
+  }  // warp 15: spare warp of the producer warpgroup
   } else if (warp >= DQ_WARP0) {
     // ------------------------------------------------------------ dQ drain
     // Thread r holds q row r of the tile in region B (TMEM lane r): all D
