@@ -69,8 +69,9 @@ typedef struct {
  * nQ = ceil(Sq/128), nK = ceil(Skv/128).  List entries are
  * (tile_index << 2) | class with class 1 = PARTIAL, 2 = FULL. */
 typedef struct {
-  size_t status;     /* int32[4]: [0] device status bits, [1] unused, [2..3] uint64
-                        count of mask slots asked for (forward)                    */
+  size_t status;     /* int32[4]: [0] device status bits, [1] units claimed by the
+                        attention kernel's CTAs, [2..3] uint64 count of mask slots
+                        asked for (forward); zeroed by every call               */
   size_t summary;    /* int32 [B][Hm][nK][8]: min/max of LTS, LTE, UTS, UTE per k-block */
   size_t table;      /* uint8 [B][Hm][nQ][nK]: 0 EMPTY, 1 PARTIAL, 2 FULL           */
   size_t row_count;  /* int32 [B][Hm][nQ]: non-empty tiles per q-tile row             */

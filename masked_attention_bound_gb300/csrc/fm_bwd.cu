@@ -125,8 +125,9 @@ struct BwdCfg {
   static constexpr int OFF_DO = OFF_Q + 2 * TILE;     // 2 stages
   static constexpr int OFF_DS = OFF_DO + 2 * TILE;    // 128 x 128 bf16, [key][q]
   static constexpr int OFF_LD = OFF_DS + 128 * 128 * 2;  // 2 stages x (LSE*log2e, D) fp32
-  static constexpr int OFF_BAR = OFF_LD + 2 * 1024;
-  static constexpr int NBAR = 20;
+  static constexpr int OFF_RING = OFF_LD + 2 * 1024;   // [UNIT_RING] claimed units
+  static constexpr int OFF_BAR = OFF_RING + 16;
+  static constexpr int NBAR = 24;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
   // at least 120 KB so that one CTA (which takes all 512 TMEM columns) is
   // resident per SM
@@ -144,7 +145,16 @@ struct BwdCfg {
 };
 
 enum { C_KVFULL = 0, C_KVEMPTY, C_QFULL0, C_QFULL1, C_QEMPTY0, C_QEMPTY1, C_SFULL, C_PREADY,
-       C_DVDONE, C_DPFULL, C_DSREADY, C_DQFULL, C_DQEMPTY, C_ACCFULL, C_ACCEMPTY, C_DRAIN };
+       C_DVDONE, C_DPFULL, C_DSREADY, C_DQFULL, C_DQEMPTY, C_ACCFULL, C_ACCEMPTY, C_DRAIN,
+       C_UFULL0, C_UEMPTY0 = C_UFULL0 + 4 };
+// Units are claimed at run time (one atomic counter per launch, in the
+// workspace) by the Q/dO load warp, the first role to need the next unit,
+// and handed to the other roles that walk units through a ring of
+// UNIT_RING slots; U_READERS warps read every slot: the K/V load warp, the
+// MMA warp, the eight compute warps and the four dQ warps.  Claiming just in
+// time keeps the units in flight on all CTAs close together in the
+// head-major order (Q/dO stay in L2).
+constexpr int UNIT_RING = 4, U_READERS = 14;
 
 struct BwdParams {
   int B, H, Hm, Sq, Skv, nQ, nK, n_units;
@@ -153,6 +163,7 @@ struct BwdParams {
   const int32_t* col_count;
   const int32_t* col_list;
   const int32_t* order;
+  int* next_unit;         // claim counter (zero at launch)
   const float* delta;     // [B][H][nQ*128]
   const float* lse_log2;  // [B][H][nQ*128]
   float* dq_acc;          // [B][H][Sq][D]
@@ -197,6 +208,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sDS = sbase + C::OFF_DS;
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * i; };
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + C::OFF_RING);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -221,6 +233,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(bar(C_ACCFULL), 1);
     mbar_init(bar(C_ACCEMPTY), 256);
     mbar_init(bar(C_DRAIN), 1);
+    for (int r = 0; r < UNIT_RING; ++r) {
+      mbar_init(bar(C_UFULL0 + r), 1);
+      mbar_init(bar(C_UEMPTY0 + r), U_READERS);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -267,6 +283,25 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     list = P.col_list + static_cast<size_t>(col) * P.nQ;
     return P.col_count[col];
   };
+  // the n-th claimed unit (-1: none left, or the launch was aborted).
+  // claimed_one: one thread of the warp reads and releases the ring slot;
+  // claimed_all: all 32 lanes call it, lane 0 reads, the others get a copy
+  auto claimed_one = [&](uint32_t& n) -> int {
+    int idx = -1;
+    const int r = n % UNIT_RING;
+    if (wait(C_UFULL0 + r, (n / UNIT_RING) & 1)) {
+      idx = ring[r];
+      mbar_arrive(bar(C_UEMPTY0 + r));
+    }
+    ++n;
+    return idx;
+  };
+  auto claimed_all = [&](uint32_t& n) -> int {
+    uint32_t m = n;
+    const int idx = lane == 0 ? claimed_one(m) : -1;
+    ++n;
+    return __shfl_sync(0xffffffffu, idx, 0);
+  };
 
   if (warp >= TMA_WARP) {
   // producer warpgroup: small register budget (each role branch below runs
@@ -276,8 +311,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     // ------------------------------------------------------------ K / V loads
     // once per unit, after the previous unit's MMAs are done with K and V
     if (lane == 0) {
-      uint32_t un = 0;
-      for (int idx = blockIdx.x; idx < P.n_units; idx += gridDim.x) {
+      uint32_t un = 0, cn = 0;
+      while (true) {
+        const int idx = claimed_one(cn);
+        if (idx < 0) break;
         int b, h, kj;
         const int32_t* list;
         const int n = unit_info(idx, b, h, kj, list);
@@ -300,9 +337,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     // its own warp, so the next unit's first tiles load as soon as a stage
     // is free, without waiting for the unit's K and V
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t it = 0, cn = 0;
       bool ok = true;
-      for (int idx = blockIdx.x; ok && idx < P.n_units; idx += gridDim.x) {
+      while (ok) {
+        // claim the next unit and publish it to the other roles
+        const int r = cn % UNIT_RING;
+        const uint32_t use = cn / UNIT_RING;
+        ++cn;
+        if (use > 0 && !wait(C_UEMPTY0 + r, (use - 1) & 1)) break;
+        int idx = atomicAdd(P.next_unit, 1);
+        if (idx >= P.n_units) idx = -1;
+        ring[r] = idx;
+        mbar_arrive(bar(C_UFULL0 + r));
+        if (idx < 0) break;
         int b, h, kj;
         const int32_t* list;
         const int n = unit_info(idx, b, h, kj, list);
@@ -337,9 +384,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t idKB = idesc_bf16(128, D, false, true);     // dV, dK (B MN-major)
       constexpr uint32_t idDQ = idesc_bf16(128, D, true, true);      // dQ (A, B MN-major)
-      uint32_t it = 0, un = 0;
+      uint32_t it = 0, un = 0, cn = 0;
       bool ok = true;
-      for (int idx = blockIdx.x; ok && idx < P.n_units; idx += gridDim.x) {
+      while (ok) {
+        const int idx = claimed_one(cn);
+        if (idx < 0) break;
         int b, h, kj;
         const int32_t* list;
         const int n = unit_info(idx, b, h, kj, list);
@@ -423,9 +472,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     regs_increase<C::REGS_DQ>();
     const int quarter = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    uint32_t it = 0;
+    uint32_t it = 0, cn = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; ok && idx < P.n_units; idx += gridDim.x) {
+    while (ok) {
+      const int idx = claimed_all(cn);
+      if (idx < 0) break;
       int b, h, kj;
       const int32_t* list;
       const int n = unit_info(idx, b, h, kj, list);
@@ -484,9 +535,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const int r = quarter * 32 + lane;  // TMEM lane: key row (S^T, dP^T, dK, dV), q row (dQ)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int c0 = half * 64;           // this thread's 64 of the 128 q columns
-    uint32_t it = 0, un = 0;
+    uint32_t it = 0, un = 0, cn = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; ok && idx < P.n_units; idx += gridDim.x) {
+    while (ok) {
+      const int idx = claimed_all(cn);
+      if (idx < 0) break;
       int b, h, kj;
       const int32_t* list;
       const int n = unit_info(idx, b, h, kj, list);
@@ -674,6 +727,7 @@ static fm_status launch_bwd_d(const Plan& p, const fm_desc& desc, const TensorAr
   P.col_count = reinterpret_cast<const int32_t*>(ws + p.L.col_count);
   P.col_list = reinterpret_cast<const int32_t*>(ws + p.L.col_list);
   P.order = reinterpret_cast<const int32_t*>(ws + p.L.bwd_order);
+  P.next_unit = reinterpret_cast<int*>(ws + p.L.status) + 1;
   P.delta = delta;
   P.lse_log2 = lse2;
   P.dq_acc = acc;

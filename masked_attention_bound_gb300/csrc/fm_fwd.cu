@@ -45,8 +45,9 @@ struct FwdCfg {
   static constexpr int OFF_V = OFF_K + 2 * TILE;               // 2 stages
   static constexpr int OFF_MSK = OFF_V + 2 * TILE;             // [stage][slot] bit masks
   static constexpr int OFF_DESC = OFF_MSK + 4 * kMaskBytes;    // [stage] entry word
-  static constexpr int OFF_BAR = OFF_DESC + 16;
-  static constexpr int NBAR = 24;
+  static constexpr int OFF_RING = OFF_DESC + 16;               // [UNIT_RING] claimed units
+  static constexpr int OFF_BAR = OFF_RING + 16;
+  static constexpr int NBAR = 32;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
   // at least 120 KB so that one CTA (which takes all 512 TMEM columns) is
   // resident per SM
@@ -66,8 +67,16 @@ struct FwdCfg {
 // barrier slots; "s" = q-tile slot (0 = a, 1 = b), "st" = K/V stage (0/1)
 enum {
   B_QFULL0 = 0, B_QEMPTY0 = 2, B_SFULL0 = 4, B_PFULL0 = 6, B_PVDONE0 = 8, B_OEMPTY0 = 10,
-  B_KFULL0 = 12, B_KEMPTY0 = 14, B_VFULL0 = 16, B_VEMPTY0 = 18, B_MEMPTY0 = 20, B_DRAIN = 22
+  B_KFULL0 = 12, B_KEMPTY0 = 14, B_VFULL0 = 16, B_VEMPTY0 = 18, B_MEMPTY0 = 20, B_DRAIN = 22,
+  B_UFULL0 = 23, B_UEMPTY0 = 27
 };
+// Units are claimed at run time (one atomic counter per launch, in the
+// workspace) by the K/mask load warp when it is ready to load the next one,
+// and handed to the other roles that walk units through a ring of
+// UNIT_RING slots; U_READERS warps read every slot: the V load warp and the
+// eight softmax warps.  Claiming just in time keeps the units in flight on
+// all CTAs close together in the head-major order (K/V stay in L2).
+constexpr int UNIT_RING = 4, U_READERS = 9;
 
 // entry word the load warp hands to the MMA warp: the pair-list classes in
 // bits 0-3 (class_b bits 0-1, class_a bits 2-3), then whether this entry is
@@ -75,6 +84,8 @@ enum {
 // within its unit
 constexpr uint32_t E_A = 12u, E_B = 3u, E_FIRST_A = 16u, E_LAST_A = 32u, E_FIRST_B = 64u,
                    E_LAST_B = 128u;
+// the word of the entry after the CTA's last one: no tiles, end of the stream
+constexpr uint32_t E_END = 256u;
 
 struct FwdParams {
   int B, H, Hm, Sq, Skv, nQ, nK, nP, n_units;
@@ -83,6 +94,7 @@ struct FwdParams {
   const int4* pair_info;    // per pair row: entries, tiles of 2p, tiles of 2p+1, sum
   const int32_t* pair_list;
   const int32_t* order;
+  int* next_unit;           // claim counter (zero at launch)
   const int32_t* row_mask;  // first visibility-mask slot of a q-tile row's partial tiles, -1: none
   const uint8_t* masks;     // 2 KB per slot: 128 rows x 128 column bits, set = hidden
   __nv_bfloat16* o;
@@ -91,9 +103,10 @@ struct FwdParams {
   int* status;
 };
 
-// The CTA's units are idx = blockIdx.x + k * gridDim.x, k = 0, 1, 2, ...;
-// every role walks them in that order and their entries one by one, so all
-// agree on the K/V stage (entry count mod 2) and the barrier phases.
+// Each CTA claims units idx = 0, 1, 2, ... of the longest-first order as it
+// finishes earlier ones; every role walks the claimed units in claim order
+// and their entries one by one, so all agree on the K/V stage (entry count
+// mod 2) and the barrier phases.
 struct PairUnit {
   int b, h, qa, prow, row_a, n, na, nb;
 };
@@ -141,6 +154,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   auto bar = [&](int i) { return bar0 + 8u * i; };
   uint4* msk = reinterpret_cast<uint4*>(smem + C::OFF_MSK);  // [stage * 2 + slot][128 rows]
   volatile uint32_t* desc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_DESC);
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + C::OFF_RING);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -164,6 +178,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       mbar_init(bar(B_MEMPTY0 + s), 256);
     }
     mbar_init(bar(B_DRAIN), 1);
+    for (int r = 0; r < UNIT_RING; ++r) {
+      mbar_init(bar(B_UFULL0 + r), 1);
+      mbar_init(bar(B_UEMPTY0 + r), U_READERS);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -194,6 +212,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   auto wait_all = [&](int b, uint32_t parity) -> bool {
     const bool ok = wait(b, parity);
     return __all_sync(0xffffffffu, ok);
+  };
+  // the n-th claimed unit (-1: none left, or the launch was aborted); all 32
+  // lanes call it, lane 0 reads the ring slot and releases it
+  auto claimed = [&](uint32_t& n) -> int {
+    int idx = -1;
+    if (lane == 0) {
+      const int r = n % UNIT_RING;
+      if (wait(B_UFULL0 + r, (n / UNIT_RING) & 1)) {
+        idx = ring[r];
+        mbar_arrive(bar(B_UEMPTY0 + r));
+      }
+    }
+    ++n;
+    return __shfl_sync(0xffffffffu, idx, 0);
   };
 
   if (warp >= 8) {
@@ -234,12 +266,28 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         rows[g * 32 + lane] = mine;
       }
     };
-    uint32_t e = 0;
+    uint32_t e = 0, un = 0;
     Pair<uint32_t> qn{0, 0};
     bool ok = true;
-    for (int k = 0; ok; ++k) {
-      const int idx = blockIdx.x + k * gridDim.x;
-      if (idx >= P.n_units) break;
+    while (ok) {
+      // claim the next unit and publish it to the other roles
+      int idx = -1;
+      if (lane == 0) {
+        const int r = un % UNIT_RING;
+        const uint32_t use = un / UNIT_RING;
+        if (use == 0 || wait(B_UEMPTY0 + r, (use - 1) & 1)) {
+          idx = atomicAdd(P.next_unit, 1);
+          if (idx >= P.n_units) idx = -1;
+          ring[r] = idx;
+          mbar_arrive(bar(B_UFULL0 + r));
+        } else {
+          ok = false;
+        }
+      }
+      ++un;
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (idx < 0) break;
       const PairUnit u = unit_of(P, idx);
       if (u.n == 0) continue;
 #pragma unroll
@@ -313,23 +361,39 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
       }
     }
-    // drain: every issued copy has landed before the CTA may exit
+    // drain: every issued copy has landed before the CTA may exit (before
+    // the end marker below, which completes one more phase of a stage)
     if (lane == 0) {
       for (uint32_t x = (e > 2u ? e - 2u : 0u); x < e; ++x)
         mbar_wait(bar(B_KFULL0 + (x & 1)), (x >> 1) & 1, P.status);
       if (qn.v0 > 0) mbar_wait(bar(B_QFULL0), (qn.v0 - 1) & 1, P.status);
       if (qn.v1 > 0) mbar_wait(bar(B_QFULL0 + 1), (qn.v1 - 1) & 1, P.status);
     }
+    // the end marker: one more entry word, no tiles, so the MMA warp stops.
+    // Like any entry it waits until the entry two before has been read by
+    // the MMAs and by the softmax threads that read its bits: those threads
+    // wait on this stage's KFULL barrier, which must not run two phases
+    // ahead of them.
+    if (ok) {
+      const int st = e & 1;
+      const uint32_t use = e >> 1;
+      if (use > 0) ok = wait_all(B_KEMPTY0 + st, (use - 1) & 1);
+      if (ok && use > 0) ok = wait_all(B_MEMPTY0 + st, (use - 1) & 1);
+      if (ok && lane == 0) {
+        desc[st] = E_END;
+        mbar_arrive(bar(B_KFULL0 + st));
+      }
+    }
     __syncwarp();
   } else if (warp == V_WARP) {
     // ------------------------------------------------------------ V loads
     // its own warp, so a V stage that is still in use never holds up K loads
-    if (lane == 0) {
-      uint32_t e = 0;
-      bool ok = true;
-      for (int k = 0; ok; ++k) {
-        const int idx = blockIdx.x + k * gridDim.x;
-        if (idx >= P.n_units) break;
+    uint32_t e = 0, un = 0;
+    bool ok = true;
+    while (ok) {
+      const int idx = claimed(un);
+      if (idx < 0) break;
+      if (lane == 0) {
         const PairUnit u = unit_of(P, idx);
         for (int t = 0; t < u.n; ++t, ++e) {
           const int kj = P.pair_list[static_cast<size_t>(u.prow) * P.nK + t] >> 4;
@@ -343,20 +407,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                         x * 64, u.h, kj * kTile, u.b);
         }
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    // drain: every issued copy has landed before the CTA may exit
+    if (lane == 0)
       for (uint32_t x = (e > 2u ? e - 2u : 0u); x < e; ++x)
         mbar_wait(bar(B_VFULL0 + (x & 1)), (x >> 1) & 1, P.status);
-    }
     __syncwarp();
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
-    // entries this CTA walks: the lanes sum the units' counts
-    uint32_t total = 0;
-    for (long long k0 = 0;; k0 += 32) {
-      if (blockIdx.x + k0 * gridDim.x >= P.n_units) break;
-      const long long idx = blockIdx.x + (k0 + lane) * gridDim.x;
-      const int n = idx < P.n_units ? unit_of(P, static_cast<int>(idx)).n : 0;
-      total += static_cast<uint32_t>(__reduce_add_sync(0xffffffffu, n));
-    }
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
@@ -408,23 +467,24 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         mma_commit(bar(B_PVDONE0 + s));
         return true;
       };
-      bool ok = true;
-      if (total > 0) {
-        uint32_t fc = 0;
-        ok = entry(0, fc);
-        if (ok && (fc & E_A)) ok = issue_s(0, 0, fc);
+      // entries arrive in order until the end marker
+      uint32_t fc = 0;
+      bool ok = entry(0, fc);
+      if (ok && !(fc & E_END)) {
+        if (fc & E_A) ok = issue_s(0, 0, fc);
         if (ok && (fc & E_B)) ok = issue_s(1, 0, fc);
         if (ok) mma_commit(bar(B_KEMPTY0));
-        for (uint32_t j = 0; ok && j < total; ++j) {
-          const bool more = j + 1 < total;
+        for (uint32_t j = 0; ok; ++j) {
           uint32_t fn = 0;
-          if ((fc & E_A) && !issue_pv(0, j, fc)) { ok = false; break; }
-          if (more && !entry(j + 1, fn)) { ok = false; break; }
-          if (more && (fn & E_A) && !issue_s(0, j + 1, fn)) { ok = false; break; }
-          if ((fc & E_B) && !issue_pv(1, j, fc)) { ok = false; break; }
+          if ((fc & E_A) && !issue_pv(0, j, fc)) break;
+          if (!entry(j + 1, fn)) break;
+          const bool more = !(fn & E_END);
+          if (more && (fn & E_A) && !issue_s(0, j + 1, fn)) break;
+          if ((fc & E_B) && !issue_pv(1, j, fc)) break;
           mma_commit(bar(B_VEMPTY0 + (j & 1)));
-          if (more && (fn & E_B) && !issue_s(1, j + 1, fn)) { ok = false; break; }
-          if (more) mma_commit(bar(B_KEMPTY0 + ((j + 1) & 1)));
+          if (more && (fn & E_B) && !issue_s(1, j + 1, fn)) break;
+          if (!more) break;
+          mma_commit(bar(B_KEMPTY0 + ((j + 1) & 1)));
           fc = fn;
         }
       }
@@ -442,11 +502,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tbase + lane_off + 128 * slot;
     const uint32_t tO = tbase + lane_off + 256 + 128 * slot;
-    uint32_t e = 0, j = 0;  // entries walked, tiles of this slot done
+    uint32_t e = 0, j = 0, un = 0;  // entries walked, tiles of this slot done, units claimed
     bool ok = true;
-    for (int k = 0; ok; ++k) {
-      const int idx = blockIdx.x + k * gridDim.x;
-      if (idx >= P.n_units) break;
+    while (ok) {
+      const int idx = claimed(un);
+      if (idx < 0) break;
       const PairUnit u = unit_of(P, idx);
       const int qt = u.qa + slot;
       if (qt >= P.nQ) {  // odd nQ: the last pair has no second q-tile
@@ -619,6 +679,7 @@ static fm_status launch_fwd_d(const Plan& p, const fm_desc& desc, const TensorAr
   P.pair_info = reinterpret_cast<const int4*>(ws + p.L.pair_info);
   P.pair_list = reinterpret_cast<const int32_t*>(ws + p.L.pair_list);
   P.order = reinterpret_cast<const int32_t*>(ws + p.L.fwd_order);
+  P.next_unit = reinterpret_cast<int*>(ws + p.L.status) + 1;
   P.row_mask = reinterpret_cast<const int32_t*>(ws + p.L.row_mask);
   P.masks = reinterpret_cast<const uint8_t*>(ws + p.L.masks);
   P.o = static_cast<__nv_bfloat16*>(t.o_out);
