@@ -94,7 +94,7 @@ typedef struct {
                         k-tiles, ascending, (kj << 4) | (class_2p << 2) | class_2p+1,
                         a non-empty ragged last k-tile as PARTIAL (forward only)   */
   size_t delta;      /* float [B][H][nQ*128]: D_i = dO_i . O_i, 0 past Sq (backward)  */
-  size_t lse_log2;   /* float [B][H][nQ*128]: LSE_i * log2(e), +inf for rows that see
+  size_t lse_log2;   /* float [B][H][nQ*128]: -LSE_i * log2(e), -inf for rows that see
                         no key and past Sq (backward only)                          */
   size_t dq_acc;     /* float [B][H][Sq][d]: fp32 dQ accumulator (backward only)      */
   size_t total;      /* bytes needed */

@@ -9,8 +9,8 @@
 //   dK = scale dS^T Q,  dQ = scale dS K.
 //
 // Three kernels:
-//   bwd_pre_kernel    D_i and LSE_i*log2(e) per query row, padded to whole
-//                     128-row tiles (+inf / 0 past Sq and on rows that see no
+//   bwd_pre_kernel    D_i and -LSE_i*log2(e) per query row, padded to whole
+//                     128-row tiles (-inf / 0 past Sq and on rows that see no
 //                     key, so P = 0 there without a branch);
 //   bwd_kernel        one unit = one (batch, head, k-tile): K and V stay in
 //                     smem, the unit walks its column of non-empty q-tiles.
@@ -39,55 +39,55 @@
 namespace fm {
 
 // ------------------------------------------------------------------ preprocess
-// One warp per (b, h, row) over nQ*128 padded rows.
+// One thread per (b, h, row) over nQ*128 padded rows: the row's D values of O
+// and of dO (one 2D-byte run each) are loaded whole, so every thread keeps
+// 4D bytes of reads in flight; consecutive threads take consecutive rows,
+// so the two fp32 outputs are written coalesced.
 template <int D>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
+__global__ void __launch_bounds__(128) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dout,
                                                       int64_t os0, int64_t os1, int64_t os2,
                                                       const float* __restrict__ lse, int B, int H,
                                                       int Sq, int rows_pad, float* delta,
                                                       float* lse_log2) {
-  const int lane = threadIdx.x & 31;
-  const long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long w = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long total = static_cast<long long>(B) * H * rows_pad;
   if (w >= total) return;
   const int i = static_cast<int>(w % rows_pad);
   const int bh = static_cast<int>(w / rows_pad);
   const int b = bh / H, h = bh - b * H;
   float dsum = 0.f;
-  float l2 = INFINITY;
+  float l2 = -INFINITY;
   if (i < Sq) {
     const size_t at = static_cast<size_t>(b) * os0 + static_cast<size_t>(i) * os1 +
                       static_cast<size_t>(h) * os2;
-    constexpr int PER = D / 32;  // elements per lane: 4 (d=128) or 2 (d=64)
-    if constexpr (PER == 4) {
-      const uint2 a = *reinterpret_cast<const uint2*>(o + at + lane * 4);
-      const uint2 g = *reinterpret_cast<const uint2*>(dout + at + lane * 4);
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+    const uint4* a4 = reinterpret_cast<const uint4*>(o + at);
+    const uint4* g4 = reinterpret_cast<const uint4*>(dout + at);
+    uint4 a[D / 8], g[D / 8];
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
+    for (int c = 0; c < D / 8; ++c) {
+      a[c] = __ldg(a4 + c);
+      g[c] = __ldg(g4 + c);
+    }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[c]);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g[c]);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
         const float2 x = __bfloat1622float2(a2[t]);
         const float2 y = __bfloat1622float2(g2[t]);
-        dsum = fmaf(x.x, y.x, dsum);
-        dsum = fmaf(x.y, y.y, dsum);
+        acc[t] = fmaf(x.x, y.x, acc[t]);
+        acc[t] = fmaf(x.y, y.y, acc[t]);
       }
-    } else {
-      const uint32_t a = *reinterpret_cast<const uint32_t*>(o + at + lane * 2);
-      const uint32_t g = *reinterpret_cast<const uint32_t*>(dout + at + lane * 2);
-      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
-      const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g));
-      dsum = fmaf(x.x, y.x, x.y * y.y);
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+    dsum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     const float L = lse[static_cast<size_t>(bh) * Sq + i];
-    l2 = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
+    l2 = (L == -INFINITY) ? -INFINITY : -L * 1.4426950408889634f;
   }
-  if (lane == 0) {
-    delta[static_cast<size_t>(bh) * rows_pad + i] = dsum;
-    lse_log2[static_cast<size_t>(bh) * rows_pad + i] = l2;
-  }
+  delta[static_cast<size_t>(bh) * rows_pad + i] = dsum;
+  lse_log2[static_cast<size_t>(bh) * rows_pad + i] = l2;
 }
 
 // ------------------------------------------------------------------ dQ convert
@@ -124,7 +124,7 @@ struct BwdCfg {
   static constexpr int OFF_Q = OFF_V + TILE;          // 2 stages
   static constexpr int OFF_DO = OFF_Q + 2 * TILE;     // 2 stages
   static constexpr int OFF_DS = OFF_DO + 2 * TILE;    // 128 x 128 bf16, [key][q]
-  static constexpr int OFF_LD = OFF_DS + 128 * 128 * 2;  // 2 stages x (LSE*log2e, D) fp32
+  static constexpr int OFF_LD = OFF_DS + 128 * 128 * 2;  // 2 stages x (-LSE*log2e, D) fp32
   static constexpr int OFF_RING = OFF_LD + 2 * 1024;   // [UNIT_RING] claimed units
   static constexpr int OFF_BAR = OFF_RING + 16;
   static constexpr int NBAR = 24;
@@ -586,13 +586,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           uint32_t raw[64];
           tmem_ld64(tbase + lane_off + C::T_A + c0, raw);
           tmem_wait_ld();
+          // two columns per packed FMA: S^T * scale*log2e + (-LSE*log2e)
+          const uint64_t sc2 = splat2(P.scale_log2);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float4 L = *reinterpret_cast<const float4*>(lse_s + 4 * i);
-            p[4 * i + 0] = ex2(fmaf(__uint_as_float(raw[4 * i + 0]), P.scale_log2, -L.x));
-            p[4 * i + 1] = ex2(fmaf(__uint_as_float(raw[4 * i + 1]), P.scale_log2, -L.y));
-            p[4 * i + 2] = ex2(fmaf(__uint_as_float(raw[4 * i + 2]), P.scale_log2, -L.z));
-            p[4 * i + 3] = ex2(fmaf(__uint_as_float(raw[4 * i + 3]), P.scale_log2, -L.w));
+            float a0, a1, a2, a3;
+            fma2_bv(a0, a1, __uint_as_float(raw[4 * i + 0]), __uint_as_float(raw[4 * i + 1]), sc2,
+                    L.x, L.y);
+            fma2_bv(a2, a3, __uint_as_float(raw[4 * i + 2]), __uint_as_float(raw[4 * i + 3]), sc2,
+                    L.z, L.w);
+            p[4 * i + 0] = ex2(a0);
+            p[4 * i + 1] = ex2(a1);
+            p[4 * i + 2] = ex2(a2);
+            p[4 * i + 3] = ex2(a3);
           }
         }
         if (partial) {
@@ -634,10 +641,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             for (int i = 0; i < 2; ++i) {
               const float4 Dv = *reinterpret_cast<const float4*>(del_s + 8 * j + 4 * i);
               const int c = 8 * j + 4 * i;
-              const float s0 = p[c + 0] * (__uint_as_float(raw[c + 0]) - Dv.x);
-              const float s1 = p[c + 1] * (__uint_as_float(raw[c + 1]) - Dv.y);
-              const float s2 = p[c + 2] * (__uint_as_float(raw[c + 2]) - Dv.z);
-              const float s3 = p[c + 3] * (__uint_as_float(raw[c + 3]) - Dv.w);
+              float s0, s1, s2, s3;
+              mulsub2(s0, s1, p[c + 0], p[c + 1], __uint_as_float(raw[c + 0]),
+                      __uint_as_float(raw[c + 1]), Dv.x, Dv.y);
+              mulsub2(s2, s3, p[c + 2], p[c + 3], __uint_as_float(raw[c + 2]),
+                      __uint_as_float(raw[c + 3]), Dv.z, Dv.w);
               w[2 * i] = pack_bf16(s0, s1);
               w[2 * i + 1] = pack_bf16(s2, s3);
             }
@@ -702,10 +710,10 @@ static fm_status launch_bwd_d(const Plan& p, const fm_desc& desc, const TensorAr
   const size_t acc_bytes = static_cast<size_t>(p.B) * p.H * p.Sq * D * 4;
   if (cudaMemsetAsync(acc, 0, acc_bytes, s) != cudaSuccess) return FM_ERR_CUDA;
   {
-    const long long warps = static_cast<long long>(p.B) * p.H * rows_pad;
-    const long long blocks = (warps + 7) / 8;
+    const long long rows = static_cast<long long>(p.B) * p.H * rows_pad;
+    const long long blocks = (rows + 127) / 128;
     prof_begin(K_BWD_PRE, s);
-    bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+    bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 128, 0, s>>>(
         static_cast<const __nv_bfloat16*>(t.o), static_cast<const __nv_bfloat16*>(t.dout),
         desc.o_stride[0], desc.o_stride[1], desc.o_stride[2], t.lse_in, p.B, p.H, p.Sq, rows_pad,
         delta, lse2);

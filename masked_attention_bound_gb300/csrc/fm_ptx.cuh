@@ -302,6 +302,26 @@ __device__ __forceinline__ void add2_acc(float& s0, float& s1, float a0, float a
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(s) : "l"(s), "l"(a));
   asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(s));
 }
+// (d0, d1) = (a0 * b + c0, a1 * b + c1)
+__device__ __forceinline__ void fma2_bv(float& d0, float& d1, float a0, float a1, uint64_t b2,
+                                        float c0, float c1) {
+  uint64_t a, c, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(c) : "f"(c0), "f"(c1));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b2), "l"(c));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
+}
+// (d0, d1) = (p0 * (x0 - y0), p1 * (x1 - y1))
+__device__ __forceinline__ void mulsub2(float& d0, float& d1, float p0, float p1, float x0,
+                                        float x1, float y0, float y1) {
+  uint64_t p, x, y, t;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(p) : "f"(p0), "f"(p1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(y0), "f"(y1));
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(t) : "l"(x), "l"(y));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(t) : "l"(p), "l"(t));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(t));
+}
 __device__ __forceinline__ uint64_t splat2(float x) {
   uint64_t r;
   asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(x));
