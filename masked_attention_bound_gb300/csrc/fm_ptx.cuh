@@ -62,18 +62,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
-// One bounded attempt: the thread is suspended (not spinning, so it takes no
-// issue slots from the warps that do the work) until the phase completes or
-// about `hint_ns` pass.
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity,
-                                              uint32_t hint_ns = 1000000u) {
+// One bounded attempt: the thread may be suspended for a system-dependent
+// time while the phase is incomplete.  No suspend-time hint is given: with
+// a long hint the waiter resumed measurably later after the phase completed.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
