@@ -182,7 +182,7 @@ struct BwdParams {
 //                               dQ warps: atomics of dQ(t-1)
 //   dV += P^T(t) dO           [after P^T(t)]
 //                               compute: dS^T(t) = P^T o (dP^T - D) -> smem
-//   dK += dS^T Q, dQ = dS K -> B   [after dS^T(t)]
+//   dQ = dS K -> B, dK += dS^T Q   [after dS^T(t)]
 // so the P, dS and dQ work overlaps S, dP and dV.
 // Bits [a, b) of a 64-bit word, with a and b clipped to [0, 64].
 __device__ __forceinline__ uint64_t row_span(int a, int b) {
@@ -431,20 +431,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             mma_ts(tbase + C::T_DV, tbase + C::T_A + acol,
                    sdesc_sw128(sDO + kk * 2048, 16384, 1024), idKB, (t > 0 || kk > 0) ? 1u : 0u);
           }
-          // dK += dS^T Q and dQ = dS K once dS^T is in smem
+          // dQ = dS K and dK += dS^T Q once dS^T is in smem; dQ first, so its
+          // drain (which frees region B for the next dP^T) starts earlier.
+          // The dQ warps may then use this stage's dO buffer while dK runs:
+          // dK reads Q and dS^T only
           if (!wait(C_DSREADY, it & 1)) { ok = false; break; }
           tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tbase + C::T_B, sdesc_sw128(sDS + kk * 2048, 16384, 1024),
+                   sdesc_sw128(sK + kk * 2048, 16384, 1024), idDQ, kk > 0 ? 1u : 0u);
+          mma_commit(bar(C_DQFULL));
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
             mma_ss(tbase + C::T_DK, sdesc_sw128(sDS + aoff, 16, 1024),
                    sdesc_sw128(sQ + kk * 2048, 16384, 1024), idKB, (t > 0 || kk > 0) ? 1u : 0u);
           }
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tbase + C::T_B, sdesc_sw128(sDS + kk * 2048, 16384, 1024),
-                   sdesc_sw128(sK + kk * 2048, 16384, 1024), idDQ, kk > 0 ? 1u : 0u);
-          mma_commit(bar(C_DQFULL));
           mma_commit(bar(C_QEMPTY0 + st));
         }
         if (!ok) break;
