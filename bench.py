@@ -230,6 +230,24 @@ def run_e2e(args, fm, q, k, v, do, bounds, scale, o, lse, dq, dk, dv, ws_f, ws_b
     return e2e_ms, h2d, d2h
 
 
+def _traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, or None
+    when the kernel's sources have changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    try:
+        rec = json.load(open(path))[kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    m = hashlib.sha256()
+    for f in rec["sources"]:
+        try:
+            m.update(open(os.path.join(ROOT, "masked_attention_bound_gb300", "csrc", f), "rb").read())
+        except OSError:
+            return None
+    return int(rec["bytes_per_launch"]) if m.hexdigest() == rec["sources_sha256"] else None
+
+
 def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2d, d2h, clk):
     B, H, S, d = W["B"], W["H"], W["S"], W["d"]
     flop_step = flop_fwd + flop_bwd
@@ -272,7 +290,8 @@ def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2
             "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2),
                          "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                          "peak_source": f"bf16_tflops (burst) of {peak_src}",
-                         "traffic": None},
+                         "traffic": _traffic(dom) if (W["H"] == 32 and world >= 1) else None,
+                         "traffic_unit": "bytes per launch (ncu dram read + write)"},
             "kernel_ms_per_step": {n: round(t / args.steps, 4) for n, (t, c) in prof.items() if c},
             "kernel_launches_per_step": {n: c // args.steps for n, (t, c) in prof.items() if c},
             "kernel_time_share": {n: round(t / total_kernel_ms, 4) for n, (t, c) in prof.items() if c},
