@@ -139,7 +139,7 @@ struct BwdCfg {
   static constexpr int THREADS = 512;
   // register split (setmaxnreg): 2 x 128 x REGS_COMPUTE + 128 x REGS_DQ +
   // 128 x REGS_PRODUCER = 65536 = THREADS x 128 registers at launch
-  static constexpr uint32_t REGS_COMPUTE = 152, REGS_DQ = 152, REGS_PRODUCER = 56;
+  static constexpr uint32_t REGS_COMPUTE = 144, REGS_DQ = 152, REGS_PRODUCER = 72;
   static constexpr int MIN_LAUNCH_REGS =
       (2 * 128 * REGS_COMPUTE + 128 * REGS_DQ + 128 * REGS_PRODUCER + THREADS - 1) / THREADS;
 };
