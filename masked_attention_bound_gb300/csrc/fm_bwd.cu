@@ -674,7 +674,48 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(bar(C_ACCEMPTY));
-      if (key < P.Skv) {
+      if constexpr (D == 128) {
+        // Each thread holds 64 columns of its key row of dV and of dK.
+        // Stored straight from registers, every store instruction of a warp
+        // would touch 32 rows; instead each 32 x 64 bf16 block goes through
+        // this warp's 4 KB patch of the dS^T buffer (idle: the unit's MMAs
+        // are done, and these warps write the next dS^T only afterwards), so
+        // that an instruction stores four rows x 128 contiguous bytes.
+        const uint32_t patch = sDS + half * 16384 + quarter * 4096;
+        const int key0 = kj * kTile + quarter * 32;
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const float sc = m ? P.scale : 1.f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t* x = m ? rk + 8 * j : rv + 8 * j;
+            const uint32_t chunk = static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7);
+            st_shared_v4(patch + lane * 128 + chunk * 16,
+                         pack_bf16(__uint_as_float(x[0]) * sc, __uint_as_float(x[1]) * sc),
+                         pack_bf16(__uint_as_float(x[2]) * sc, __uint_as_float(x[3]) * sc),
+                         pack_bf16(__uint_as_float(x[4]) * sc, __uint_as_float(x[5]) * sc),
+                         pack_bf16(__uint_as_float(x[6]) * sc, __uint_as_float(x[7]) * sc));
+          }
+          __syncwarp();
+          __nv_bfloat16* base = m ? P.dk : P.dv;
+          const int64_t* st3 = m ? P.k_stride : P.v_stride;
+          const int jj = lane & 7;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rl = i * 4 + (lane >> 3);  // row within the warp's 32 keys
+            const uint32_t chunk = static_cast<uint32_t>(jj) ^ static_cast<uint32_t>(rl & 7);
+            uint4 val;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                         : "r"(patch + rl * 128 + chunk * 16));
+            const int kr = key0 + rl;
+            if (kr < P.Skv)
+              *reinterpret_cast<uint4*>(base + b * st3[0] + static_cast<int64_t>(kr) * st3[1] +
+                                        h * st3[2] + half * (D / 2) + jj * 8) = val;
+          }
+          __syncwarp();
+        }
+      } else if (key < P.Skv) {
         const float sc = P.scale;
         uint4* dv_dst = reinterpret_cast<uint4*>(dv_row);
         uint4* dk_dst = reinterpret_cast<uint4*>(dk_row);
