@@ -74,8 +74,9 @@ enum {
 // workspace) by the K/mask load warp when it is ready to load the next one,
 // and handed to the other roles that walk units through a ring of
 // UNIT_RING slots; U_READERS warps read every slot: the V load warp and the
-// eight softmax warps.  Claiming just in time keeps the units in flight on
-// all CTAs close together in the head-major order (K/V stay in L2).
+// eight softmax warps.  Only units with at least one tile go through the
+// ring.  Claiming just in time keeps the units in flight on all CTAs close
+// together in the head-major order (K/V stay in L2).
 constexpr int UNIT_RING = 4, U_READERS = 9;
 
 // entry word the load warp hands to the MMA warp: the pair-list classes in
@@ -266,30 +267,60 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         rows[g * 32 + lane] = mine;
       }
     };
+    // A pair with no visible tile at all (every row of both q-tiles hidden
+    // from every key) is finished by this warp: zero O rows and -inf LSE.
+    // Consecutive 16-byte words of a row go to consecutive lanes.
+    auto finish_empty_pair = [&](const PairUnit& u) {
+      constexpr int WPR = D / 8;  // 16-byte words per O row
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int s = 0; s < 2 && u.qa + s < P.nQ; ++s) {
+        const int row0 = (u.qa + s) * kTile;
+        for (int i = lane; i < kTile * WPR; i += 32) {
+          const int row = row0 + i / WPR;
+          if (row < P.Sq)
+            reinterpret_cast<uint4*>(P.o + u.b * P.o_stride[0] +
+                                     static_cast<int64_t>(row) * P.o_stride[1] +
+                                     u.h * P.o_stride[2])[i % WPR] = z;
+        }
+        for (int rr = lane; rr < kTile; rr += 32)
+          if (row0 + rr < P.Sq)
+            P.lse[(static_cast<size_t>(u.b) * P.H + u.h) * P.Sq + row0 + rr] = -INFINITY;
+      }
+    };
     uint32_t e = 0, un = 0;
     Pair<uint32_t> qn{0, 0};
     bool ok = true;
     while (ok) {
-      // claim the next unit and publish it to the other roles
-      int idx = -1;
-      if (lane == 0) {
-        const int r = un % UNIT_RING;
-        const uint32_t use = un / UNIT_RING;
-        if (use == 0 || wait(B_UEMPTY0 + r, (use - 1) & 1)) {
+      // claim the next unit with tiles and publish it to the other roles.
+      // Pairs without tiles are finished here and never published: the last
+      // PV of a unit waits for the entry word after it, so the claim that
+      // yields the next entry must not have to wait for a free ring slot,
+      // and a run of published empty pairs could fill the ring before it.
+      const int r = un % UNIT_RING;
+      const uint32_t use = un / UNIT_RING;
+      ++un;
+      if (lane == 0 && use > 0 && !wait(B_UEMPTY0 + r, (use - 1) & 1)) ok = false;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      int idx;
+      PairUnit u;
+      while (true) {
+        idx = -1;
+        if (lane == 0) {
           idx = atomicAdd(P.next_unit, 1);
           if (idx >= P.n_units) idx = -1;
-          ring[r] = idx;
-          mbar_arrive(bar(B_UFULL0 + r));
-        } else {
-          ok = false;
         }
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        if (idx < 0) break;
+        u = unit_of(P, idx);
+        if (u.n > 0) break;
+        finish_empty_pair(u);
       }
-      ++un;
-      idx = __shfl_sync(0xffffffffu, idx, 0);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (lane == 0) {
+        ring[r] = idx;
+        mbar_arrive(bar(B_UFULL0 + r));
+      }
       if (idx < 0) break;
-      const PairUnit u = unit_of(P, idx);
-      if (u.n == 0) continue;
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
         if ((s ? u.nb : u.na) == 0) continue;  // no tile of this slot: no Q

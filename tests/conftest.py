@@ -18,3 +18,32 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return GOLDEN
+
+
+@pytest.fixture(autouse=True)
+def _device_status_checked(request, monkeypatch):
+    """In GPU tests every fm.forward / fm.backward runs on a workspace whose
+    device status word is read back after the call, so a launch that gave up
+    on a wait (FM_ERR_TIMEOUT) or met a bad bound fails the test even where
+    the untouched output memory happens to hold plausible values."""
+    if request.node.get_closest_marker("gpu") is None:
+        yield
+        return
+    import masked_attention_bound_gb300 as fm
+    from masked_attention_bound_gb300._abi import status_string
+
+    def wrap(fn, for_bwd):
+        def call(q, k, v, *args, ws=None, **kw):
+            if ws is None:
+                bounds = args[3] if for_bwd else args[0]
+                desc = fm.make_desc(q, k, v, q, Hm=bounds.shape[2])
+                ws = fm.workspace(desc, for_bwd, q.device)
+            out = fn(q, k, v, *args, ws=ws, **kw)
+            code = fm.device_status(ws, kw.get("stream"))
+            assert code == 0, f"{fn.__name__}: device status {code} ({status_string(code)})"
+            return out
+        return call
+
+    monkeypatch.setattr(fm, "forward", wrap(fm.forward, False))
+    monkeypatch.setattr(fm, "backward", wrap(fm.backward, True))
+    yield

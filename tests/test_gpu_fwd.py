@@ -125,3 +125,27 @@ def test_long_128k_sampled():
     o, lse = fm.forward(q, k, v, bounds, W.scale)
     torch.cuda.synchronize()
     compare_fwd(q, k, v, bounds, W.scale, o, lse, heads=[(0, 0), (0, 7)], rows=64)
+
+
+def test_many_hidden_pairs_after_the_visible_ones():
+    """Rows [S/4, S) see no key: three quarters of the q-tile pairs have no
+    tile and come last in the longest-first order, so every CTA claims a long
+    run of them after its last pair with tiles.  Their O rows are zero and
+    their LSE -inf, written into NaN-filled outputs, and the launch ends with
+    a clean device status (checked by the test fixture)."""
+    B, S, H, d = 1, 16384, 16, 128
+    q, k, v, _ = _inputs(B, S, H, d, seed=5)
+    R0 = S // 4
+    lts = np.full(S, R0, dtype=np.int64)
+    lte = np.full(S, S, dtype=np.int64)
+    z = np.zeros(S, dtype=np.int64)
+    bounds = bounds_tensor([[(lts, lte, z, z)]], device="cuda")
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, H, S), float("nan"), device="cuda")
+    for _ in range(2):
+        fm.forward(q, k, v, bounds, d ** -0.5, o=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(o[:, R0:] == 0)
+    assert torch.all(torch.isneginf(lse[:, :, R0:]))
+    assert not torch.isnan(o).any() and not torch.isnan(lse).any()
+    compare_fwd(q, k, v, bounds, d ** -0.5, o, lse, heads=[(0, 0), (0, 15)], rows=64)
