@@ -11,7 +11,8 @@
 // Three kernels:
 //   bwd_pre_kernel    D_i and -LSE_i*log2(e) per query row, padded to whole
 //                     128-row tiles (-inf / 0 past Sq and on rows that see no
-//                     key, so P = 0 there without a branch);
+//                     key, so P = 0 there without a branch), and the zeroed
+//                     fp32 dQ accumulator;
 //   bwd_kernel        one unit = one (batch, head, k-tile): K and V stay in
 //                     smem, the unit walks its column of non-empty q-tiles.
 //                     Warps 0-7 (compute): thread r owns key row r (TMEM
@@ -39,55 +40,92 @@
 namespace fm {
 
 // ------------------------------------------------------------------ preprocess
-// One thread per (b, h, row) over nQ*128 padded rows: the row's D values of O
-// and of dO (one 2D-byte run each) are loaded whole, so every thread keeps
-// 4D bytes of reads in flight; consecutive threads take consecutive rows,
-// so the two fp32 outputs are written coalesced.
+// One warp per 16 consecutive rows of one (b, h), over nQ*128 padded rows.
+// Eight lanes share a row: lane (rr, part) = (lane >> 3, lane & 7) loads the
+// 16-byte words part, part + 8, ... of row 4k + rr of O and of dO, so that a
+// warp load covers four whole 128-byte segments; all 16 rows' loads are
+// issued before any arithmetic (256 bytes in flight per thread).  The eight
+// partial dot products of a row are summed with shuffles.  The warp also
+// zeroes those rows of the fp32 dQ accumulator (the backward kernel adds
+// into it), with the same coalesced pattern.
 template <int D>
 __global__ void __launch_bounds__(128) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dout,
                                                       int64_t os0, int64_t os1, int64_t os2,
                                                       const float* __restrict__ lse, int B, int H,
                                                       int Sq, int rows_pad, float* delta,
-                                                      float* lse_log2) {
-  const long long w = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long total = static_cast<long long>(B) * H * rows_pad;
-  if (w >= total) return;
-  const int i = static_cast<int>(w % rows_pad);
-  const int bh = static_cast<int>(w / rows_pad);
+                                                      float* lse_log2, float* dq_acc) {
+  constexpr int W = D / 64;  // 16-byte words per lane per row
+  const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31, rr = lane >> 3, part = lane & 7;
+  const int groups = rows_pad / 16;
+  if (gw >= static_cast<long long>(B) * H * groups) return;
+  const int bh = static_cast<int>(gw / groups);
+  const int i0 = static_cast<int>(gw - static_cast<long long>(bh) * groups) * 16;
   const int b = bh / H, h = bh - b * H;
-  float dsum = 0.f;
-  float l2 = -INFINITY;
-  if (i < Sq) {
-    const size_t at = static_cast<size_t>(b) * os0 + static_cast<size_t>(i) * os1 +
-                      static_cast<size_t>(h) * os2;
-    const uint4* a4 = reinterpret_cast<const uint4*>(o + at);
-    const uint4* g4 = reinterpret_cast<const uint4*>(dout + at);
-    uint4 a[D / 8], g[D / 8];
+  uint4 a[4][W], g[4][W];
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      a[c] = __ldg(a4 + c);
-      g[c] = __ldg(g4 + c);
+  for (int k = 0; k < 4; ++k) {
+    const int i = i0 + 4 * k + rr;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      a[k][w] = make_uint4(0u, 0u, 0u, 0u);
+      g[k][w] = make_uint4(0u, 0u, 0u, 0u);
     }
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (i < Sq) {
+      const size_t at = static_cast<size_t>(b) * os0 + static_cast<size_t>(i) * os1 +
+                        static_cast<size_t>(h) * os2;
+      const uint4* a4 = reinterpret_cast<const uint4*>(o + at);
+      const uint4* g4 = reinterpret_cast<const uint4*>(dout + at);
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[c]);
-      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g[c]);
+      for (int w = 0; w < W; ++w) {
+        a[k][w] = __ldg(a4 + part + 8 * w);
+        g[k][w] = __ldg(g4 + part + 8 * w);
+      }
+    }
+  }
+  float dot[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[k][w]);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g[k][w]);
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const float2 x = __bfloat1622float2(a2[t]);
         const float2 y = __bfloat1622float2(g2[t]);
-        acc[t] = fmaf(x.x, y.x, acc[t]);
-        acc[t] = fmaf(x.y, y.y, acc[t]);
+        acc0 = fmaf(x.x, y.x, acc0);
+        acc1 = fmaf(x.y, y.y, acc1);
       }
     }
-    dsum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-    const float L = lse[static_cast<size_t>(bh) * Sq + i];
-    l2 = (L == -INFINITY) ? -INFINITY : -L * 1.4426950408889634f;
+    dot[k] = acc0 + acc1;
   }
-  delta[static_cast<size_t>(bh) * rows_pad + i] = dsum;
-  lse_log2[static_cast<size_t>(bh) * rows_pad + i] = l2;
+#pragma unroll
+  for (int sh = 1; sh < 8; sh <<= 1)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dot[k] += __shfl_xor_sync(0xffffffffu, dot[k], sh);
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = i0 + 4 * k + rr;
+    if (i < Sq) {
+      float4* acc_row = reinterpret_cast<float4*>(dq_acc + (static_cast<size_t>(bh) * Sq + i) * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) acc_row[part + 8 * c] = z;
+    }
+    if (part == 0) {
+      float l2 = -INFINITY, dsum = 0.f;
+      if (i < Sq) {
+        const float L = lse[static_cast<size_t>(bh) * Sq + i];
+        l2 = (L == -INFINITY) ? -INFINITY : -L * 1.4426950408889634f;
+        dsum = dot[k];
+      }
+      delta[static_cast<size_t>(bh) * rows_pad + i] = dsum;
+      lse_log2[static_cast<size_t>(bh) * rows_pad + i] = l2;
+    }
+  }
 }
 
 // ------------------------------------------------------------------ dQ convert
@@ -751,16 +789,15 @@ static fm_status launch_bwd_d(const Plan& p, const fm_desc& desc, const TensorAr
   float* delta = reinterpret_cast<float*>(ws + p.L.delta);
   float* lse2 = reinterpret_cast<float*>(ws + p.L.lse_log2);
   float* acc = reinterpret_cast<float*>(ws + p.L.dq_acc);
-  const size_t acc_bytes = static_cast<size_t>(p.B) * p.H * p.Sq * D * 4;
-  if (cudaMemsetAsync(acc, 0, acc_bytes, s) != cudaSuccess) return FM_ERR_CUDA;
   {
+    // four warps per block, one warp per 16 rows (rows_pad is a multiple of 128)
     const long long rows = static_cast<long long>(p.B) * p.H * rows_pad;
-    const long long blocks = (rows + 127) / 128;
+    const long long blocks = (rows / 16 + 3) / 4;
     prof_begin(K_BWD_PRE, s);
     bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 128, 0, s>>>(
         static_cast<const __nv_bfloat16*>(t.o), static_cast<const __nv_bfloat16*>(t.dout),
         desc.o_stride[0], desc.o_stride[1], desc.o_stride[2], t.lse_in, p.B, p.H, p.Sq, rows_pad,
-        delta, lse2);
+        delta, lse2, acc);
     prof_end(K_BWD_PRE, s);
     if (cudaGetLastError() != cudaSuccess) return FM_ERR_CUDA;
   }
