@@ -137,12 +137,22 @@ __global__ void __launch_bounds__(256) classify_rows_kernel(const int32_t* __res
 // row, thread r = query row r0 + r of the tile): bit c of row r is set when
 // key column kj*128 + c is hidden from that row (or lies past Skv).  The
 // masks depend only on (batch, mask head), so every query head reuses them.
+// kMaskSplit CTAs share a row (blockIdx.y = g builds the row's partial
+// tiles g, g + kMaskSplit, ...), so a row with many partial tiles does not
+// set the kernel's length.  Each reads the row's tile list in coalesced
+// chunks and compacts the partial tiles in shared memory; the bounds of its
+// tiles are loaded kMaskBatch tiles at a time (one load latency per batch),
+// each thread reading column r of every tile of the batch.
+constexpr int kMaskBatch = 4, kMaskSplit = 8;
 __global__ void __launch_bounds__(kTile) tile_mask_kernel(
     const int32_t* __restrict__ lts, const int32_t* __restrict__ lte,
     const int32_t* __restrict__ uts, const int32_t* __restrict__ ute, int nQ, int nK, int Skv,
     const int32_t* __restrict__ row_count, const int32_t* __restrict__ row_list,
     const int32_t* __restrict__ row_mask, uint4* masks) {
-  __shared__ int4 sb[kTile];
+  __shared__ int4 sb[kMaskBatch][kTile];
+  __shared__ int kjs[kTile];   // partial tiles of the current list chunk, in list order
+  __shared__ int nchunk_part;
+  __shared__ int warp_part[kTile / 32];
   const int row = blockIdx.x;
   const int first = row_mask[row];
   if (first < 0) return;
@@ -150,29 +160,67 @@ __global__ void __launch_bounds__(kTile) tile_mask_kernel(
   const int n = row_count[row];
   const int32_t* lst = row_list + static_cast<size_t>(row) * nK;
   const size_t bbase = static_cast<size_t>(bh) * Skv;
-  const int r = threadIdx.x;
+  const int r = threadIdx.x, lane = r & 31, wid = r >> 5;
   const int R = qi * kTile + r;
   const bool ragged = (Skv & (kTile - 1)) != 0;
-  int ord = 0;
-  for (int t = 0; t < n; ++t) {
-    const int e = lst[t];
-    const int kj = e >> 2;
-    if ((e & 3) != CLS_PARTIAL && !(ragged && kj == nK - 1)) continue;
-    __syncthreads();  // previous tile's bounds no longer read
-    const int j = kj * kTile + r;
-    sb[r] = j < Skv ? make_int4(__ldg(lts + bbase + j), __ldg(lte + bbase + j),
-                                __ldg(uts + bbase + j), __ldg(ute + bbase + j))
-                    : make_int4(0, 0x7fffffff, 0, 0);
-    __syncthreads();
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-    for (int c = 0; c < kTile; ++c) {
-      const int4 v = sb[c];
-      const bool hid = (v.x <= R && R < v.y) || (v.z <= R && R < v.w);
-      w[c >> 5] |= (hid ? 1u : 0u) << (c & 31);
+  int ord = 0;  // partial tiles written so far
+  for (int base = 0; base < n; base += kTile) {
+    // compact this chunk's partial tiles, keeping list order
+    const int t = base + r;
+    bool part = false;
+    int kj = 0;
+    if (t < n) {
+      const int e = lst[t];
+      kj = e >> 2;
+      part = (e & 3) == CLS_PARTIAL || (ragged && kj == nK - 1);
     }
-    masks[(static_cast<size_t>(first + ord) * kTile + r)] = make_uint4(w[0], w[1], w[2], w[3]);
-    ++ord;
+    const unsigned m = __ballot_sync(0xffffffffu, part);
+    __syncthreads();  // the previous chunk's kjs and bounds are no longer read
+    if (lane == 0) warp_part[wid] = __popc(m);
+    __syncthreads();
+    int off = 0;
+#pragma unroll
+    for (int w = 0; w < kTile / 32; ++w) off += w < wid ? warp_part[w] : 0;
+    if (part) kjs[off + __popc(m & ((1u << lane) - 1u))] = kj;
+    if (r == 0) {
+      int tot = 0;
+#pragma unroll
+      for (int w = 0; w < kTile / 32; ++w) tot += warp_part[w];
+      nchunk_part = tot;
+    }
+    __syncthreads();
+    const int np = nchunk_part;
+    // this CTA's tiles of the chunk: i = i0, i0 + kMaskSplit, ... (global
+    // partial index ord + i congruent to blockIdx.y)
+    const int g = static_cast<int>(blockIdx.y);
+    const int i0 = ((g - ord) % kMaskSplit + kMaskSplit) % kMaskSplit;
+    const int mine = np > i0 ? (np - i0 + kMaskSplit - 1) / kMaskSplit : 0;
+    for (int b0 = 0; b0 < mine; b0 += kMaskBatch) {
+      const int nb = min(kMaskBatch, mine - b0);
+      if (b0 > 0) __syncthreads();  // the previous batch's bounds are no longer read
+#pragma unroll
+      for (int x = 0; x < kMaskBatch; ++x) {
+        if (x < nb) {
+          const int j = kjs[i0 + (b0 + x) * kMaskSplit] * kTile + r;
+          sb[x][r] = j < Skv ? make_int4(__ldg(lts + bbase + j), __ldg(lte + bbase + j),
+                                         __ldg(uts + bbase + j), __ldg(ute + bbase + j))
+                             : make_int4(0, 0x7fffffff, 0, 0);
+        }
+      }
+      __syncthreads();
+      for (int x = 0; x < nb; ++x) {
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int c = 0; c < kTile; ++c) {
+          const int4 v = sb[x][c];
+          const bool hid = (v.x <= R && R < v.y) || (v.z <= R && R < v.w);
+          w[c >> 5] |= (hid ? 1u : 0u) << (c & 31);
+        }
+        const int i = i0 + (b0 + x) * kMaskSplit;
+        masks[(static_cast<size_t>(first + ord + i) * kTile + r)] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+    ord += np;
   }
 }
 
@@ -376,7 +424,7 @@ cudaError_t launch_classify(const Plan& p, char* ws, int for_bwd, cudaStream_t s
 cudaError_t launch_tile_masks(const Plan& p, const int32_t* lts, const int32_t* lte,
                               const int32_t* uts, const int32_t* ute, char* ws, cudaStream_t s) {
   prof_begin(K_TILE_MASKS, s);
-  tile_mask_kernel<<<p.B * p.Hm * p.nQ, kTile, 0, s>>>(
+  tile_mask_kernel<<<dim3(p.B * p.Hm * p.nQ, kMaskSplit), kTile, 0, s>>>(
       lts, lte, uts, ute, p.nQ, p.nK, p.Skv, reinterpret_cast<const int32_t*>(ws + p.L.row_count),
       reinterpret_cast<const int32_t*>(ws + p.L.row_list),
       reinterpret_cast<const int32_t*>(ws + p.L.row_mask), reinterpret_cast<uint4*>(ws + p.L.masks));
