@@ -20,12 +20,12 @@
 //              P (bf16) over S in TMEM, rescales O in TMEM when the max moves
 //              by more than 2^8, and writes O / LSE at the end of the unit;
 //   warp 8     loads Q (per slot), K and the partial tiles' bit masks; passes
-//              each entry's classes and unit boundaries to the MMA warp;
-//   warp 9     one thread issues tcgen05 MMAs: S = Q K^T (both K-major,
-//              smem), O += P V (P from TMEM, V MN-major from smem), in the
-//              order PV_a(e), S_a(e+1), PV_b(e), S_b(e+1), so one slot's
-//              softmax runs while the other slot's MMAs do;
-//   warp 10    loads V;  warp 11 idle.
+//              each entry's classes and unit boundaries to the MMA warps;
+//   warps 9/11 one thread each issues the tcgen05 MMAs of slot a / b:
+//              S = Q K^T (both K-major, smem), O += P V (P from TMEM, V
+//              MN-major from smem), per entry e PV(e) then S(e+1), so one
+//              slot's softmax runs while the other slot's MMAs do;
+//   warp 10    loads V.
 // TMEM (512 columns): S/P of slot s at [128 s, 128 s + 128), O of slot s at
 // [256 + 128 s, 256 + 128 s + D).
 #include <cuda_bf16.h>
@@ -54,7 +54,7 @@ struct FwdCfg {
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   static constexpr uint32_t T_COLS = 512;
   // warpgroups 0 and 1: softmax of slot a / b; warpgroup 2: the Q/K/mask
-  // load warp, the MMA warp, the V load warp and one idle warp
+  // load warp, the V load warp and the two MMA warps
   static constexpr int THREADS = 384;
   // register split (setmaxnreg): 2 x 128 x REGS_SOFTMAX + 128 x REGS_PRODUCER
   // = 62464 <= THREADS x (compiled registers); the launch checks that the
@@ -79,7 +79,7 @@ enum {
 // together in the head-major order (K/V stay in L2).
 constexpr int UNIT_RING = 4, U_READERS = 9;
 
-// entry word the load warp hands to the MMA warp: the pair-list classes in
+// entry word the load warp hands to the MMA warps: the pair-list classes in
 // bits 0-3 (class_b bits 0-1, class_a bits 2-3), then whether this entry is
 // the first / last non-empty tile of slot a (bits 4, 5) and of slot b (6, 7)
 // within its unit
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr int TMA_WARP = 8, MMA_WARP = 9, V_WARP = 10;
+  constexpr int TMA_WARP = 8, MMA_WARP = 9, V_WARP = 10, MMA_WARP_B = 11;
 
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -170,15 +170,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       mbar_init(bar(B_PVDONE0 + s), 1);
       mbar_init(bar(B_OEMPTY0 + s), 128);
       mbar_init(bar(B_KFULL0 + s), 1);
-      mbar_init(bar(B_KEMPTY0 + s), 1);
+      mbar_init(bar(B_KEMPTY0 + s), 2);  // one commit per MMA thread
       mbar_init(bar(B_VFULL0 + s), 1);
-      mbar_init(bar(B_VEMPTY0 + s), 1);
+      mbar_init(bar(B_VEMPTY0 + s), 2);
       // per stage: 128 arrivals for each slot, from its softmax threads when
       // the slot's tile there is partial (they read the bits), else from the
       // load warp on the slot's behalf
       mbar_init(bar(B_MEMPTY0 + s), 256);
     }
-    mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_DRAIN), 2);
     for (int r = 0; r < UNIT_RING; ++r) {
       mbar_init(bar(B_UFULL0 + r), 1);
       mbar_init(bar(B_UEMPTY0 + r), U_READERS);
@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       if (qn.v0 > 0) mbar_wait(bar(B_QFULL0), (qn.v0 - 1) & 1, P.status);
       if (qn.v1 > 0) mbar_wait(bar(B_QFULL0 + 1), (qn.v1 - 1) & 1, P.status);
     }
-    // the end marker: one more entry word, no tiles, so the MMA warp stops.
+    // the end marker: one more entry word, no tiles, so the MMA warps stop.
     // Like any entry it waits until the entry two before has been read by
     // the MMAs and by the softmax threads that read its bits: those threads
     // wait on this stage's KFULL barrier, which must not run two phases
@@ -445,47 +445,58 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       for (uint32_t x = (e > 2u ? e - 2u : 0u); x < e; ++x)
         mbar_wait(bar(B_VFULL0 + (x & 1)), (x >> 1) & 1, P.status);
     __syncwarp();
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == MMA_WARP || warp == MMA_WARP_B) {
+    // ------------------------------------------------------------ MMA issuers
+    // One thread per slot (warp 9: slot a, warp 11: slot b).  The tensor
+    // pipe accepts about one MMA ahead of the one it runs, so whatever the
+    // issuing thread does between its MMA groups (barrier waits, the entry
+    // word) leaves the pipe idle unless another thread issues meanwhile;
+    // with one thread per slot, neither slot's waits hold up the other's
+    // MMAs.  Both walk every entry: the K and V stages are released when
+    // both have committed (their barriers count two arrivals).
     if (lane == 0) {
+      const int s = warp == MMA_WARP ? 0 : 1;
+      const uint32_t fA = s ? E_B : E_A, fFIRST = s ? E_FIRST_B : E_FIRST_A,
+                     fLAST = s ? E_LAST_B : E_LAST_A;
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
-      Pair<uint32_t> qn{0, 0}, np{0, 0}, un{0, 0};
+      const uint32_t sQ = sbase + C::OFF_Q + s * C::TILE;
+      const uint32_t tS = tbase + 128 * s, tO = tbase + 256 + 128 * s;
+      uint32_t qn = 0, np = 0, un = 0;
       // entry word of entry e, once its K tile (and bits) have landed
       auto entry = [&](uint32_t e, uint32_t& f) -> bool {
         if (!wait(B_KFULL0 + (e & 1), (e >> 1) & 1)) return false;
         f = desc[e & 1];
         return true;
       };
-      // S of slot s for entry e.  It overwrites the slot's P of its previous
-      // tile; MMAs issued by this thread run in issue order, so the PV that
-      // reads that P (issued before) is done with it first.
-      auto issue_s = [&](int s, uint32_t e, uint32_t f) -> bool {
-        if (f & (s ? E_FIRST_B : E_FIRST_A)) {
-          if (!wait(B_QFULL0 + s, qn.get(s) & 1)) return false;
-          qn.set(s, qn.get(s) + 1);
+      // S of this slot for entry e.  It overwrites the slot's P of its
+      // previous tile; MMAs issued by this thread run in issue order, so the
+      // PV that reads that P (issued before) is done with it first.
+      auto issue_s = [&](uint32_t e, uint32_t f) -> bool {
+        if (f & fFIRST) {
+          if (!wait(B_QFULL0 + s, qn & 1)) return false;
+          ++qn;
         }
         tc_fence_after();
-        const uint32_t sQ = sbase + C::OFF_Q + s * C::TILE;
         const uint32_t sK = sbase + C::OFF_K + (e & 1) * C::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tbase + 128 * s, sdesc_sw128(sQ + koff, 16, 1024),
-                 sdesc_sw128(sK + koff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          mma_ss(tS, sdesc_sw128(sQ + koff, 16, 1024), sdesc_sw128(sK + koff, 16, 1024), idS,
+                 kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(B_SFULL0 + s));
-        if (f & (s ? E_LAST_B : E_LAST_A)) mma_commit(bar(B_QEMPTY0 + s));
+        if (f & fLAST) mma_commit(bar(B_QEMPTY0 + s));
         return true;
       };
-      auto issue_pv = [&](int s, uint32_t e, uint32_t f) -> bool {
-        if (!wait(B_PFULL0 + s, np.get(s) & 1)) return false;
-        np.set(s, np.get(s) + 1);
-        const bool first = (f & (s ? E_FIRST_B : E_FIRST_A)) != 0;
+      auto issue_pv = [&](uint32_t e, uint32_t f) -> bool {
+        if (!wait(B_PFULL0 + s, np & 1)) return false;
+        ++np;
+        const bool first = (f & fFIRST) != 0;
         if (first) {
           // O of this slot is overwritten: its previous epilogue must be done
-          if (un.get(s) > 0 && !wait(B_OEMPTY0 + s, (un.get(s) - 1) & 1)) return false;
-          un.set(s, un.get(s) + 1);
+          if (un > 0 && !wait(B_OEMPTY0 + s, (un - 1) & 1)) return false;
+          ++un;
         }
         const int st = e & 1;
         if (!wait(B_VFULL0 + st, (e >> 1) & 1)) return false;
@@ -493,28 +504,33 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const uint32_t sV = sbase + C::OFF_V + st * C::TILE;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tbase + 256 + 128 * s, tbase + 128 * s + kk * 8,
-                 sdesc_sw128(sV + kk * 2048, 128 * 128, 1024), idPV, (!first || kk > 0) ? 1u : 0u);
+          mma_ts(tO, tS + kk * 8, sdesc_sw128(sV + kk * 2048, 128 * 128, 1024), idPV,
+                 (!first || kk > 0) ? 1u : 0u);
         mma_commit(bar(B_PVDONE0 + s));
         return true;
       };
-      // entries arrive in order until the end marker
+      // entries arrive in order until the end marker; per entry: this
+      // slot's PV of it, then its S of the next one
       uint32_t fc = 0;
       bool ok = entry(0, fc);
       if (ok && !(fc & E_END)) {
-        if (fc & E_A) ok = issue_s(0, 0, fc);
-        if (ok && (fc & E_B)) ok = issue_s(1, 0, fc);
+        if (fc & fA) ok = issue_s(0, fc);
         if (ok) mma_commit(bar(B_KEMPTY0));
         for (uint32_t j = 0; ok; ++j) {
           uint32_t fn = 0;
-          if ((fc & E_A) && !issue_pv(0, j, fc)) break;
-          if (!entry(j + 1, fn)) break;
-          const bool more = !(fn & E_END);
-          if (more && (fn & E_A) && !issue_s(0, j + 1, fn)) break;
-          if ((fc & E_B) && !issue_pv(1, j, fc)) break;
+          // release V(j) only once it has landed, also when this slot does
+          // not use it: then V(j) loaded means the release of V(j - 2) was
+          // complete, so this thread's two arrivals never fill one phase of
+          // the stage's barrier (the other thread may still be using V(j - 2))
+          if (fc & fA) {
+            if (!issue_pv(j, fc)) break;
+          } else if (!wait(B_VFULL0 + (j & 1), (j >> 1) & 1)) {
+            break;
+          }
           mma_commit(bar(B_VEMPTY0 + (j & 1)));
-          if (more && (fn & E_B) && !issue_s(1, j + 1, fn)) break;
-          if (!more) break;
+          if (!entry(j + 1, fn)) break;
+          if (fn & E_END) break;
+          if ((fn & fA) && !issue_s(j + 1, fn)) break;
           mma_commit(bar(B_KEMPTY0 + ((j + 1) & 1)));
           fc = fn;
         }
@@ -523,7 +539,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       mbar_wait(bar(B_DRAIN), 0, P.status);
     }
     __syncwarp();
-  }  // warp 11: spare warp of the producer warpgroup, nothing to do
+  }
   } else {
     // ------------------------------------------------------------ softmax
     regs_increase<C::REGS_SOFTMAX>();
