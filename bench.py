@@ -103,6 +103,24 @@ def _dist():
     return world, rank, local
 
 
+def _max_over_ranks(ms: float, world: int, device) -> float:
+    """Step time of the whole job: the slowest rank's (all ranks hold the
+    result).  One rank: the time itself."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_value(flop_per_rank_step: float, ms: float, world: int) -> float:
+    """Whole-job throughput in TFLOP/s: the work of all ranks in one step
+    (each rank runs its own replica of the workload) over the step time."""
+    return world * flop_per_rank_step / (ms * 1e-3) / 1e12
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -162,11 +180,7 @@ def run_ours(args):
     fm.profile_enable(False)
     prof = fm.profile_read()
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = _max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, "cuda")
 
     if args.no_e2e:
         e2e_ms, h2d, d2h = float("nan"), 0, 0
@@ -220,11 +234,7 @@ def run_e2e(args, fm, q, k, v, do, bounds, scale, o, lse, dq, dk, dv, ws_f, ws_b
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    e2e_ms = ev0.elapsed_time(ev1) / e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = _max_over_ranks(ev0.elapsed_time(ev1) / e_steps, world, "cuda")
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo, hb))
     d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdq, hdk, hdv))
     return e2e_ms, h2d, d2h
@@ -264,7 +274,7 @@ def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2
         achieved = dom_flop / (dom_avg_ms * 1e-3) / 1e12
         # the timed loop lasts well under a second: compare with the burst figure
         peak = float(peaks["bf16_tflops"])
-        value = world * flop_step / (ms * 1e-3) / 1e12
+        value = _job_value(flop_step, ms, world)
         launches = sum(n for _, n in prof.values())
         total_kernel_ms = sum(t for t, _ in prof.values())
         out = {
@@ -297,7 +307,7 @@ def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2
             "kernel_time_share": {n: round(t / total_kernel_ms, 4) for n, (t, c) in prof.items() if c},
             "gpu_launches": launches,
             "e2e": None if e2e_ms != e2e_ms else {
-                "value": round(world * flop_step / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "value": round(_job_value(flop_step, e2e_ms, world), 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
             "clocks": clk,
