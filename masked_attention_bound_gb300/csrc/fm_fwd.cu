@@ -57,9 +57,11 @@ struct FwdCfg {
   // load warp, the V load warp and the two MMA warps
   static constexpr int THREADS = 384;
   // register split (setmaxnreg): 2 x 128 x REGS_SOFTMAX + 128 x REGS_PRODUCER
-  // = 62464 <= THREADS x (compiled registers); the launch checks that the
-  // kernel was compiled with at least MIN_LAUNCH_REGS registers per thread
-  static constexpr uint32_t REGS_SOFTMAX = 216, REGS_PRODUCER = 56;
+  // = 64512 = THREADS x 168 (the compiled registers); the launch checks that
+  // the kernel was compiled with at least MIN_LAUNCH_REGS registers per
+  // thread.  With 56 for the producer warpgroup its roles spilled, and the
+  // MMA threads' spills sat between their MMA groups.
+  static constexpr uint32_t REGS_SOFTMAX = 216, REGS_PRODUCER = 72;
   static constexpr int MIN_LAUNCH_REGS =
       (2 * 128 * REGS_SOFTMAX + 128 * REGS_PRODUCER + THREADS - 1) / THREADS;
 };
