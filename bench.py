@@ -103,6 +103,14 @@ def _dist():
     return world, rank, local
 
 
+def _config(W, n_vis: int, world: int) -> dict:
+    """The workload as both arms report it."""
+    return {"workload": W["name"], "B": W["B"], "H": W["H"], "S": W["S"], "d": W["d"],
+            "mask": W["mask"], "visible_entries_per_rank": n_vis,
+            "l2": "inputs larger than L2 (Q, K, V, dO 256 MiB each); no flush between steps",
+            "parallelism": f"replicas x{world} (no collective on the data path)"}
+
+
 def _max_over_ranks(ms: float, world: int, device) -> float:
     """Step time of the whole job: the slowest rank's (all ranks hold the
     result).  One rank: the time itself."""
@@ -319,10 +327,7 @@ def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) Q/K/V/dO, seeded document lengths)",
-            "config": {"workload": W["name"], "B": B, "H": H, "S": S, "d": d, "mask": W["mask"],
-                       "visible_entries_per_rank": n_vis, "l2": "inputs larger than L2 "
-                       "(Q, K, V, dO 256 MiB each); no flush between steps",
-                       "parallelism": f"replicas x{world} (no collective on the data path)"},
+            "config": _config(W, n_vis, world),
             "fwd_tflops": round(flop_fwd / (fwd_avg * 1e-3) / 1e12, 2),
             "bwd_tflops": round(flop_bwd / (bwd_avg * 1e-3) / 1e12, 2),
             "pct_bf16_peak": round(100.0 * value / world / peak, 1),
@@ -418,12 +423,14 @@ def run_reference(args):
     cores = len(os.sched_getaffinity(0))
     sample = (f"fp64 oracle backward (with its forward) of query rows [0, {rows}) of one head of "
               f"{W['name']} per step, {n_vis} visible entries")
+    # the whole workload's count, as the device arm reports it
+    from fm_inputs.tensors import mask_bounds
+    n_vis_job = _visible_entries(mask_bounds(W["mask"], W["B"], S, device="cpu").numpy(), S, W["H"])
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": W["name"], "B": 1, "H": 1, "S": S, "d": d,
-                                        "mask": W["mask"], "sample_rows": rows},
+        "data": "synthetic", "config": _config(W, n_vis_job, world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
