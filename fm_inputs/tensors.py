@@ -31,6 +31,16 @@ def qkv_do(B: int, Sq: int, Skv: int, H: int, d: int, seed: int = 0,
     return q, k, v, do
 
 
+def randn_bf16(*shape, seed: int, device: str = "cpu") -> torch.Tensor:
+    """One N(0, 1) bf16 tensor of ``shape`` from a torch CPU generator seeded
+    with ``seed`` (float32 draws rounded to bf16), moved to ``device``; the
+    values do not depend on the device."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    t = torch.randn(*shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return t.to(device) if device != "cpu" else t
+
+
 def bounds_tensor(masks_per_batch, device: str = "cpu") -> torch.Tensor:
     """Stack per-(batch, mask-head) bound vectors into one int32 tensor of shape
     [4][B][Hm][Skv] (LTS, LTE, UTS, UTE), the layout the library reads.

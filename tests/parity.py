@@ -2,7 +2,9 @@
 with the oracle on the same seeded inputs.
 
 Tolerances (written here once, used by every parity test):
-  O:     max |O - O_ref| <= 1e-2
+  O:     max (|O - O_ref| - u(O_ref)) <= 1e-2, u(x) = half a bf16 ulp at |x|:
+         the 1e-2 budget is for the computation, and the rounding to the bf16
+         output (up to 2^-7 for |O_ref| in [2, 4)) comes on top of it
   LSE:   max |LSE - LSE_ref| <= 1e-3 on rows that see a key, exactly -inf otherwise
   grads: max |G - G_ref| <= 2e-2 * max(max |G_ref|, 1e-4)
          (the floor only matters when the reference gradient is identically
@@ -15,11 +17,17 @@ import numpy as np
 import torch
 
 from oracle import attention as oa
+from rounding_model import bf16_half_ulp
 
 O_TOL = 1e-2
 LSE_TOL = 1e-3
 GRAD_REL = 2e-2
 GRAD_FLOOR = 1e-4
+
+
+def o_excess(got, ref):
+    """|O - O_ref| beyond the unavoidable rounding of O_ref to bf16, elementwise."""
+    return np.abs(got - ref) - bf16_half_ulp(ref)
 
 
 def head_slice(t, b, h):
@@ -56,13 +64,13 @@ def compare_fwd(q, k, v, bounds, scale, o, lse, heads=None, rows=None, seed=0, s
                                  skip_hidden=True)
         go = o[b, r, h].float().cpu().numpy()
         gl = lse[b, h, r].cpu().numpy().astype(np.float64)
-        eo = float(np.abs(go - ro).max()) if len(r) else 0.0
+        eo = float(o_excess(go, ro).max()) if len(r) else 0.0
         dead = np.isneginf(rl)
         assert np.array_equal(np.isneginf(gl), dead), f"-inf LSE rows differ at (b={b}, h={h})"
         el = float(np.abs(gl[~dead] - rl[~dead]).max()) if (~dead).any() else 0.0
         assert np.all(go[dead] == 0), "rows that see no key must have O = 0"
         worst_o, worst_l = max(worst_o, eo), max(worst_l, el)
-        assert eo <= O_TOL, f"O error {eo} at (b={b}, h={h})"
+        assert eo <= O_TOL, f"O error {eo} beyond the bf16 output rounding at (b={b}, h={h})"
         assert el <= LSE_TOL, f"LSE error {el} at (b={b}, h={h})"
     return worst_o, worst_l
 

@@ -11,7 +11,7 @@ import masked_attention_bound_gb300 as fm
 from fm_inputs import masks as gen
 from fm_inputs.configs import (LOCALIZE_64K, LOCALIZE_RANKS, LONG_128K, SUITE_32K, SWEEP_4K, TINY,
                                TINY_DOCS, dual_chunk_map)
-from fm_inputs.tensors import bounds_tensor, mask_bounds, qkv_do
+from fm_inputs.tensors import bounds_tensor, mask_bounds, qkv_do, randn_bf16
 from parity import GRAD_REL, O_TOL, compare_bwd, compare_fwd
 
 pytestmark = pytest.mark.gpu
@@ -59,8 +59,8 @@ def test_fully_masked_rows_and_columns_are_zero():
 
 def test_per_head_masks_strides_and_cross_lengths():
     B, Sq, Skv, H, d = 2, 384, 640, 3, 128
-    base_q = torch.randn(B, Sq, H, 2 * d, device="cuda").bfloat16()
-    base_kv = torch.randn(B, Skv, H, 2 * d, device="cuda").bfloat16()
+    base_q = randn_bf16(B, Sq, H, 2 * d, seed=11, device="cuda")
+    base_kv = randn_bf16(B, Skv, H, 2 * d, seed=12, device="cuda")
     q = base_q[..., :d]
     do = base_q[..., d:]
     k, v = base_kv[..., :d], base_kv[..., d:]

@@ -7,7 +7,7 @@ import torch
 import masked_attention_bound_gb300 as fm
 from fm_inputs import masks as gen
 from fm_inputs.configs import LONG_128K, SUITE_32K, SWEEP_4K, TINY, TINY_DOCS
-from fm_inputs.tensors import bounds_tensor, mask_bounds, qkv_do
+from fm_inputs.tensors import bounds_tensor, mask_bounds, qkv_do, randn_bf16
 from oracle import masks as om
 from parity import compare_fwd
 
@@ -41,10 +41,15 @@ def test_small_shapes(name, S, d):
     compare_fwd(q, k, v, bounds, d ** -0.5, o, lse)
 
 
-def test_per_head_masks_and_strides():
+# seed 267 is a named case: its head (b=0, h=1) has an element that the bf16
+# rounding of P and of the output alone puts 0.011 from the exact result (see
+# tests/test_rounding_model.py); it passes the bar, which allows for the
+# output's rounding on top of 1e-2
+@pytest.mark.parametrize("seed", [0, 1, 2, 267])
+def test_per_head_masks_and_strides(seed):
     """Hm = H, and Q/K/V/O as non-contiguous views (head-dim still contiguous)."""
     B, S, H, d = 2, 640, 3, 128
-    base = torch.randn(B, S, H, 3 * d, device="cuda").bfloat16()
+    base = randn_bf16(B, S, H, 3 * d, seed=seed, device="cuda")
     q, k, v = base[..., :d], base[..., d:2 * d], base[..., 2 * d:]
     per_b = [[gen.make_mask(n, S, seed=b) for n in ("causal", "share_question", "prefix_document")]
              for b in range(B)]
@@ -57,6 +62,32 @@ def test_per_head_masks_and_strides():
     torch.cuda.synchronize()
     assert torch.all(o_big[..., :d] == 0)
     compare_fwd(q, k, v, bounds, 0.1, o, lse)
+
+
+def test_forward_matches_its_rounding_model():
+    """The kernel's O equals the rounding model of tests/rounding_model.py (fp32
+    scores and sums, bf16 P, bf16 output) up to one bf16 ulp in under 1 % of
+    the elements (the two sum in different orders), on the seed-267 inputs of
+    the per-head test, whose worst element is 0.011 from the exact result."""
+    import rounding_model as rm
+    B, S, H, d = 2, 640, 3, 128
+    base = randn_bf16(B, S, H, 3 * d, seed=267, device="cuda")
+    q, k, v = base[..., :d], base[..., d:2 * d], base[..., 2 * d:]
+    per_b = [[gen.make_mask(n, S, seed=b) for n in ("causal", "share_question", "prefix_document")]
+             for b in range(B)]
+    bounds = bounds_tensor(per_b, device="cuda")
+    o, _ = fm.forward(q, k, v, bounds, 0.1)
+    torch.cuda.synchronize()
+    bc = base.float().cpu().numpy().astype(np.float64)
+    oc = o.float().cpu().numpy()
+    for b in range(B):
+        for h in range(H):
+            M = om.dense_mask(*per_b[b][h], S)
+            model, _ = rm.forward_head(bc[b, :, h, :d], bc[b, :, h, d:2 * d], bc[b, :, h, 2 * d:], M, 0.1)
+            diff = np.abs(oc[b, :, h] - model)
+            ulp = 2 * rm.bf16_half_ulp(np.maximum(np.abs(oc[b, :, h]), np.abs(model)))
+            assert np.all(diff <= ulp + 1e-12), (b, h, float(diff.max()))
+            assert (diff > 0).mean() < 0.01, (b, h, float((diff > 0).mean()))
 
 
 def test_cross_lengths():

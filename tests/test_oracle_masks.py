@@ -250,19 +250,40 @@ def _table_of(b, S):
     return om.tile_table(bounds, S)
 
 
-def test_pair_lists_by_hand():
-    """Causal, S = 384: tile (qi, kj) is FULL below the diagonal, PARTIAL on
-    it, EMPTY above.  Pair 0 = rows 0, 1; pair 1 = row 2 alone (nQ = 3).
-    Full mask, S = 300: every tile FULL, but the ragged last k-tile is PARTIAL."""
+def test_col_lists_by_hand():
+    """Column lists in order and with their classes, worked out by hand.
+
+    From a hand-written table (rows = q-tiles, columns = k-tiles):
+        q0: FULL    PARTIAL EMPTY
+        q1: EMPTY   PARTIAL FULL
+        q2: PARTIAL EMPTY   PARTIAL
+    column 0 holds q-tiles 0 (FULL), 2 (PARTIAL); column 1 q-tiles 0, 1
+    (both PARTIAL); column 2 q-tiles 1 (FULL), 2 (PARTIAL).  The table is not
+    symmetric, so returning row lists for column lists fails.
+
+    Then from a mask: causal documents [0, 200) and [200, 384), S = 384, by
+    hand.  (q0, k0), (q1, k1), (q2, k2) hold the diagonal (PARTIAL); (q1, k0)
+    has rows 128..199 that see every key of k0 and rows 200..255 in the next
+    document (PARTIAL); (q2, k0): every key of k0 is in document 0, whose lower
+    interval [200, 384) covers rows 256..383 (EMPTY); (q2, k1): keys 128..199
+    are hidden from rows 256..383, keys 200..255 are seen by all of them
+    (PARTIAL); the tiles above the diagonal are covered by the upper
+    interval [0, j) (EMPTY).  Column lists: k0 -> q0, q1; k1 -> q1, q2;
+    k2 -> q2."""
     P, F, E = om.PARTIAL, om.FULL, om.EMPTY
-    n, c, lst = om.pair_lists(_table_of(gen.causal(384), 384), 384)
-    assert lst[(0, 0, 0)] == [(0, P, F), (1, E, P)]
-    assert lst[(0, 0, 1)] == [(0, F, E), (1, F, E), (2, P, E)]
-    assert n.tolist() == [[[2, 3]]] and c.tolist() == [[[3, 3]]]
-    n, c, lst = om.pair_lists(_table_of(gen.full(300), 300), 300)
-    assert lst[(0, 0, 0)] == [(0, F, F), (1, F, F), (2, P, P)]
-    assert lst[(0, 0, 1)] == [(0, F, E), (1, F, E), (2, P, E)]
-    assert c.tolist() == [[[6, 3]]]
+    table = np.array([[[[F, P, E], [E, P, F], [P, E, P]]]], dtype=np.uint8)
+    cc, cl = om.col_lists(table)
+    assert cc.tolist() == [[[2, 2, 2]]]
+    assert cl == {(0, 0, 0): [(0, F), (2, P)],
+                  (0, 0, 1): [(0, P), (1, P)],
+                  (0, 0, 2): [(1, F), (2, P)]}
+    derived = _table_of(gen.causal_document(384, [200, 184]), 384)
+    assert derived.tolist() == [[[[P, E, E], [P, P, E], [E, P, P]]]]
+    cc, cl = om.col_lists(derived)
+    assert cc.tolist() == [[[2, 2, 1]]]
+    assert cl == {(0, 0, 0): [(0, P), (1, P)],
+                  (0, 0, 1): [(1, P), (2, P)],
+                  (0, 0, 2): [(2, P)]}
 
 
 @pytest.mark.parametrize("name", ["causal_document", "qk_sparse", "random_eviction", "share_question"])
