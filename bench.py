@@ -36,6 +36,22 @@ WORKLOAD = dict(name="suite_32k/causal_document", B=1, H=32, S=32768, d=128, mas
 METRIC = "effective fwd+bwd TFLOP/s on visible score entries (causal-document mask, 32K, hd128)"
 
 
+# Every (workload, mask) point of the metric, measured after the headline step:
+# (name, B, H, S, d, masks, mask parameters).  The localised 64K point runs
+# four simulated ranks, one after another, each with its local query rows
+# (two chunks of 8192, dual-chunk order) against the full keys.
+PER_MASK_POINTS = (
+    ("sweep_4k", 4, 16, 4096, 128,
+     ("full", "causal", "sliding_window", "causal_document", "prefix_lm"), {}),
+    ("suite_32k", 1, 32, 32768, 128,
+     ("causal", "sliding_window", "causal_document", "bidirectional_document", "prefix_lm",
+      "prefix_document", "share_question", "causal_blockwise", "random_eviction",
+      "global_sliding", "qk_sparse", "block_sparse"), {}),
+    ("long_128k", 1, 8, 131072, 128, ("causal_document_window",), {"window": 8192}),
+    ("localize_64k", 1, 16, 65536, 128, ("causal_document",), {}),
+)
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -195,7 +211,15 @@ def run_ours(args):
     else:
         e2e_ms, h2d, d2h = run_e2e(args, fm, q, k, v, do, bounds, scale, o, lse, dq, dk, dv,
                                    ws_f, ws_b, stream, world)
-    report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2d, d2h, clk)
+    per_mask = None
+    if not args.no_per_mask and rank == 0:
+        del q, k, v, do, o, lse, dq, dk, dv, ws_f, ws_b
+        torch.cuda.empty_cache()
+        per_mask = run_per_mask(args, fm)
+    if world > 1:
+        dist.barrier()
+    report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2d, d2h, clk,
+           per_mask)
     if world > 1:
         dist.destroy_process_group()
 
@@ -277,6 +301,118 @@ def run_e2e(args, fm, q, k, v, do, bounds, scale, o, lse, dq, dk, dv, ws_f, ws_b
     return e2e_ms, h2d, d2h
 
 
+def run_per_mask(args, fm):
+    """Forward, backward and step throughput of every (workload, mask) point,
+    with the fp64 oracle timed beside each on a bounded sample.  Inputs are
+    resident in HBM; each point does 2 untimed and ``args.mask_steps`` timed
+    steps (CUDA events on the launch stream around fm_fwd and fm_bwd)."""
+    import torch
+
+    from fm_inputs.configs import LOCALIZE_RANKS, dual_chunk_map
+    from fm_inputs.tensors import mask_bounds, qkv_do
+    peak = float(_peaks()[0]["bf16_tflops"])
+    stream = torch.cuda.current_stream()
+    out = []
+    for name, B, H, S, d, masks, params in PER_MASK_POINTS:
+        if args.mask_points and name not in args.mask_points:
+            continue
+        scale = d ** -0.5
+        q, k, v, do = qkv_do(B, S, S, H, d, seed=0, device="cuda")
+        for mask in masks:
+            bounds = mask_bounds(mask, B, S, device="cuda", **params)
+            bounds_np = bounds.cpu().numpy()
+            n_vis = _visible_entries(bounds_np, S, H)
+            if name == "localize_64k":
+                # simulated ranks: local Q / dO rows, localised bounds, full K / V
+                ranks = []
+                for chunks in dual_chunk_map(S, LOCALIZE_RANKS):
+                    rows = torch.cat([torch.arange(g, g + c, device="cuda") for g, c in chunks])
+                    ranks.append((q[:, rows].contiguous(), do[:, rows].contiguous(),
+                                  fm.localize(bounds, chunks)))
+            else:
+                ranks = [(q, do, bounds)]
+            bufs = []
+            for ql, dol, bl in ranks:
+                o = torch.empty_like(ql)
+                lse = torch.empty(B, H, ql.shape[1], dtype=torch.float32, device="cuda")
+                desc = fm.make_desc(ql, k, v, o)
+                bufs.append((ql, dol, bl, o, lse, torch.empty_like(ql), torch.empty_like(k),
+                             torch.empty_like(v), fm.workspace(desc, False), fm.workspace(desc, True)))
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4 * args.mask_steps)]
+            for i in range(2 + args.mask_steps):
+                timed = i >= 2
+                j = (i - 2) * 4
+                if timed:
+                    ev[j].record(stream)
+                for ql, dol, bl, o, lse, dq, dk, dv, wf, wb in bufs:
+                    fm.forward(ql, k, v, bl, scale, o=o, lse=lse, ws=wf, stream=stream)
+                if timed:
+                    ev[j + 1].record(stream)
+                for ql, dol, bl, o, lse, dq, dk, dv, wf, wb in bufs:
+                    fm.backward(ql, k, v, o, lse, dol, bl, scale, dq=dq, dk=dk, dv=dv, ws=wb,
+                                stream=stream)
+                if timed:
+                    ev[j + 2].record(stream)
+            torch.cuda.synchronize()
+            for b_ in bufs:
+                if fm.device_status(b_[8]) != 0 or fm.device_status(b_[9]) != 0:
+                    raise RuntimeError(f"device status not OK for {name}/{mask}")
+            n = args.mask_steps
+            fwd_ms = sum(ev[4 * i].elapsed_time(ev[4 * i + 1]) for i in range(n)) / n
+            bwd_ms = sum(ev[4 * i + 1].elapsed_time(ev[4 * i + 2]) for i in range(n)) / n
+            ff, fb = 4.0 * d * n_vis, 10.0 * d * n_vis
+            tot = (ff + fb) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12
+            row = {"workload": name, "mask": mask, "B": B, "H": H, "S": S, "d": d,
+                   "visible_entries": n_vis,
+                   "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4),
+                   "fwd_tflops": round(ff / (fwd_ms * 1e-3) / 1e12, 1),
+                   "bwd_tflops": round(fb / (bwd_ms * 1e-3) / 1e12, 1),
+                   "tflops": round(tot, 1), "pct_bf16_peak": round(100.0 * tot / peak, 1)}
+            if name == "localize_64k":
+                row["note"] = (f"{LOCALIZE_RANKS} simulated ranks one after another on one GPU, "
+                               "each fm_localize'd bounds, local Q/dO x full K/V")
+            if not args.no_cpu_baseline:
+                row["oracle"] = oracle_point(bounds_np, S, d, args.mask_oracle_seconds)
+            out.append(row)
+            del bufs, ranks
+        del q, k, v, do
+        torch.cuda.empty_cache()
+    return out
+
+
+def oracle_point(bounds_np, S, d, seconds):
+    """The fp64 oracle, as it stands, on a bounded sample of one point: the
+    backward pass (with its forward) of query rows [S/2, S/2 + R) of one head,
+    R doubled from 64 until about ``seconds`` pass.  Those rows see the full
+    key axis through bounds localised to them (oracle.masks.localize_bounds),
+    so the sample is the same computation as in the full problem; the value
+    is per visible entry of the sample."""
+    import numpy as np
+
+    from oracle import attention as oa
+    from oracle import masks as om
+    rng = np.random.default_rng(1)
+    q, k, v, do = (rng.standard_normal((S, d)).astype(np.float32).astype(np.float64) for _ in range(4))
+    R, el, work = 64, 0.0, 0
+    while True:
+        r0 = S // 2
+        R = min(R, S - r0)
+        lb = om.localize_bounds(bounds_np[:, :1, :1], [(r0, R)])
+        mvec = tuple(lb[t, 0, 0] for t in range(4))
+        t0 = time.perf_counter()
+        oa.backward_head(q[r0:r0 + R], k, v, do[r0:r0 + R], mvec, d ** -0.5, slice_rows=256,
+                         skip_hidden=True)
+        el = time.perf_counter() - t0
+        work = om.visible_count(*mvec, R)
+        if el >= seconds or R >= S - S // 2:
+            break
+        R *= 2
+    return {"value": round(14.0 * d * work / max(el, 1e-9) / 1e12, 6), "unit": "TFLOP/s",
+            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"backward of query rows [{S // 2}, {S // 2 + R}) of one head, {work} visible "
+                      f"entries in {el:.2f} s"}
+
+
 def _traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu record, or None
     when the kernel's sources have changed since the counters were taken."""
@@ -295,7 +431,8 @@ def _traffic(kernel: str):
     return int(rec["bytes_per_launch"]) if m.hexdigest() == rec["sources_sha256"] else None
 
 
-def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2d, d2h, clk):
+def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2d, d2h, clk,
+           per_mask=None):
     B, H, S, d = W["B"], W["H"], W["S"], W["d"]
     flop_step = flop_fwd + flop_bwd
     if rank == 0:
@@ -349,6 +486,8 @@ def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2
                            "move while step i computes"},
             "clocks": clk,
         }
+        if per_mask is not None:
+            out["per_mask"] = per_mask
         if not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
         print(json.dumps(out), flush=True)
@@ -446,6 +585,13 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-per-mask", action="store_true",
+                    help="skip the per-(workload, mask) measurements after the headline step")
+    ap.add_argument("--mask-steps", type=int, default=5, help="timed steps per (workload, mask)")
+    ap.add_argument("--mask-oracle-seconds", type=float, default=0.6,
+                    help="CPU seconds of oracle sample per (workload, mask)")
+    ap.add_argument("--mask-points", nargs="*", default=None,
+                    help="only these workloads of the per-mask sweep")
     ap.add_argument("--heads", type=int, default=0,
                     help="override H (smaller cases for profiler captures; not a bench line)")
     args = ap.parse_args()

@@ -199,6 +199,20 @@ fm_status fm_profile_enable(int on);
 fm_status fm_profile_read(double* total_ms, int* launches, int n);
 const char* fm_kernel_name(int id);
 
+/* Test hooks for the device-side wait limit (process-wide; they apply to
+ * every launch made after the call).  Every mbarrier wait in the attention
+ * kernels gives up after wait_limit_ns nanoseconds (0 restores the default of
+ * 2 s); the launch then records FM_ERR_TIMEOUT in its status word, finishes
+ * the copies and MMAs it has issued, frees its tensor memory and returns,
+ * leaving its outputs undefined.  withhold_release makes one consumer
+ * release never happen, so that a wait runs out on purpose: 0 none,
+ * 1 fm_fwd (the softmax warps of the first q-tile of each unit pair skip
+ * their first "P ready" arrival in each CTA), 2 fm_bwd (the compute warps
+ * skip their first "P ready" arrival in each CTA).  For tests of the unwind
+ * path only; calls that overlap a change of these settings see either value.
+ * FM_ERR_INVALID for other withhold values. */
+fm_status fm_test_hooks(uint64_t wait_limit_ns, int withhold_release);
+
 /* Synchronise `stream` and read the device status word of `ws`: FM_OK,
  * FM_ERR_BOUNDS, FM_ERR_TIMEOUT, or FM_ERR_CUDA if a kernel found its shared
  * memory misaligned and did nothing (precedence: CUDA, timeout, bounds). */

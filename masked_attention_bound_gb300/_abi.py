@@ -60,6 +60,7 @@ SIGNATURES = {
     "fm_localize": (ctypes.c_int, [I32P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
                                    ctypes.c_int, I32P, P]),
     "fm_device_status": (ctypes.c_int, [P, P]),
+    "fm_test_hooks": (ctypes.c_int, [ctypes.c_uint64, ctypes.c_int]),
     "fm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fm_version": (ctypes.c_int, []),
     "fm_profile_enable": (ctypes.c_int, [ctypes.c_int]),

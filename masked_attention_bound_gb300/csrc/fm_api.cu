@@ -18,6 +18,12 @@ int num_sms() {
   return n;
 }
 
+namespace {
+TestHooks g_hooks = {FM_WAIT_LIMIT_NS, 0};
+}  // namespace
+
+TestHooks test_hooks() { return g_hooks; }
+
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 static bool strides_ok(const int64_t* st) {
@@ -223,6 +229,13 @@ fm_status fm_device_status(const void* ws, void* stream) {
   if (word & DEV_LAYOUT) return FM_ERR_CUDA;
   if (word & DEV_TIMEOUT) return FM_ERR_TIMEOUT;
   if (word & DEV_BOUNDS) return FM_ERR_BOUNDS;
+  return FM_OK;
+}
+
+fm_status fm_test_hooks(uint64_t wait_limit_ns, int withhold_release) {
+  if (withhold_release < 0 || withhold_release > 2) return FM_ERR_INVALID;
+  g_hooks.wait_ns = wait_limit_ns ? wait_limit_ns : FM_WAIT_LIMIT_NS;
+  g_hooks.withhold = withhold_release;
   return FM_OK;
 }
 

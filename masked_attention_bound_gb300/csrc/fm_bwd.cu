@@ -209,6 +209,8 @@ struct BwdParams {
   __nv_bfloat16* dv;
   int64_t k_stride[3], v_stride[3];
   int* status;
+  uint64_t wait_ns;  // limit of every mbarrier wait
+  int withhold;      // test hook: 2 = the compute warps withhold their first P-ready arrival
 };
 
 // Tile pipeline per q-tile t of a unit (MMA issue order on the left, other
@@ -298,7 +300,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   auto wait = [&](int b, uint32_t parity) -> bool {
     if (*abort_flag) return false;
-    if (!mbar_wait(bar(b), parity, P.status)) {
+    if (!mbar_wait(bar(b), parity, P.status, P.wait_ns)) {
       *abort_flag = 1;
       return false;
     }
@@ -367,7 +369,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
       }
       // drain every issued copy before exit
-      if (un > 0) mbar_wait(bar(C_KVFULL), (un - 1) & 1, P.status);
+      if (un > 0) mbar_wait(bar(C_KVFULL), (un - 1) & 1, P.status, P.wait_ns);
     }
     __syncwarp();
   } else if (warp == QTMA_WARP) {
@@ -413,7 +415,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
       // drain every issued copy before exit
       for (uint32_t k = (it > 2u ? it - 2u : 0u); k < it; ++k)
-        mbar_wait(bar(C_QFULL0 + (k & 1)), (k >> 1) & 1, P.status);
+        mbar_wait(bar(C_QFULL0 + (k & 1)), (k >> 1) & 1, P.status, P.wait_ns);
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
@@ -422,6 +424,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t idKB = idesc_bf16(128, D, false, true);     // dV, dK (B MN-major)
       constexpr uint32_t idDQ = idesc_bf16(128, D, true, true);      // dQ (A, B MN-major)
+      // operand descriptors of each buffer, computed once (each MMA adds a
+      // constant offset); "k" = K-major view, "m" = MN-major view
+      const uint32_t dKk = sdesc_lo(sK, 16), dKm = sdesc_lo(sK, 16384);
+      const uint32_t dVk = sdesc_lo(sV, 16);
+      const uint32_t dSk = sdesc_lo(sDS, 16), dSm = sdesc_lo(sDS, 16384);
+      const uint32_t dQk0 = sdesc_lo(sbase + C::OFF_Q, 16), dQm0 = sdesc_lo(sbase + C::OFF_Q, 16384);
+      const uint32_t dOk0 = sdesc_lo(sbase + C::OFF_DO, 16), dOm0 = sdesc_lo(sbase + C::OFF_DO, 16384);
       uint32_t it = 0, un = 0, cn = 0;
       bool ok = true;
       while (ok) {
@@ -434,8 +443,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if (!wait(C_KVFULL, un & 1)) break;
         for (int t = 0; t < n; ++t, ++it) {
           const int st = it & 1;
-          const uint32_t sQ = sbase + C::OFF_Q + st * C::TILE;
-          const uint32_t sDO = sbase + C::OFF_DO + st * C::TILE;
+          const uint32_t stage = st * (C::TILE >> 4);
+          const uint32_t dQk = dQk0 + stage, dQm = dQm0 + stage;
+          const uint32_t dOk = dOk0 + stage, dOm = dOm0 + stage;
           if (!wait(C_QFULL0 + st, (it >> 1) & 1)) { ok = false; break; }
           // S^T overwrites P^T of the previous tile in region A: the dV that
           // reads it was issued earlier, and MMAs issued by this thread run in
@@ -444,8 +454,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tbase + C::T_A, sdesc_sw128(sK + koff, 16, 1024),
-                   sdesc_sw128(sQ + koff, 16, 1024), idSS, kk > 0 ? 1u : 0u);
+            mma_ss(tbase + C::T_A, sdesc_at(dKk, koff), sdesc_at(dQk, koff), idSS,
+                   kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(C_SFULL));
           // dP^T into region B once the previous dQ tile was drained
@@ -454,8 +464,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tbase + C::T_B, sdesc_sw128(sV + koff, 16, 1024),
-                   sdesc_sw128(sDO + koff, 16, 1024), idSS, kk > 0 ? 1u : 0u);
+            mma_ss(tbase + C::T_B, sdesc_at(dVk, koff), sdesc_at(dOk, koff), idSS,
+                   kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(C_DPFULL));
           // dV += P^T dO once P^T is in TMEM (and the previous unit's dV/dK were read)
@@ -467,7 +477,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             // P^T of q columns 0..63 sits in TMEM columns [0,32), 64..127 in [64,96)
             const uint32_t acol = (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
             mma_ts(tbase + C::T_DV, tbase + C::T_A + acol,
-                   sdesc_sw128(sDO + kk * 2048, 16384, 1024), idKB, (t > 0 || kk > 0) ? 1u : 0u);
+                   sdesc_at(dOm, kk * 2048), idKB, (t > 0 || kk > 0) ? 1u : 0u);
           }
           // dQ = dS K and dK += dS^T Q once dS^T is in smem; dQ first, so its
           // drain (which frees region B for the next dP^T) starts earlier.
@@ -477,14 +487,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tbase + C::T_B, sdesc_sw128(sDS + kk * 2048, 16384, 1024),
-                   sdesc_sw128(sK + kk * 2048, 16384, 1024), idDQ, kk > 0 ? 1u : 0u);
+            mma_ss(tbase + C::T_B, sdesc_at(dSm, kk * 2048), sdesc_at(dKm, kk * 2048), idDQ,
+                   kk > 0 ? 1u : 0u);
           mma_commit(bar(C_DQFULL));
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tbase + C::T_DK, sdesc_sw128(sDS + aoff, 16, 1024),
-                   sdesc_sw128(sQ + kk * 2048, 16384, 1024), idKB, (t > 0 || kk > 0) ? 1u : 0u);
+            mma_ss(tbase + C::T_DK, sdesc_at(dSk, aoff), sdesc_at(dQm, kk * 2048), idKB,
+                   (t > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(bar(C_QEMPTY0 + st));
         }
@@ -494,7 +504,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         ++un;
       }
       mma_commit(bar(C_DRAIN));
-      mbar_wait(bar(C_DRAIN), 0, P.status);
+      mbar_wait(bar(C_DRAIN), 0, P.status, P.wait_ns);
     }
     __syncwarp();
   }  // warp 15: spare warp of the producer warpgroup
@@ -666,7 +676,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tmem_wait_st();
         }
         tc_fence_before();
-        mbar_arrive(bar(C_PREADY));
+        // (a test of the wait limit withholds the first P-ready arrival: the
+        // MMA thread then gives up on it and the launch unwinds with DEV_TIMEOUT)
+        if (!(P.withhold == 2 && it == 0)) mbar_arrive(bar(C_PREADY));
         // ---- dS^T = P^T o (dP^T - D), to smem as bf16 [key][q] (slab = half)
         if (!wait_all(C_DPFULL, it & 1)) { ok = false; break; }
         tc_fence_after();
@@ -827,6 +839,9 @@ static fm_status launch_bwd_d(const Plan& p, const fm_desc& desc, const TensorAr
     P.v_stride[i] = desc.v_stride[i];
   }
   P.status = reinterpret_cast<int*>(ws + p.L.status);
+  const TestHooks th = test_hooks();
+  P.wait_ns = th.wait_ns;
+  P.withhold = th.withhold;
   auto kern = bwd_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)

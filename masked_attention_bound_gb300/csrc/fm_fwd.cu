@@ -69,7 +69,7 @@ struct FwdCfg {
 // barrier slots; "s" = q-tile slot (0 = a, 1 = b), "st" = K/V stage (0/1)
 enum {
   B_QFULL0 = 0, B_QEMPTY0 = 2, B_SFULL0 = 4, B_PFULL0 = 6, B_PVDONE0 = 8, B_OEMPTY0 = 10,
-  B_KFULL0 = 12, B_KEMPTY0 = 14, B_VFULL0 = 16, B_VEMPTY0 = 18, B_MEMPTY0 = 20, B_DRAIN = 22,
+  B_KFULL0 = 12, B_VFULL0 = 16, B_KVEMPTY0 = 18, B_MEMPTY0 = 20, B_DRAIN = 22,
   B_UFULL0 = 23, B_UEMPTY0 = 27
 };
 // Units are claimed at run time (one atomic counter per launch, in the
@@ -104,6 +104,8 @@ struct FwdParams {
   int64_t o_stride[3];
   float* lse;
   int* status;
+  uint64_t wait_ns;  // limit of every mbarrier wait
+  int withhold;      // test hook: 1 = slot a's softmax withholds its first P-ready arrival
 };
 
 // Each CTA claims units idx = 0, 1, 2, ... of the longest-first order as it
@@ -172,9 +174,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       mbar_init(bar(B_PVDONE0 + s), 1);
       mbar_init(bar(B_OEMPTY0 + s), 128);
       mbar_init(bar(B_KFULL0 + s), 1);
-      mbar_init(bar(B_KEMPTY0 + s), 2);  // one commit per MMA thread
       mbar_init(bar(B_VFULL0 + s), 1);
-      mbar_init(bar(B_VEMPTY0 + s), 2);
+      // stage s of K, V (and the bits) is free again once both MMA threads
+      // are past its PV: one commit per MMA thread per entry
+      mbar_init(bar(B_KVEMPTY0 + s), 2);
       // per stage: 128 arrivals for each slot, from its softmax threads when
       // the slot's tile there is partial (they read the bits), else from the
       // load warp on the slot's behalf
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 
   auto wait = [&](int b, uint32_t parity) -> bool {
     if (*abort_flag) return false;
-    if (!mbar_wait(bar(b), parity, P.status)) {
+    if (!mbar_wait(bar(b), parity, P.status, P.wait_ns)) {
       *abort_flag = 1;
       return false;
     }
@@ -348,7 +351,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const int kj = ent >> 4, ca = (ent >> 2) & 3, cb = ent & 3;
         const int st = e & 1;
         const uint32_t use = e >> 1;
-        if (use > 0 && !wait_all(B_KEMPTY0 + st, (use - 1) & 1)) { ok = false; break; }
+        if (use > 0 && !wait_all(B_KVEMPTY0 + st, (use - 1) & 1)) { ok = false; break; }
         if (use > 0 && !wait_all(B_MEMPTY0 + st, (use - 1) & 1)) { ok = false; break; }
         int ms0 = -1, ms1 = -1;  // precomputed mask slots (bulk-copied below)
         if (ca == CLS_PARTIAL) {
@@ -398,9 +401,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // the end marker below, which completes one more phase of a stage)
     if (lane == 0) {
       for (uint32_t x = (e > 2u ? e - 2u : 0u); x < e; ++x)
-        mbar_wait(bar(B_KFULL0 + (x & 1)), (x >> 1) & 1, P.status);
-      if (qn.v0 > 0) mbar_wait(bar(B_QFULL0), (qn.v0 - 1) & 1, P.status);
-      if (qn.v1 > 0) mbar_wait(bar(B_QFULL0 + 1), (qn.v1 - 1) & 1, P.status);
+        mbar_wait(bar(B_KFULL0 + (x & 1)), (x >> 1) & 1, P.status, P.wait_ns);
+      if (qn.v0 > 0) mbar_wait(bar(B_QFULL0), (qn.v0 - 1) & 1, P.status, P.wait_ns);
+      if (qn.v1 > 0) mbar_wait(bar(B_QFULL0 + 1), (qn.v1 - 1) & 1, P.status, P.wait_ns);
     }
     // the end marker: one more entry word, no tiles, so the MMA warps stop.
     // Like any entry it waits until the entry two before has been read by
@@ -410,7 +413,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     if (ok) {
       const int st = e & 1;
       const uint32_t use = e >> 1;
-      if (use > 0) ok = wait_all(B_KEMPTY0 + st, (use - 1) & 1);
+      if (use > 0) ok = wait_all(B_KVEMPTY0 + st, (use - 1) & 1);
       if (ok && use > 0) ok = wait_all(B_MEMPTY0 + st, (use - 1) & 1);
       if (ok && lane == 0) {
         desc[st] = E_END;
@@ -432,7 +435,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           const int kj = P.pair_list[static_cast<size_t>(u.prow) * P.nK + t] >> 4;
           const int st = e & 1;
           const uint32_t use = e >> 1;
-          if (use > 0 && !wait(B_VEMPTY0 + st, (use - 1) & 1)) { ok = false; break; }
+          if (use > 0 && !wait(B_KVEMPTY0 + st, (use - 1) & 1)) { ok = false; break; }
           mbar_arrive_expect_tx(bar(B_VFULL0 + st), C::TILE);
 #pragma unroll
           for (int x = 0; x < C::SLABS; ++x)
@@ -445,7 +448,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // drain: every issued copy has landed before the CTA may exit
     if (lane == 0)
       for (uint32_t x = (e > 2u ? e - 2u : 0u); x < e; ++x)
-        mbar_wait(bar(B_VFULL0 + (x & 1)), (x >> 1) & 1, P.status);
+        mbar_wait(bar(B_VFULL0 + (x & 1)), (x >> 1) & 1, P.status, P.wait_ns);
     __syncwarp();
   } else if (warp == MMA_WARP || warp == MMA_WARP_B) {
     // ------------------------------------------------------------ MMA issuers
@@ -463,6 +466,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
       const uint32_t sQ = sbase + C::OFF_Q + s * C::TILE;
+      // operand descriptors of each buffer, computed once (each MMA adds a
+      // constant offset): Q and K K-major, V MN-major
+      const uint32_t dQ = sdesc_lo(sQ, 16);
+      const uint32_t dK0 = sdesc_lo(sbase + C::OFF_K, 16);
+      const uint32_t dV0 = sdesc_lo(sbase + C::OFF_V, 128 * 128);
       const uint32_t tS = tbase + 128 * s, tO = tbase + 256 + 128 * s;
       uint32_t qn = 0, np = 0, un = 0;
       // entry word of entry e, once its K tile (and bits) have landed
@@ -480,12 +488,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           ++qn;
         }
         tc_fence_after();
-        const uint32_t sK = sbase + C::OFF_K + (e & 1) * C::TILE;
+        const uint32_t dK = dK0 + (e & 1) * (C::TILE >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tS, sdesc_sw128(sQ + koff, 16, 1024), sdesc_sw128(sK + koff, 16, 1024), idS,
-                 kk > 0 ? 1u : 0u);
+          mma_ss(tS, sdesc_at(dQ, koff), sdesc_at(dK, koff), idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(B_SFULL0 + s));
         if (f & fLAST) mma_commit(bar(B_QEMPTY0 + s));
@@ -503,12 +510,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const int st = e & 1;
         if (!wait(B_VFULL0 + st, (e >> 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t sV = sbase + C::OFF_V + st * C::TILE;
+        const uint32_t dV = dV0 + st * (C::TILE >> 4);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tO, tS + kk * 8, sdesc_sw128(sV + kk * 2048, 128 * 128, 1024), idPV,
-                 (!first || kk > 0) ? 1u : 0u);
-        mma_commit(bar(B_PVDONE0 + s));
+          mma_ts(tO, tS + kk * 8, sdesc_at(dV, kk * 2048), idPV, (!first || kk > 0) ? 1u : 0u);
+        // the epilogue reads O after the unit's last PV only
+        if (f & fLAST) mma_commit(bar(B_PVDONE0 + s));
         return true;
       };
       // entries arrive in order until the end marker; per entry: this
@@ -517,7 +524,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       bool ok = entry(0, fc);
       if (ok && !(fc & E_END)) {
         if (fc & fA) ok = issue_s(0, fc);
-        if (ok) mma_commit(bar(B_KEMPTY0));
         for (uint32_t j = 0; ok; ++j) {
           uint32_t fn = 0;
           // release V(j) only once it has landed, also when this slot does
@@ -529,16 +535,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           } else if (!wait(B_VFULL0 + (j & 1), (j >> 1) & 1)) {
             break;
           }
-          mma_commit(bar(B_VEMPTY0 + (j & 1)));
+          mma_commit(bar(B_KVEMPTY0 + (j & 1)));
           if (!entry(j + 1, fn)) break;
           if (fn & E_END) break;
           if ((fn & fA) && !issue_s(j + 1, fn)) break;
-          mma_commit(bar(B_KEMPTY0 + ((j + 1) & 1)));
           fc = fn;
         }
       }
       mma_commit(bar(B_DRAIN));
-      mbar_wait(bar(B_DRAIN), 0, P.status);
+      mbar_wait(bar(B_DRAIN), 0, P.status, P.wait_ns);
     }
     __syncwarp();
   }
@@ -552,6 +557,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const uint32_t tS = tbase + lane_off + 128 * slot;
     const uint32_t tO = tbase + lane_off + 256 + 128 * slot;
     uint32_t e = 0, j = 0, un = 0;  // entries walked, tiles of this slot done, units claimed
+    uint32_t pd = 0;                // units of this slot with tiles (PV-done phases)
     bool ok = true;
     while (ok) {
       const int idx = claimed(un);
@@ -672,14 +678,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         l += sum;
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(B_PFULL0 + slot));
+        // (a test of the wait limit withholds the first P-ready arrival of
+        // slot a: the slot's MMA thread then gives up on it and the launch
+        // unwinds with DEV_TIMEOUT)
+        if (!(P.withhold == 1 && slot == 0 && j == 0)) mbar_arrive(bar(B_PFULL0 + slot));
         ++j;
         ++done;
       }
       if (!ok) break;
       // epilogue: O / l and LSE, after this unit's last PV.  O is read from
       // TMEM first and released, so the slot's next unit may overwrite it
-      if (!wait_all(B_PVDONE0 + slot, (j - 1) & 1)) break;
+      if (!wait_all(B_PVDONE0 + slot, pd & 1)) break;
+      ++pd;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint32_t ro[D];
@@ -735,6 +745,9 @@ static fm_status launch_fwd_d(const Plan& p, const fm_desc& desc, const TensorAr
   for (int i = 0; i < 3; ++i) P.o_stride[i] = desc.o_stride[i];
   P.lse = t.lse_out;
   P.status = reinterpret_cast<int*>(ws + p.L.status);
+  const TestHooks th = test_hooks();
+  P.wait_ns = th.wait_ns;
+  P.withhold = th.withhold;
   auto kern = fwd_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)

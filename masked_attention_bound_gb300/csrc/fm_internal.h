@@ -62,6 +62,14 @@ fm_status launch_bwd(const Plan& p, const fm_desc& desc, const TensorArgs& t, ch
 
 int num_sms();
 
+// Settings of fm_test_hooks (process-wide): the limit of every device-side
+// mbarrier wait, and which release a test withholds (0 none).
+struct TestHooks {
+  uint64_t wait_ns;
+  int withhold;
+};
+TestHooks test_hooks();
+
 // Kernel ids for the timing hooks (fm_profile_*).
 enum KernelId : int { K_SUMMARY = 0, K_CLASSIFY, K_ORDER, K_LOCALIZE, K_FWD, K_BWD_PRE, K_BWD,
                       K_DQ_CONVERT, K_TILE_MASKS, K_COUNT };

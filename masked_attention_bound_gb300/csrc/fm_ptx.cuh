@@ -77,13 +77,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait until the phase with the given parity has completed.  Returns false
-// (and records DEV_TIMEOUT) if that takes longer than FM_WAIT_LIMIT_NS.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status) {
+// (and records DEV_TIMEOUT) if that takes longer than limit_ns nanoseconds
+// (each launch passes its limit; FM_WAIT_LIMIT_NS unless a test shortened it).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status,
+                                          uint64_t limit_ns = FM_WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > FM_WAIT_LIMIT_NS) {
+    if (globaltimer() - t0 > limit_ns) {
       if (status) atomicOr(status, DEV_TIMEOUT);
       return false;
     }
@@ -246,6 +248,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   d |= static_cast<uint64_t>(1) << 46;  // descriptor version for tcgen05
   d |= static_cast<uint64_t>(2) << 61;  // 128-byte swizzle
   return d;
+}
+// The same descriptor split in two words: every tile here has sbo = 1024,
+// so the high word is one constant, and the low word holds the start address
+// (address >> 4, 14 bits) and lbo.  Shared-memory addresses stay below 2^18,
+// so adding (bytes >> 4) to a low word never carries out of the address
+// field: with a tile's low word computed once, an MMA `bytes` further on in
+// the tile needs one add.
+constexpr uint32_t kSdescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ uint64_t sdesc_at(uint32_t lo, uint32_t bytes) {
+  return (static_cast<uint64_t>(kSdescHi) << 32) | (lo + (bytes >> 4));
 }
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulation.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {

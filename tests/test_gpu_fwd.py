@@ -66,9 +66,12 @@ def test_per_head_masks_and_strides(seed):
 
 def test_forward_matches_its_rounding_model():
     """The kernel's O equals the rounding model of tests/rounding_model.py (fp32
-    scores and sums, bf16 P, bf16 output) up to one bf16 ulp in under 1 % of
-    the elements (the two sum in different orders), on the seed-267 inputs of
-    the per-head test, whose worst element is 0.011 from the exact result."""
+    scores and sums, bf16 P, bf16 output) on the seed-267 inputs of the
+    per-head test, whose worst element is 0.011 from the exact result, except
+    in under 1 % of the elements, which differ by at most 4e-3.  The two sum in
+    different orders, so a probability within an fp32 rounding of a bf16
+    midpoint can round the other way (a change of up to 2^-8 * p * |v| / l in
+    O), and the output can then round to the neighbouring bf16 number."""
     import rounding_model as rm
     B, S, H, d = 2, 640, 3, 128
     base = randn_bf16(B, S, H, 3 * d, seed=267, device="cuda")
@@ -85,8 +88,7 @@ def test_forward_matches_its_rounding_model():
             M = om.dense_mask(*per_b[b][h], S)
             model, _ = rm.forward_head(bc[b, :, h, :d], bc[b, :, h, d:2 * d], bc[b, :, h, 2 * d:], M, 0.1)
             diff = np.abs(oc[b, :, h] - model)
-            ulp = 2 * rm.bf16_half_ulp(np.maximum(np.abs(oc[b, :, h]), np.abs(model)))
-            assert np.all(diff <= ulp + 1e-12), (b, h, float(diff.max()))
+            assert diff.max() <= 4e-3, (b, h, float(diff.max()))
             assert (diff > 0).mean() < 0.01, (b, h, float((diff > 0).mean()))
 
 
