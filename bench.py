@@ -52,6 +52,12 @@ PER_MASK_POINTS = (
 )
 
 
+# GEMMs of 2 * d flop per visible entry in each attention kernel: the
+# forward S and P V; the dK/dV pass S^T, dP^T, dV, dK; the dQ pass S, dP, dQ
+# (S and dP are computed in both backward passes)
+KERNEL_GEMMS = {"fwd_kernel": 2, "bwd_kv_kernel": 4, "bwd_dq_kernel": 3}
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -437,15 +443,17 @@ def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2
     flop_step = flop_fwd + flop_bwd
     if rank == 0:
         peaks, peak_src = _peaks()
-        bwd_ms, bwd_n = prof["bwd_kernel"]
-        fwd_ms, fwd_n = prof["fwd_kernel"]
-        bwd_avg = bwd_ms / max(bwd_n, 1)
-        fwd_avg = fwd_ms / max(fwd_n, 1)
-        # the dominant kernel is the one with the larger share of device time
-        dom = "bwd_kernel" if bwd_ms >= fwd_ms else "fwd_kernel"
-        dom_flop = (flop_bwd if dom == "bwd_kernel" else flop_fwd)
-        dom_avg_ms = bwd_avg if dom == "bwd_kernel" else fwd_avg
-        achieved = dom_flop / (dom_avg_ms * 1e-3) / 1e12
+        avg = {k: prof[k][0] / max(prof[k][1], 1) for k in KERNEL_GEMMS if k in prof}
+        fwd_avg = avg["fwd_kernel"]
+        bwd_avg = avg["bwd_kv_kernel"] + avg["bwd_dq_kernel"]
+        # each attention kernel's own tensor work on the visible entries:
+        # 2 * d flop per entry and GEMM (the step's metric counts 14 * d)
+        flop_unit = flop_fwd / 4.0  # d * visible entries
+        kernel_tflops = {k: round(2 * g * flop_unit / (avg[k] * 1e-3) / 1e12, 2)
+                         for k, g in KERNEL_GEMMS.items()}
+        # the dominant kernel is the one with the largest share of device time
+        dom = max(KERNEL_GEMMS, key=lambda k: prof[k][0])
+        achieved = kernel_tflops[dom]
         # the timed loop lasts well under a second: compare with the burst figure
         peak = float(peaks["bf16_tflops"])
         value = _job_value(flop_step, ms, world)
@@ -467,8 +475,11 @@ def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2
             "config": _config(W, n_vis, world),
             "fwd_tflops": round(flop_fwd / (fwd_avg * 1e-3) / 1e12, 2),
             "bwd_tflops": round(flop_bwd / (bwd_avg * 1e-3) / 1e12, 2),
+            "kernel_tflops": kernel_tflops,
             "pct_bf16_peak": round(100.0 * value / world / peak, 1),
             "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2),
+                         "algorithmic_flop": f"{2 * KERNEL_GEMMS[dom]} * d * visible entries "
+                                             f"per launch",
                          "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                          "peak_source": f"bf16_tflops (burst) of {peak_src}",
                          "traffic": _traffic(dom) if (W["H"] == 32 and world >= 1) else None,

@@ -19,7 +19,9 @@
  *
  * Conventions for every entry point:
  *  - Tensors are caller-owned DEVICE pointers.  The library allocates and
- *    frees nothing; its only scratch is the caller's workspace `ws`.
+ *    frees nothing.  Its scratch is the caller's workspace `ws`, except for
+ *    fm_fwd_static, whose scratch is a fixed array of device memory inside
+ *    the library (see its declaration below).
  *  - Q, K, V, O, dO, dQ, dK, dV are bf16 in BSHD layout: element (b, s, h, c)
  *    at  b*stride[0] + s*stride[1] + h*stride[2] + c  (elements; the head
  *    dimension is contiguous).  Base pointers must be 16-byte aligned and the
@@ -69,9 +71,10 @@ typedef struct {
  * nQ = ceil(Sq/128), nK = ceil(Skv/128).  List entries are
  * (tile_index << 2) | class with class 1 = PARTIAL, 2 = FULL. */
 typedef struct {
-  size_t status;     /* int32[4]: [0] device status bits, [1] units claimed by the
-                        attention kernel's CTAs, [2..3] uint64 count of mask slots
-                        asked for (forward); zeroed by every call               */
+  size_t status;     /* int32[8]: [0] device status bits, [1] units claimed by the
+                        CTAs of the forward or of the dK/dV kernel, [2..3] uint64
+                        count of mask slots asked for, [4] units claimed by the
+                        CTAs of the dQ kernel; zeroed by every call              */
   size_t summary;    /* int32 [B][Hm][nK][8]: min/max of LTS, LTE, UTS, UTE per k-block */
   size_t table;      /* uint8 [B][Hm][nQ][nK]: 0 EMPTY, 1 PARTIAL, 2 FULL           */
   size_t row_count;  /* int32 [B][Hm][nQ]: non-empty tiles per q-tile row             */
@@ -82,12 +85,12 @@ typedef struct {
                         (q-tiles 2p and 2p+1), longest first                       */
   size_t bwd_order;  /* int32 [B*H*nK]: backward units u=(b*H+h)*nK+kj, longest first */
   size_t row_mask;   /* int32 [B][Hm][nQ]: first visibility-mask slot of the row's partial
-                        tiles (consecutive in list order), -1 if none (forward only)  */
+                        tiles (consecutive in list order), -1 if none              */
   size_t masks;      /* uint8 [cap][128][16], cap = min(B*Hm*nQ*nK, 65536): per partial
                         tile (and the ragged last k-tile) 128 rows of 128 column bits,
-                        bit c of 32-bit word w = column 32w+c, set = hidden (forward
-                        only).  Rows whose tiles do not fit get row_mask -1 and the
-                        forward kernel builds their bits itself                    */
+                        bit c of 32-bit word w = column 32w+c, set = hidden (the last
+                        region).  Rows whose tiles do not fit get row_mask -1 and the
+                        forward and dQ kernels build their bits themselves         */
   size_t pair_info;  /* int32 [B][Hm][nP][4]: entries of the pair list, non-empty tiles
                         of q-tile 2p, of q-tile 2p+1, and their sum (forward only) */
   size_t pair_list;  /* int32 [B][Hm][nP][nK]: union of the two q-tiles' non-empty
@@ -96,7 +99,8 @@ typedef struct {
   size_t delta;      /* float [B][H][nQ*128]: D_i = dO_i . O_i, 0 past Sq (backward)  */
   size_t lse_log2;   /* float [B][H][nQ*128]: -LSE_i * log2(e), -inf for rows that see
                         no key and past Sq (backward only)                          */
-  size_t dq_acc;     /* float [B][H][Sq][d]: fp32 dQ accumulator (backward only)      */
+  size_t row_order;  /* int32 [B*H*nQ]: dQ units u=(b*H+h)*nQ+qi (q-tile rows), longest
+                        first (backward only)                                      */
   size_t total;      /* bytes needed */
 } fm_ws_layout;
 
@@ -108,9 +112,12 @@ size_t fm_workspace_size(const fm_desc* desc, int for_bwd);
 fm_status fm_workspace_layout(const fm_desc* desc, int for_bwd, fm_ws_layout* out);
 
 /* Mask analysis into `ws`: validate the bounds (status word), the per-k-block
- * summary, the tile table, the work lists (rows for for_bwd = 0, columns for
- * for_bwd = 1) and the longest-first unit order.  fm_fwd and fm_bwd call this
- * themselves; it is exported so the tables can be inspected. */
+ * summary, the tile table, the q-tile row lists with the partial tiles' bit
+ * masks, and then for for_bwd = 0 the q-tile pair lists and the forward's
+ * longest-first unit order, for for_bwd = 1 the k-tile column lists and the
+ * longest-first orders of the dK/dV units (columns) and the dQ units (rows).
+ * fm_fwd and fm_bwd call this themselves; it is exported so the tables can
+ * be inspected. */
 fm_status fm_plan(const fm_desc* desc, const int32_t* lts, const int32_t* lte,
                   const int32_t* uts, const int32_t* ute, void* ws, size_t ws_bytes,
                   int for_bwd, void* stream);
@@ -128,7 +135,9 @@ fm_status fm_fwd(const fm_desc* desc, const void* q, const void* k, const void* 
 /* Backward pass.  Inputs q, k, v, o (bf16), lse (fp32, from fm_fwd with the
  * same bounds and scale), dout = dO (bf16, o_stride); outputs dq, dk, dv
  * (bf16).  Gradients of rows that see no key, and of columns no row sees,
- * are 0.  `ws` must hold fm_workspace_size(desc, 1) bytes. */
+ * are 0.  `ws` must hold fm_workspace_size(desc, 1) bytes.  dK and dV are
+ * accumulated per k-tile column and dQ per q-tile row, each on chip, so the
+ * outputs are written once and need no clearing beforehand. */
 fm_status fm_bwd(const fm_desc* desc, const void* q, const void* k, const void* v,
                  const void* o, const float* lse, const void* dout, const int32_t* lts,
                  const int32_t* lte, const int32_t* uts, const int32_t* ute, float scale,
@@ -191,8 +200,8 @@ fm_status fm_localize(const int32_t* bounds, int B, int Hm, int Skv,
  * kernel id the summed device time in milliseconds and the launch count into
  * total_ms[0..n) and launches[0..n) (either may be NULL), and clears the
  * record.  Kernel ids: 0 block summary, 1 classify, 2 unit order,
- * 3 localize, 4 forward, 5 backward preprocess, 6 backward, 7 dQ convert,
- * 8 partial-tile visibility masks;
+ * 3 localize, 4 forward, 5 backward preprocess, 6 backward dK/dV, 7 backward
+ * dQ, 8 partial-tile visibility masks;
  * fm_kernel_name(id) names them.  At most 65536 launches are recorded per
  * read; later launches are counted but not timed. */
 fm_status fm_profile_enable(int on);

@@ -29,7 +29,7 @@ class FmWsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status", "summary", "table", "row_count", "row_list", "col_count", "col_list",
         "fwd_order", "bwd_order", "row_mask", "masks", "pair_info", "pair_list", "delta",
-        "lse_log2", "dq_acc", "total")]
+        "lse_log2", "row_order", "total")]
 
 
 class FMError(RuntimeError):

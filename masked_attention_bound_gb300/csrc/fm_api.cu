@@ -51,7 +51,7 @@ fm_status make_plan(const fm_desc* desc, int for_bwd, Plan* p, size_t limit) {
   fm_ws_layout& L = p->L;
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t at = off; off = align256(off + bytes); return at; };
-  L.status = take(16);
+  L.status = take(32);
   L.summary = take(BHm * p->nK * 8 * 4);
   L.table = take(BHm * p->nQ * p->nK);
   L.row_count = take(BHm * p->nQ * 4);
@@ -60,33 +60,29 @@ fm_status make_plan(const fm_desc* desc, int for_bwd, Plan* p, size_t limit) {
   L.col_list = take(BHm * p->nK * p->nQ * 4);
   L.fwd_order = take(BH * p->nQ * 4);
   L.bwd_order = take(BH * p->nK * 4);
+  L.row_mask = take(BHm * p->nQ * 4);
   if (!for_bwd) {
-    // the mask region comes last and takes what the limit leaves, up to one
-    // slot per tile and kMaxMaskTiles slots
-    L.row_mask = take(BHm * p->nQ * 4);
     L.pair_info = take(BHm * p->nP * 16);
     L.pair_list = take(BHm * p->nP * p->nK * 4);
+    L.delta = 0;
+    L.lse_log2 = 0;
+    L.row_order = 0;
+  } else {
+    L.pair_info = 0;
+    L.pair_list = 0;
+    L.delta = take(BH * p->nQ * kTile * 4);
+    L.lse_log2 = take(BH * p->nQ * kTile * 4);
+    L.row_order = take(BH * p->nQ * 4);
+  }
+  {
+    // the mask region comes last and takes what the limit leaves, up to one
+    // slot per tile and kMaxMaskTiles slots
     size_t cap = BHm * p->nQ * p->nK;
     if (cap > static_cast<size_t>(kMaxMaskTiles)) cap = kMaxMaskTiles;
     const size_t room = limit > off ? (limit - off) / kMaskBytes : 0;
     if (cap > room) cap = room;
     p->mask_cap = static_cast<int>(cap);
     L.masks = take(cap * kMaskBytes);
-  } else {
-    p->mask_cap = 0;
-    L.row_mask = 0;
-    L.masks = 0;
-    L.pair_info = 0;
-    L.pair_list = 0;
-  }
-  if (for_bwd) {
-    L.delta = take(BH * p->nQ * kTile * 4);
-    L.lse_log2 = take(BH * p->nQ * kTile * 4);
-    L.dq_acc = take(BH * D.Sq * static_cast<size_t>(D.d) * 4);
-  } else {
-    L.delta = 0;
-    L.lse_log2 = 0;
-    L.dq_acc = 0;
   }
   L.total = off;
   return FM_OK;
@@ -105,12 +101,16 @@ static bool aligned16(const void* ptr) {
 static fm_status run_plan(const Plan& p, const int32_t* lts, const int32_t* lte,
                           const int32_t* uts, const int32_t* ute, char* ws, int for_bwd,
                           cudaStream_t s) {
-  if (cudaMemsetAsync(ws + p.L.status, 0, 16, s) != cudaSuccess) return FM_ERR_CUDA;
+  if (cudaMemsetAsync(ws + p.L.status, 0, 32, s) != cudaSuccess) return FM_ERR_CUDA;
   if (launch_summary(p, lts, lte, uts, ute, ws, s) != cudaSuccess) return FM_ERR_CUDA;
   if (launch_classify(p, ws, for_bwd, s) != cudaSuccess) return FM_ERR_CUDA;
-  if (!for_bwd && launch_tile_masks(p, lts, lte, uts, ute, ws, s) != cudaSuccess)
+  if (launch_tile_masks(p, lts, lte, uts, ute, ws, s) != cudaSuccess) return FM_ERR_CUDA;
+  if (!for_bwd) {
+    if (launch_order(p, ws, ORDER_PAIRS, s) != cudaSuccess) return FM_ERR_CUDA;
+  } else if (launch_order(p, ws, ORDER_COLS, s) != cudaSuccess ||
+             launch_order(p, ws, ORDER_ROWS, s) != cudaSuccess) {
     return FM_ERR_CUDA;
-  if (launch_order(p, ws, for_bwd, s) != cudaSuccess) return FM_ERR_CUDA;
+  }
   return FM_OK;
 }
 

@@ -8,29 +8,22 @@
 //   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),  D_i = dO_i . O_i,
 //   dK = scale dS^T Q,  dQ = scale dS K.
 //
-// Three kernels:
-//   bwd_pre_kernel    D_i and -LSE_i*log2(e) per query row, padded to whole
-//                     128-row tiles (-inf / 0 past Sq and on rows that see no
-//                     key, so P = 0 there without a branch), and the zeroed
-//                     fp32 dQ accumulator;
-//   bwd_kernel        one unit = one (batch, head, k-tile): K and V stay in
-//                     smem, the unit walks its column of non-empty q-tiles.
-//                     Warps 0-7 (compute): thread r owns key row r (TMEM
-//                     lane r, warp quarter w & 3) and half of the q columns
-//                     (w >> 2) of S^T and dP^T, and half of dK / dV.
-//                     Warps 8-11 (dQ): thread r owns q row r of the dQ tile
-//                     and adds it into the fp32 accumulator.
-//                     Warp 12: K/V loads, warp 14: Q/dO/LSE/D loads (TMA).
-//                     Warp 13: one thread issues tcgen05:
-//                       S^T = K Q^T, dP^T = V dO^T      (SS, both K-major)
-//                       dV += P^T dO                     (P^T from TMEM, dO MN-major)
-//                       dK += dS^T Q                     (dS^T smem K-major, Q MN-major)
-//                       dQ  = dS K                       (dS smem MN-major, K MN-major)
-//                     dQ tiles are added into an fp32 accumulator with
-//                     vector atomics; dK, dV leave once per unit;
-//   dq_convert_kernel fp32 accumulator -> bf16 dQ.
-// TMEM (512 columns): [0,128) S^T then P^T (packed bf16, 64 columns);
-// [128,256) dP^T then the dQ tile; [256,256+d) dV; [384,384+d) dK.
+// Three kernels, each over its own units:
+//   bwd_pre_kernel  D_i and -LSE_i*log2(e) per query row, padded to whole
+//                   128-row tiles (-inf / 0 past Sq and on rows that see no
+//                   key, so P = 0 there without a branch);
+//   bwd_kv_kernel   one unit = one (batch, head, k-tile): K and V stay in
+//                   smem, the unit walks its column of non-empty q-tiles and
+//                   accumulates dV and dK in TMEM (four GEMMs per tile);
+//   bwd_dq_kernel   one unit = one (batch, head, q-tile): Q and dO stay in
+//                   smem, the unit walks its row of non-empty k-tiles and
+//                   accumulates dQ in TMEM (three GEMMs per tile), written
+//                   once as bf16.
+// dQ is not reduced across k-tiles through global memory: each q-tile row
+// sums its own dQ on chip.  The price is S and dP computed twice (once per
+// kernel); the gain is no fp32 accumulator to clear, reduce into and
+// convert, and two kernels whose tensor-core work hides the softmax-side
+// arithmetic.
 #include <cuda_bf16.h>
 
 #include "fm_internal.h"
@@ -45,16 +38,14 @@ namespace fm {
 // 16-byte words part, part + 8, ... of row 4k + rr of O and of dO, so that a
 // warp load covers four whole 128-byte segments; all 16 rows' loads are
 // issued before any arithmetic (256 bytes in flight per thread).  The eight
-// partial dot products of a row are summed with shuffles.  The warp also
-// zeroes those rows of the fp32 dQ accumulator (the backward kernel adds
-// into it), with the same coalesced pattern.
+// partial dot products of a row are summed with shuffles.
 template <int D>
 __global__ void __launch_bounds__(128) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dout,
                                                       int64_t os0, int64_t os1, int64_t os2,
                                                       const float* __restrict__ lse, int B, int H,
                                                       int Sq, int rows_pad, float* delta,
-                                                      float* lse_log2, float* dq_acc) {
+                                                      float* lse_log2) {
   constexpr int W = D / 64;  // 16-byte words per lane per row
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31, rr = lane >> 3, part = lane & 7;
@@ -106,16 +97,10 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(const __nv_bfloat16* __res
   for (int sh = 1; sh < 8; sh <<= 1)
 #pragma unroll
     for (int k = 0; k < 4; ++k) dot[k] += __shfl_xor_sync(0xffffffffu, dot[k], sh);
-  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (part == 0) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int i = i0 + 4 * k + rr;
-    if (i < Sq) {
-      float4* acc_row = reinterpret_cast<float4*>(dq_acc + (static_cast<size_t>(bh) * Sq + i) * D);
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) acc_row[part + 8 * c] = z;
-    }
-    if (part == 0) {
+    for (int k = 0; k < 4; ++k) {
+      const int i = i0 + 4 * k + rr;
       float l2 = -INFINITY, dsum = 0.f;
       if (i < Sq) {
         const float L = lse[static_cast<size_t>(bh) * Sq + i];
@@ -128,34 +113,46 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(const __nv_bfloat16* __res
   }
 }
 
-// ------------------------------------------------------------------ dQ convert
-template <int D>
-__global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* dq, int64_t s0,
-                                  int64_t s1, int64_t s2, int H, int Sq, long long n_vec) {
-  // one thread per 8 consecutive elements of one row
-  for (long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; v < n_vec;
-       v += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long e = v * 8;
-    const int c = static_cast<int>(e % D);
-    const long long row = e / D;  // (b*H + h)*Sq + i
-    const int i = static_cast<int>(row % Sq);
-    const long long bh = row / Sq;
-    const int h = static_cast<int>(bh % H);
-    const int b = static_cast<int>(bh / H);
-    const float4 x = *reinterpret_cast<const float4*>(acc + e);
-    const float4 y = *reinterpret_cast<const float4*>(acc + e + 4);
-    uint4 w;
-    w.x = pack_bf16(x.x, x.y);
-    w.y = pack_bf16(x.z, x.w);
-    w.z = pack_bf16(y.x, y.y);
-    w.w = pack_bf16(y.z, y.w);
-    *reinterpret_cast<uint4*>(dq + b * s0 + static_cast<int64_t>(i) * s1 + h * s2 + c) = w;
-  }
+// Units are claimed at run time (one atomic counter per kernel, in the
+// workspace) by the warp that loads the per-unit operands, the first role to
+// need the next unit, and handed to the roles that walk units through a
+// ring of UNIT_RING slots.  Claiming just in time keeps the units in flight
+// on all CTAs close together in the head-major order (the streamed operands
+// stay in L2).
+constexpr int UNIT_RING = 4;
+
+struct BwdParams {
+  int B, H, Hm, Sq, Skv, nQ, nK, n_units;
+  float scale, scale_log2;
+  const int32_t* bounds[4];
+  const int32_t* list_count;  // units' tile counts: columns (dK/dV) or rows (dQ)
+  const int32_t* list;        // units' tile lists, entry = tile << 2 | class
+  const int32_t* order;
+  int* next_unit;             // claim counter (zero at launch)
+  const float* delta;         // [B][H][nQ*128]
+  const float* lse_log2;      // [B][H][nQ*128]
+  const int32_t* row_mask;    // dQ: first visibility-mask slot of a q-tile row, -1: none
+  const uint8_t* masks;       // dQ: 2 KB per slot, 128 rows x 128 column bits, set = hidden
+  __nv_bfloat16* out0;        // dK (dK/dV kernel) or dQ (dQ kernel)
+  __nv_bfloat16* out1;        // dV (dK/dV kernel)
+  int64_t s0[3], s1[3];       // strides of out0, out1
+  int* status;
+  uint64_t wait_ns;  // limit of every mbarrier wait
+  int withhold;      // test hook: 2 = the dK/dV compute warps withhold their first P-ready arrival
+};
+
+// Bits [a, b) of a 64-bit word, with a and b clipped to [0, 64].
+__device__ __forceinline__ uint64_t row_span(int a, int b) {
+  a = min(max(a, 0), 64);
+  b = min(max(b, 0), 64);
+  if (a >= b) return 0ull;
+  const uint64_t below_b = b == 64 ? ~0ull : ((1ull << b) - 1ull);
+  return below_b & ~((1ull << a) - 1ull);
 }
 
-// ------------------------------------------------------------------ main kernel
+// ------------------------------------------------------------------ dK / dV kernel
 template <int D>
-struct BwdCfg {
+struct KvCfg {
   static constexpr int TILE = 128 * D * 2;   // one 128-row bf16 tile
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE;
@@ -172,73 +169,39 @@ struct BwdCfg {
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   static constexpr uint32_t T_A = 0, T_B = 128, T_DV = 256, T_DK = 384, T_COLS = 512;
   // warpgroups 0-1: compute (P^T, dS^T, the dV/dK epilogue); warpgroup 2:
-  // dQ drain; warpgroup 3: the K/V load warp, the MMA warp, the Q/dO load
-  // warp and one idle warp
-  static constexpr int THREADS = 512;
-  // register split (setmaxnreg): 2 x 128 x REGS_COMPUTE + 128 x REGS_DQ +
-  // 128 x REGS_PRODUCER = 65536 = THREADS x 128 registers at launch
-  static constexpr uint32_t REGS_COMPUTE = 144, REGS_DQ = 152, REGS_PRODUCER = 72;
+  // the K/V load warp, the MMA warp, the Q/dO load warp and one idle warp
+  static constexpr int THREADS = 384;
+  // register split (setmaxnreg): 2 x 128 x REGS_COMPUTE + 128 x REGS_PRODUCER
+  // = 64512 = THREADS x 168 registers at launch
+  static constexpr uint32_t REGS_COMPUTE = 216, REGS_PRODUCER = 72;
   static constexpr int MIN_LAUNCH_REGS =
-      (2 * 128 * REGS_COMPUTE + 128 * REGS_DQ + 128 * REGS_PRODUCER + THREADS - 1) / THREADS;
+      (2 * 128 * REGS_COMPUTE + 128 * REGS_PRODUCER + THREADS - 1) / THREADS;
 };
 
-enum { C_KVFULL = 0, C_KVEMPTY, C_QFULL0, C_QFULL1, C_QEMPTY0, C_QEMPTY1, C_SFULL, C_PREADY,
-       C_DVDONE, C_DPFULL, C_DSREADY, C_DQFULL, C_DQEMPTY, C_ACCFULL, C_ACCEMPTY, C_DRAIN,
-       C_UFULL0, C_UEMPTY0 = C_UFULL0 + 4 };
-// Units are claimed at run time (one atomic counter per launch, in the
-// workspace) by the Q/dO load warp, the first role to need the next unit,
-// and handed to the other roles that walk units through a ring of
-// UNIT_RING slots; U_READERS warps read every slot: the K/V load warp, the
-// MMA warp, the eight compute warps and the four dQ warps.  Claiming just in
-// time keeps the units in flight on all CTAs close together in the
-// head-major order (Q/dO stay in L2).
-constexpr int UNIT_RING = 4, U_READERS = 14;
+enum { A_KFULL = 0, A_KEMPTY, A_VFULL, A_VEMPTY, A_QFULL0, A_QFULL1, A_QEMPTY0, A_QEMPTY1,
+       A_SFULL, A_PREADY, A_DPFULL, A_DSREADY, A_ACCFULL, A_ACCEMPTY, A_DRAIN, A_UFULL0,
+       A_UEMPTY0 = A_UFULL0 + 4 };
+// every slot of the unit ring is read by the K/V load warp, the MMA warp and
+// the eight compute warps
+constexpr int A_READERS = 10;
 
-struct BwdParams {
-  int B, H, Hm, Sq, Skv, nQ, nK, n_units;
-  float scale, scale_log2;
-  const int32_t* bounds[4];
-  const int32_t* col_count;
-  const int32_t* col_list;
-  const int32_t* order;
-  int* next_unit;         // claim counter (zero at launch)
-  const float* delta;     // [B][H][nQ*128]
-  const float* lse_log2;  // [B][H][nQ*128]
-  float* dq_acc;          // [B][H][Sq][D]
-  __nv_bfloat16* dk;
-  __nv_bfloat16* dv;
-  int64_t k_stride[3], v_stride[3];
-  int* status;
-  uint64_t wait_ns;  // limit of every mbarrier wait
-  int withhold;      // test hook: 2 = the compute warps withhold their first P-ready arrival
-};
-
-// Tile pipeline per q-tile t of a unit (MMA issue order on the left, other
-// warps on the right; region A = TMEM [0,128), region B = [128,256)):
+// MMA issue order (region A = TMEM [0,128), region B = [128,256); t-1 is the
+// previous tile of the same unit):
 //   S^T(t) = K Q^T -> A       [after dV(t-1) read P^T(t-1) from A]
-//                               dQ warps: dQ(t-1) from B to registers
-//   dP^T(t) = V dO^T -> B     [after that read]
-//                               compute: P^T(t) = exp2(S^T*scale*log2e - LSE*log2e) -> A
-//                               dQ warps: atomics of dQ(t-1)
-//   dV += P^T(t) dO           [after P^T(t)]
-//                               compute: dS^T(t) = P^T o (dP^T - D) -> smem
-//   dQ = dS K -> B, dK += dS^T Q   [after dS^T(t)]
-// so the P, dS and dQ work overlaps S, dP and dV.
-// Bits [a, b) of a 64-bit word, with a and b clipped to [0, 64].
-__device__ __forceinline__ uint64_t row_span(int a, int b) {
-  a = min(max(a, 0), 64);
-  b = min(max(b, 0), 64);
-  if (a >= b) return 0ull;
-  const uint64_t below_b = b == 64 ? ~0ull : ((1ull << b) - 1ull);
-  return below_b & ~((1ull << a) - 1ull);
-}
-
+//   dK += dS^T(t-1) Q(t-1)     [after dS^T(t-1) is in smem]
+//   dP^T(t) = V dO^T -> B     [B free: the compute warps read dP^T(t-1) before dS^T(t-1)]
+//   dV += P^T(t) dO(t)        [after P^T(t) is in TMEM]
+// and the unit's last dK after its last tile.  The compute warps work out
+// P^T(t) while dK(t-1) and dP^T(t) run, and dS^T(t) while dV(t) and S^T(t+1)
+// run, so the tensor pipe need not wait for them.  dS^T(t) goes into the
+// one dS buffer only after dP^T(t) has completed, which implies dK(t-1),
+// issued before it by the same thread, has completed too.
 template <int D>
-__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
-    bwd_kernel(const __grid_constant__ BwdParams P, const __grid_constant__ CUtensorMap tmQ,
-               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-               const __grid_constant__ CUtensorMap tmDO) {
-  using C = BwdCfg<D>;
+__global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
+    bwd_kv_kernel(const __grid_constant__ BwdParams P, const __grid_constant__ CUtensorMap tmQ,
+                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmDO) {
+  using C = KvCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {  // swizzled tiles need a 1024-aligned base
     if (threadIdx.x == 0) atomicOr(P.status, DEV_LAYOUT);
@@ -252,30 +215,29 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr int DQ_WARP0 = 8, TMA_WARP = 12, MMA_WARP = 13, QTMA_WARP = 14;
+  constexpr int KV_WARP = 8, MMA_WARP = 9, Q_WARP = 10;
 
   if (tid == 0) {
-    mbar_init(bar(C_KVFULL), 1);
-    mbar_init(bar(C_KVEMPTY), 1);
-    mbar_init(bar(C_QFULL0), 1);
-    mbar_init(bar(C_QFULL1), 1);
-    // a Q/dO stage is free once the tile's MMAs are done (commit) and the dQ
-    // warps, which use its dO buffer as transpose scratch, are done (128)
-    mbar_init(bar(C_QEMPTY0), 1 + 128);
-    mbar_init(bar(C_QEMPTY1), 1 + 128);
-    mbar_init(bar(C_SFULL), 1);
-    mbar_init(bar(C_PREADY), 256);
-    mbar_init(bar(C_DVDONE), 1);
-    mbar_init(bar(C_DPFULL), 1);
-    mbar_init(bar(C_DSREADY), 256);
-    mbar_init(bar(C_DQFULL), 1);
-    mbar_init(bar(C_DQEMPTY), 128);
-    mbar_init(bar(C_ACCFULL), 1);
-    mbar_init(bar(C_ACCEMPTY), 256);
-    mbar_init(bar(C_DRAIN), 1);
+    // K is read by the unit's S^T products only, V by its dP^T products: each
+    // is free for the next unit as soon as its last reader is done
+    mbar_init(bar(A_KFULL), 1);
+    mbar_init(bar(A_KEMPTY), 1);
+    mbar_init(bar(A_VFULL), 1);
+    mbar_init(bar(A_VEMPTY), 1);
+    mbar_init(bar(A_QFULL0), 1);
+    mbar_init(bar(A_QFULL1), 1);
+    mbar_init(bar(A_QEMPTY0), 1);  // the tile's last MMA (its dK) is done
+    mbar_init(bar(A_QEMPTY1), 1);
+    mbar_init(bar(A_SFULL), 1);
+    mbar_init(bar(A_PREADY), 8);  // one arrival per compute warp
+    mbar_init(bar(A_DPFULL), 1);
+    mbar_init(bar(A_DSREADY), 8);
+    mbar_init(bar(A_ACCFULL), 1);
+    mbar_init(bar(A_ACCEMPTY), 8);
+    mbar_init(bar(A_DRAIN), 1);
     for (int r = 0; r < UNIT_RING; ++r) {
-      mbar_init(bar(C_UFULL0 + r), 1);
-      mbar_init(bar(C_UEMPTY0 + r), U_READERS);
+      mbar_init(bar(A_UFULL0 + r), 1);
+      mbar_init(bar(A_UEMPTY0 + r), A_READERS);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -284,11 +246,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     tmem_alloc(smem_u32(tmem_slot), C::T_COLS);
     tmem_relinquish();
   }
-  if (warp == TMA_WARP && lane == 0) {
+  if (warp == KV_WARP && lane == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  if (warp == QTMA_WARP && lane == 0) {
+  if (warp == Q_WARP && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmDO);
   }
@@ -320,8 +282,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     b = bh / P.H;
     h = bh - b * P.H;
     const int col = (b * P.Hm + (P.Hm == 1 ? 0 : h)) * P.nK + kj;
-    list = P.col_list + static_cast<size_t>(col) * P.nQ;
-    return P.col_count[col];
+    list = P.list + static_cast<size_t>(col) * P.nQ;
+    return P.list_count[col];
   };
   // the n-th claimed unit (-1: none left, or the launch was aborted).
   // claimed_one: one thread of the warp reads and releases the ring slot;
@@ -329,9 +291,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   auto claimed_one = [&](uint32_t& n) -> int {
     int idx = -1;
     const int r = n % UNIT_RING;
-    if (wait(C_UFULL0 + r, (n / UNIT_RING) & 1)) {
+    if (wait(A_UFULL0 + r, (n / UNIT_RING) & 1)) {
       idx = ring[r];
-      mbar_arrive(bar(C_UEMPTY0 + r));
+      mbar_arrive(bar(A_UEMPTY0 + r));
     }
     ++n;
     return idx;
@@ -343,15 +305,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     return __shfl_sync(0xffffffffu, idx, 0);
   };
 
-  if (warp >= TMA_WARP) {
+  if (warp >= KV_WARP) {
   // producer warpgroup: small register budget (each role branch below runs
   // after the budget change, so the compiler allocates it within the budget)
   regs_decrease<C::REGS_PRODUCER>();
-  if (warp == TMA_WARP) {
+  if (warp == KV_WARP) {
     // ------------------------------------------------------------ K / V loads
     // once per unit, after the previous unit's MMAs are done with K and V
     if (lane == 0) {
-      uint32_t un = 0, cn = 0;
+      uint32_t un = 0, kn = 0, cn = 0;  // V and K loads issued
       while (true) {
         const int idx = claimed_one(cn);
         if (idx < 0) break;
@@ -359,20 +321,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         const int32_t* list;
         const int n = unit_info(idx, b, h, kj, list);
         if (n == 0) continue;
-        if (un > 0 && !wait(C_KVEMPTY, (un - 1) & 1)) break;
-        ++un;
-        mbar_arrive_expect_tx(bar(C_KVFULL), 2 * C::TILE);
+        if (un > 0 && !wait(A_KEMPTY, (un - 1) & 1)) break;
+        mbar_arrive_expect_tx(bar(A_KFULL), C::TILE);
 #pragma unroll
-        for (int s = 0; s < D / 64; ++s) {
-          tma_load_4d(sK + s * 16384, &tmK, bar(C_KVFULL), s * 64, h, kj * kTile, b);
-          tma_load_4d(sV + s * 16384, &tmV, bar(C_KVFULL), s * 64, h, kj * kTile, b);
+        for (int s = 0; s < D / 64; ++s)
+          tma_load_4d(sK + s * 16384, &tmK, bar(A_KFULL), s * 64, h, kj * kTile, b);
+        if (un > 0 && !wait(A_VEMPTY, (un - 1) & 1)) {
+          ++kn;
+          break;
         }
+        ++un;
+        ++kn;
+        mbar_arrive_expect_tx(bar(A_VFULL), C::TILE);
+#pragma unroll
+        for (int s = 0; s < D / 64; ++s)
+          tma_load_4d(sV + s * 16384, &tmV, bar(A_VFULL), s * 64, h, kj * kTile, b);
       }
       // drain every issued copy before exit
-      if (un > 0) mbar_wait(bar(C_KVFULL), (un - 1) & 1, P.status, P.wait_ns);
+      if (kn > 0) mbar_wait(bar(A_KFULL), (kn - 1) & 1, P.status, P.wait_ns);
+      if (un > 0) mbar_wait(bar(A_VFULL), (un - 1) & 1, P.status, P.wait_ns);
     }
     __syncwarp();
-  } else if (warp == QTMA_WARP) {
+  } else if (warp == Q_WARP) {
     // ------------------------------------------------------------ Q / dO / LSE / D loads
     // its own warp, so the next unit's first tiles load as soon as a stage
     // is free, without waiting for the unit's K and V
@@ -384,11 +354,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         const int r = cn % UNIT_RING;
         const uint32_t use = cn / UNIT_RING;
         ++cn;
-        if (use > 0 && !wait(C_UEMPTY0 + r, (use - 1) & 1)) break;
+        if (use > 0 && !wait(A_UEMPTY0 + r, (use - 1) & 1)) break;
         int idx = atomicAdd(P.next_unit, 1);
         if (idx >= P.n_units) idx = -1;
         ring[r] = idx;
-        mbar_arrive(bar(C_UFULL0 + r));
+        mbar_arrive(bar(A_UFULL0 + r));
         if (idx < 0) break;
         int b, h, kj;
         const int32_t* list;
@@ -398,8 +368,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           const int qi = list[t] >> 2;
           const int st = it & 1;
           const uint32_t use = it >> 1;
-          if (use > 0 && !wait(C_QEMPTY0 + st, (use - 1) & 1)) { ok = false; break; }
-          const uint32_t fb = bar(C_QFULL0 + st);
+          if (use > 0 && !wait(A_QEMPTY0 + st, (use - 1) & 1)) { ok = false; break; }
+          const uint32_t fb = bar(A_QFULL0 + st);
           mbar_arrive_expect_tx(fb, 2 * C::TILE + 1024);
           const uint32_t sQ = sbase + C::OFF_Q + st * C::TILE;
           const uint32_t sDO = sbase + C::OFF_DO + st * C::TILE;
@@ -415,7 +385,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
       // drain every issued copy before exit
       for (uint32_t k = (it > 2u ? it - 2u : 0u); k < it; ++k)
-        mbar_wait(bar(C_QFULL0 + (k & 1)), (k >> 1) & 1, P.status, P.wait_ns);
+        mbar_wait(bar(A_QFULL0 + (k & 1)), (k >> 1) & 1, P.status, P.wait_ns);
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
@@ -423,14 +393,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t idKB = idesc_bf16(128, D, false, true);     // dV, dK (B MN-major)
-      constexpr uint32_t idDQ = idesc_bf16(128, D, true, true);      // dQ (A, B MN-major)
       // operand descriptors of each buffer, computed once (each MMA adds a
       // constant offset); "k" = K-major view, "m" = MN-major view
-      const uint32_t dKk = sdesc_lo(sK, 16), dKm = sdesc_lo(sK, 16384);
+      const uint32_t dKk = sdesc_lo(sK, 16);
       const uint32_t dVk = sdesc_lo(sV, 16);
-      const uint32_t dSk = sdesc_lo(sDS, 16), dSm = sdesc_lo(sDS, 16384);
+      const uint32_t dSk = sdesc_lo(sDS, 16);
       const uint32_t dQk0 = sdesc_lo(sbase + C::OFF_Q, 16), dQm0 = sdesc_lo(sbase + C::OFF_Q, 16384);
       const uint32_t dOk0 = sdesc_lo(sbase + C::OFF_DO, 16), dOm0 = sdesc_lo(sbase + C::OFF_DO, 16384);
+      // dK += dS^T(i) Q(i) of tile i (global count), once its dS^T is in
+      // smem; then the tile's Q/dO stage is free
+      auto issue_dk = [&](uint32_t i, bool first_of_unit) -> bool {
+        if (!wait(A_DSREADY, i & 1)) return false;
+        tc_fence_after();
+        const uint32_t dQm = dQm0 + (i & 1) * (C::TILE >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tbase + C::T_DK, sdesc_at(dSk, aoff), sdesc_at(dQm, kk * 2048), idKB,
+                 (!first_of_unit || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(A_QEMPTY0 + (i & 1)));
+        return true;
+      };
       uint32_t it = 0, un = 0, cn = 0;
       bool ok = true;
       while (ok) {
@@ -440,16 +424,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         const int32_t* list;
         const int n = unit_info(idx, b, h, kj, list);
         if (n == 0) continue;
-        if (!wait(C_KVFULL, un & 1)) break;
+        if (!wait(A_KFULL, un & 1)) break;
         for (int t = 0; t < n; ++t, ++it) {
           const int st = it & 1;
           const uint32_t stage = st * (C::TILE >> 4);
-          const uint32_t dQk = dQk0 + stage, dQm = dQm0 + stage;
+          const uint32_t dQk = dQk0 + stage;
           const uint32_t dOk = dOk0 + stage, dOm = dOm0 + stage;
-          if (!wait(C_QFULL0 + st, (it >> 1) & 1)) { ok = false; break; }
-          // S^T overwrites P^T of the previous tile in region A: the dV that
-          // reads it was issued earlier, and MMAs issued by this thread run in
-          // issue order
+          if (!wait(A_QFULL0 + st, (it >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -457,9 +438,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             mma_ss(tbase + C::T_A, sdesc_at(dKk, koff), sdesc_at(dQk, koff), idSS,
                    kk > 0 ? 1u : 0u);
           }
-          mma_commit(bar(C_SFULL));
-          // dP^T into region B once the previous dQ tile was drained
-          if (it > 0 && !wait(C_DQEMPTY, (it - 1) & 1)) { ok = false; break; }
+          mma_commit(bar(A_SFULL));
+          if (t == n - 1) mma_commit(bar(A_KEMPTY));  // the unit's last reader of K
+          // the previous tile's dK, deferred until S^T of this tile is queued
+          if (t > 0 && !issue_dk(it - 1, t == 1)) { ok = false; break; }
+          if (t == 0 && !wait(A_VFULL, un & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -467,126 +450,122 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             mma_ss(tbase + C::T_B, sdesc_at(dVk, koff), sdesc_at(dOk, koff), idSS,
                    kk > 0 ? 1u : 0u);
           }
-          mma_commit(bar(C_DPFULL));
+          mma_commit(bar(A_DPFULL));
+          if (t == n - 1) mma_commit(bar(A_VEMPTY));  // the unit's last reader of V
           // dV += P^T dO once P^T is in TMEM (and the previous unit's dV/dK were read)
-          if (!wait(C_PREADY, it & 1)) { ok = false; break; }
-          if (t == 0 && un > 0 && !wait(C_ACCEMPTY, (un - 1) & 1)) { ok = false; break; }
+          if (!wait(A_PREADY, it & 1)) { ok = false; break; }
+          if (t == 0 && un > 0 && !wait(A_ACCEMPTY, (un - 1) & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             // P^T of q columns 0..63 sits in TMEM columns [0,32), 64..127 in [64,96)
             const uint32_t acol = (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-            mma_ts(tbase + C::T_DV, tbase + C::T_A + acol,
-                   sdesc_at(dOm, kk * 2048), idKB, (t > 0 || kk > 0) ? 1u : 0u);
-          }
-          // dQ = dS K and dK += dS^T Q once dS^T is in smem; dQ first, so its
-          // drain (which frees region B for the next dP^T) starts earlier.
-          // The dQ warps may then use this stage's dO buffer while dK runs:
-          // dK reads Q and dS^T only
-          if (!wait(C_DSREADY, it & 1)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tbase + C::T_B, sdesc_at(dSm, kk * 2048), sdesc_at(dKm, kk * 2048), idDQ,
-                   kk > 0 ? 1u : 0u);
-          mma_commit(bar(C_DQFULL));
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tbase + C::T_DK, sdesc_at(dSk, aoff), sdesc_at(dQm, kk * 2048), idKB,
+            mma_ts(tbase + C::T_DV, tbase + C::T_A + acol, sdesc_at(dOm, kk * 2048), idKB,
                    (t > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(bar(C_QEMPTY0 + st));
         }
         if (!ok) break;
-        mma_commit(bar(C_KVEMPTY));
-        mma_commit(bar(C_ACCFULL));
+        if (!issue_dk(it - 1, n == 1)) break;
+        mma_commit(bar(A_ACCFULL));
         ++un;
       }
-      mma_commit(bar(C_DRAIN));
-      mbar_wait(bar(C_DRAIN), 0, P.status, P.wait_ns);
+      mma_commit(bar(A_DRAIN));
+      mbar_wait(bar(A_DRAIN), 0, P.status, P.wait_ns);
     }
     __syncwarp();
-  }  // warp 15: spare warp of the producer warpgroup
-  } else if (warp >= DQ_WARP0) {
-    // ------------------------------------------------------------ dQ drain
-    // Thread r holds q row r of the tile in region B (TMEM lane r): all D
-    // columns in one TMEM round trip, region B released for the next dP^T.
-    // Straight from registers each fp32 atomic of a warp would touch 32
-    // different rows; instead the warp transposes 32 x 32 blocks through a
-    // 4 KB patch so that every reduction instruction covers four rows x 128
-    // contiguous bytes.  The patch lies in the dO buffer of this tile's Q/dO
-    // stage: the tile's MMAs have finished with it (they committed before
-    // the dQ tile), and the stage is refilled only after these warps arrive
-    // on its release barrier.  These warps do nothing else, so the
-    // reductions overlap the compute warps' P^T / dS^T work and the MMAs.
-    regs_increase<C::REGS_DQ>();
-    const int quarter = warp & 3;
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    uint32_t it = 0, cn = 0;
-    bool ok = true;
-    while (ok) {
-      const int idx = claimed_all(cn);
-      if (idx < 0) break;
-      int b, h, kj;
-      const int32_t* list;
-      const int n = unit_info(idx, b, h, kj, list);
-      float* acc_bh = P.dq_acc + (static_cast<size_t>(b) * P.H + h) * P.Sq * D;
-      for (int t = 0; t < n; ++t, ++it) {
-        const int qi = list[t] >> 2;
-        const int st = it & 1;
-        if (!wait_all(C_DQFULL, it & 1)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t raw[D];
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) tmem_ld64(tbase + lane_off + C::T_B + 64 * c, raw + 64 * c);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(C_DQEMPTY));
-        const uint32_t patch = sbase + C::OFF_DO + st * C::TILE + quarter * 4096;
-        const int row0 = qi * kTile + quarter * 32;  // first q row of this warp
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {  // 32-column blocks
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t chunk = static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7);
-            const int e = c * 32 + j * 4;
-            st_shared_v4(patch + lane * 128 + chunk * 16,
-                         __float_as_uint(__uint_as_float(raw[e]) * P.scale),
-                         __float_as_uint(__uint_as_float(raw[e + 1]) * P.scale),
-                         __float_as_uint(__uint_as_float(raw[e + 2]) * P.scale),
-                         __float_as_uint(__uint_as_float(raw[e + 3]) * P.scale));
-          }
-          __syncwarp();
-          const int j = lane & 7;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rl = i * 4 + (lane >> 3);  // row within the warp's 32
-            const uint32_t chunk = static_cast<uint32_t>(j) ^ static_cast<uint32_t>(rl & 7);
-            float4 v;
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                         : "r"(patch + rl * 128 + chunk * 16));
-            if (row0 + rl < P.Sq)
-              atomicAdd(reinterpret_cast<float4*>(acc_bh + static_cast<size_t>(row0 + rl) * D +
-                                                  c * 32 + j * 4),
-                        v);
-          }
-          __syncwarp();
-        }
-        // the stage may be refilled by TMA (async proxy) after these accesses
-        fence_proxy_async_smem();
-        mbar_arrive(bar(C_QEMPTY0 + st));
-      }
-    }
+  }  // warp 11: spare warp of the producer warpgroup
   } else {
     // ------------------------------------------------------------ compute warps
     regs_increase<C::REGS_COMPUTE>();
     const int quarter = warp & 3, half = warp >> 2;
-    const int r = quarter * 32 + lane;  // TMEM lane: key row (S^T, dP^T, dK, dV), q row (dQ)
+    const int r = quarter * 32 + lane;  // TMEM lane: key row of S^T, dP^T, dK, dV
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int c0 = half * 64;           // this thread's 64 of the 128 q columns
-    uint32_t it = 0, un = 0, cn = 0;
+    uint32_t it = 0, un = 0, cn = 0, ep = 0;  // ep: epilogues done
+    bool pending = false;                      // the previous unit's dK, dV wait in TMEM
+    int pb = 0, ph = 0, pkj = 0;               // the previous unit's batch, head, k-tile
+    // ---- epilogue of the previous unit: dV and scale * dK, this thread's
+    // half of the columns.  It runs after the next unit's first P^T, when
+    // the previous unit's last dK has long completed: its TMEM read (which
+    // lets the next dV start) then waits for nothing, and its stores overlap
+    // the next unit's MMAs.
+    auto epilogue = [&]() -> bool {
+      const int b = pb, h = ph, kj = pkj;
+      const int key = kj * kTile + r;
+      if (!wait_all(A_ACCFULL, ep & 1)) return false;
+      ++ep;
+      tc_fence_after();
+      uint32_t rv[D / 2], rk[D / 2];
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tmem_ld32(tbase + lane_off + C::T_DV + half * (D / 2) + c * 32, rv + 32 * c);
+        tmem_ld32(tbase + lane_off + C::T_DK + half * (D / 2) + c * 32, rk + 32 * c);
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive_warp(bar(A_ACCEMPTY));
+      if constexpr (D == 128) {
+        // Each thread holds 64 columns of its key row of dV and of dK.
+        // Stored straight from registers, every store instruction of a warp
+        // would touch 32 rows; instead each 32 x 64 bf16 block goes through
+        // this warp's 4 KB patch of the dS^T buffer (idle: the unit's MMAs
+        // are done, and these warps write the next dS^T only afterwards), so
+        // that an instruction stores four rows x 128 contiguous bytes.
+        const uint32_t patch = sDS + half * 16384 + quarter * 4096;
+        const int key0 = kj * kTile + quarter * 32;
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const float sc = m ? P.scale : 1.f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t* x = m ? rk + 8 * j : rv + 8 * j;
+            const uint32_t chunk = static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7);
+            st_shared_v4(patch + lane * 128 + chunk * 16,
+                         pack_bf16(__uint_as_float(x[0]) * sc, __uint_as_float(x[1]) * sc),
+                         pack_bf16(__uint_as_float(x[2]) * sc, __uint_as_float(x[3]) * sc),
+                         pack_bf16(__uint_as_float(x[4]) * sc, __uint_as_float(x[5]) * sc),
+                         pack_bf16(__uint_as_float(x[6]) * sc, __uint_as_float(x[7]) * sc));
+          }
+          __syncwarp();
+          __nv_bfloat16* base = m ? P.out0 : P.out1;
+          const int64_t* st3 = m ? P.s0 : P.s1;
+          const int jj = lane & 7;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rl = i * 4 + (lane >> 3);  // row within the warp's 32 keys
+            const uint32_t chunk = static_cast<uint32_t>(jj) ^ static_cast<uint32_t>(rl & 7);
+            uint4 val;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                         : "r"(patch + rl * 128 + chunk * 16));
+            const int kr = key0 + rl;
+            if (kr < P.Skv)
+              *reinterpret_cast<uint4*>(base + b * st3[0] + static_cast<int64_t>(kr) * st3[1] +
+                                        h * st3[2] + half * (D / 2) + jj * 8) = val;
+          }
+          __syncwarp();
+        }
+      } else if (key < P.Skv) {
+        const float sc = P.scale;
+        uint4* dv_dst = reinterpret_cast<uint4*>(P.out1 + b * P.s1[0] + static_cast<int64_t>(key) * P.s1[1] +
+                                                 h * P.s1[2] + half * (D / 2));
+        uint4* dk_dst = reinterpret_cast<uint4*>(P.out0 + b * P.s0[0] + static_cast<int64_t>(key) * P.s0[1] +
+                                                 h * P.s0[2] + half * (D / 2));
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) {
+          dv_dst[i] = make_uint4(pack_bf16(__uint_as_float(rv[8 * i + 0]), __uint_as_float(rv[8 * i + 1])),
+                                 pack_bf16(__uint_as_float(rv[8 * i + 2]), __uint_as_float(rv[8 * i + 3])),
+                                 pack_bf16(__uint_as_float(rv[8 * i + 4]), __uint_as_float(rv[8 * i + 5])),
+                                 pack_bf16(__uint_as_float(rv[8 * i + 6]), __uint_as_float(rv[8 * i + 7])));
+          dk_dst[i] = make_uint4(pack_bf16(__uint_as_float(rk[8 * i + 0]) * sc, __uint_as_float(rk[8 * i + 1]) * sc),
+                                 pack_bf16(__uint_as_float(rk[8 * i + 2]) * sc, __uint_as_float(rk[8 * i + 3]) * sc),
+                                 pack_bf16(__uint_as_float(rk[8 * i + 4]) * sc, __uint_as_float(rk[8 * i + 5]) * sc),
+                                 pack_bf16(__uint_as_float(rk[8 * i + 6]) * sc, __uint_as_float(rk[8 * i + 7]) * sc));
+        }
+      }
+      pending = false;
+      return true;
+    };
     bool ok = true;
     while (ok) {
       const int idx = claimed_all(cn);
@@ -595,10 +574,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const int32_t* list;
       const int n = unit_info(idx, b, h, kj, list);
       const int key = kj * kTile + r;
-      __nv_bfloat16* dk_row = P.dk + b * P.k_stride[0] + static_cast<int64_t>(key) * P.k_stride[1] +
-                              h * P.k_stride[2] + half * (D / 2);
-      __nv_bfloat16* dv_row = P.dv + b * P.v_stride[0] + static_cast<int64_t>(key) * P.v_stride[1] +
-                              h * P.v_stride[2] + half * (D / 2);
+      __nv_bfloat16* dk_row = P.out0 + b * P.s0[0] + static_cast<int64_t>(key) * P.s0[1] +
+                              h * P.s0[2] + half * (D / 2);
+      __nv_bfloat16* dv_row = P.out1 + b * P.s1[0] + static_cast<int64_t>(key) * P.s1[1] +
+                              h * P.s1[2] + half * (D / 2);
       if (n == 0) {
         if (key < P.Skv) {
           const uint4 z = make_uint4(0, 0, 0, 0);
@@ -628,9 +607,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LD + st * 1024) + c0;
         const float* del_s = lse_s + 128;
         // ---- P^T = exp2(S^T * scale*log2e - LSE*log2e), hidden entries 0
-        if (!wait_all(C_SFULL, it & 1)) { ok = false; break; }
+        if (!wait_all(A_SFULL, it & 1)) { ok = false; break; }
         // the LSE/D of this stage arrived with the Q/dO tiles
-        if (!wait_all(C_QFULL0 + st, (it >> 1) & 1)) { ok = false; break; }
+        if (!wait_all(A_QFULL0 + st, (it >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         float p[64];
         {
@@ -678,9 +657,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tc_fence_before();
         // (a test of the wait limit withholds the first P-ready arrival: the
         // MMA thread then gives up on it and the launch unwinds with DEV_TIMEOUT)
-        if (!(P.withhold == 2 && it == 0)) mbar_arrive(bar(C_PREADY));
+        if (!(P.withhold == 2 && it == 0)) mbar_arrive_warp(bar(A_PREADY));
+        if (t == 0 && pending && !epilogue()) { ok = false; break; }
         // ---- dS^T = P^T o (dP^T - D), to smem as bf16 [key][q] (slab = half)
-        if (!wait_all(C_DPFULL, it & 1)) { ok = false; break; }
+        if (!wait_all(A_DPFULL, it & 1)) { ok = false; break; }
         tc_fence_after();
         {
           uint32_t raw[64];
@@ -708,81 +688,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(bar(C_DSREADY));
+        mbar_arrive_warp(bar(A_DSREADY));
       }
       if (!ok) break;
-      // ---- epilogue: dV and scale * dK, this thread's half of the columns;
-      // both are read from TMEM first so the next unit's MMAs may start
-      if (!wait_all(C_ACCFULL, un & 1)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t rv[D / 2], rk[D / 2];
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        tmem_ld32(tbase + lane_off + C::T_DV + half * (D / 2) + c * 32, rv + 32 * c);
-        tmem_ld32(tbase + lane_off + C::T_DK + half * (D / 2) + c * 32, rk + 32 * c);
-      }
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(C_ACCEMPTY));
-      if constexpr (D == 128) {
-        // Each thread holds 64 columns of its key row of dV and of dK.
-        // Stored straight from registers, every store instruction of a warp
-        // would touch 32 rows; instead each 32 x 64 bf16 block goes through
-        // this warp's 4 KB patch of the dS^T buffer (idle: the unit's MMAs
-        // are done, and these warps write the next dS^T only afterwards), so
-        // that an instruction stores four rows x 128 contiguous bytes.
-        const uint32_t patch = sDS + half * 16384 + quarter * 4096;
-        const int key0 = kj * kTile + quarter * 32;
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          const float sc = m ? P.scale : 1.f;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t* x = m ? rk + 8 * j : rv + 8 * j;
-            const uint32_t chunk = static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7);
-            st_shared_v4(patch + lane * 128 + chunk * 16,
-                         pack_bf16(__uint_as_float(x[0]) * sc, __uint_as_float(x[1]) * sc),
-                         pack_bf16(__uint_as_float(x[2]) * sc, __uint_as_float(x[3]) * sc),
-                         pack_bf16(__uint_as_float(x[4]) * sc, __uint_as_float(x[5]) * sc),
-                         pack_bf16(__uint_as_float(x[6]) * sc, __uint_as_float(x[7]) * sc));
-          }
-          __syncwarp();
-          __nv_bfloat16* base = m ? P.dk : P.dv;
-          const int64_t* st3 = m ? P.k_stride : P.v_stride;
-          const int jj = lane & 7;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rl = i * 4 + (lane >> 3);  // row within the warp's 32 keys
-            const uint32_t chunk = static_cast<uint32_t>(jj) ^ static_cast<uint32_t>(rl & 7);
-            uint4 val;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                         : "r"(patch + rl * 128 + chunk * 16));
-            const int kr = key0 + rl;
-            if (kr < P.Skv)
-              *reinterpret_cast<uint4*>(base + b * st3[0] + static_cast<int64_t>(kr) * st3[1] +
-                                        h * st3[2] + half * (D / 2) + jj * 8) = val;
-          }
-          __syncwarp();
-        }
-      } else if (key < P.Skv) {
-        const float sc = P.scale;
-        uint4* dv_dst = reinterpret_cast<uint4*>(dv_row);
-        uint4* dk_dst = reinterpret_cast<uint4*>(dk_row);
-#pragma unroll
-        for (int i = 0; i < D / 16; ++i) {
-          dv_dst[i] = make_uint4(pack_bf16(__uint_as_float(rv[8 * i + 0]), __uint_as_float(rv[8 * i + 1])),
-                                 pack_bf16(__uint_as_float(rv[8 * i + 2]), __uint_as_float(rv[8 * i + 3])),
-                                 pack_bf16(__uint_as_float(rv[8 * i + 4]), __uint_as_float(rv[8 * i + 5])),
-                                 pack_bf16(__uint_as_float(rv[8 * i + 6]), __uint_as_float(rv[8 * i + 7])));
-          dk_dst[i] = make_uint4(pack_bf16(__uint_as_float(rk[8 * i + 0]) * sc, __uint_as_float(rk[8 * i + 1]) * sc),
-                                 pack_bf16(__uint_as_float(rk[8 * i + 2]) * sc, __uint_as_float(rk[8 * i + 3]) * sc),
-                                 pack_bf16(__uint_as_float(rk[8 * i + 4]) * sc, __uint_as_float(rk[8 * i + 5]) * sc),
-                                 pack_bf16(__uint_as_float(rk[8 * i + 6]) * sc, __uint_as_float(rk[8 * i + 7]) * sc));
-        }
-      }
+      pending = true;
+      pb = b;
+      ph = h;
+      pkj = kj;
       ++un;
     }
+    if (ok && pending) epilogue();
   }
 
   tc_fence_before();
@@ -793,14 +708,564 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   }
 }
 
+// ------------------------------------------------------------------ dQ kernel
+template <int D>
+struct DqCfg {
+  static constexpr int TILE = 128 * D * 2;   // one 128-row bf16 tile
+  static constexpr int KSTAGES = 3, VSTAGES = 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_DO = OFF_Q + TILE;
+  static constexpr int OFF_K = OFF_DO + TILE;              // KSTAGES stages
+  static constexpr int OFF_V = OFF_K + KSTAGES * TILE;     // VSTAGES stages
+  static constexpr int OFF_MSK = OFF_V + VSTAGES * TILE;   // one partial tile's 128 rows x 16 bytes
+  static constexpr int OFF_RING = OFF_MSK + kMaskBytes;
+  static constexpr int OFF_BAR = OFF_RING + 16;
+  static constexpr int NBAR = 34;
+  static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
+  static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+  // TMEM: S of even / odd tiles (then dS as packed bf16 over it), dP, dQ
+  static constexpr uint32_t T_S = 0, T_DP = 256, T_DQ = 384, T_COLS = 512;
+  // warpgroups 0-1: compute (P, dS, the dQ epilogue); warpgroup 2: the
+  // Q/dO/K/bits load warp, the MMA warp, the V load warp and one idle warp
+  static constexpr int THREADS = 384;
+  // register split (setmaxnreg): 2 x 128 x REGS_COMPUTE + 128 x REGS_PRODUCER
+  // = 64512 = THREADS x 168 registers at launch
+  static constexpr uint32_t REGS_COMPUTE = 216, REGS_PRODUCER = 72;
+  static constexpr int MIN_LAUNCH_REGS =
+      (2 * 128 * REGS_COMPUTE + 128 * REGS_PRODUCER + THREADS - 1) / THREADS;
+};
+
+enum { Q_QFULL = 0, Q_QEMPTY, Q_OFULL, Q_OEMPTY, Q_READY0, Q_KEMPTY0 = Q_READY0 + 3,
+       Q_VEMPTY0 = Q_KEMPTY0 + 3, Q_BFULL = Q_VEMPTY0 + 2, Q_BEMPTY, Q_SFULL0,
+       Q_DPFULL = Q_SFULL0 + 2, Q_DSREADY0, Q_DQFULL = Q_DSREADY0 + 2, Q_DQEMPTY, Q_DRAIN,
+       Q_UFULL0, Q_UEMPTY0 = Q_UFULL0 + 4 };
+// every slot of the unit ring is read by the MMA warp and the eight compute
+// warps
+constexpr int Q_READERS = 9;
+
+// One unit = q-tile qi of one (batch, head), walking its row of non-empty
+// k-tiles (g = the CTA's running tile count: TMEM S region g & 1, K stage
+// g mod 3, V stage g & 1).  MMA issue order, per tile t of the unit:
+//   S(t+1) = Q K^T -> S[(t+1) & 1]  [the region's previous dS was read by dQ(t-1)]
+//   dP(t+1) = dO V^T -> DP          [the compute warps have loaded dP(t)]
+//   dQ += dS(t) K(t)                 [dS(t) is in S[t & 1]]
+// so dS(t) has the time of S(t+1) and dP(t+1) to be ready.
+// The MMA thread checks two barriers per tile, READY(t+1) and DSREADY(t):
+// each check waits behind the MMAs it has issued, so every condition S(t+1)
+// and dP(t+1) need sits on the one READY barrier of tile t+1 (ring of three,
+// by g mod 3): the K and V copies of the tile (one expect-tx arrival of the
+// loader), and one arrival per compute warp once it has loaded dP(t) out of
+// the single dP region.  K(t) is read by S(t) and dQ(t), a period apart: the
+// loader fills tile t+1's K stage once dQ(t-2) is done and its V stage once
+// dP(t-1) is done.  The bits
+// of a partial tile have their own one-tile buffer, filled after the compute
+// warps have read the previous partial tile's bits.  dS readiness has one
+// barrier per S region: dP(t+1) is issued before the wait for dS(t), and a
+// region's barrier cannot run two phases ahead of that wait (dS(t+2) needs
+// S(t+2), issued only after dQ(t)).
+template <int D>
+__global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
+    bwd_dq_kernel(const __grid_constant__ BwdParams P, const __grid_constant__ CUtensorMap tmQ,
+                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmDO) {
+  using C = DqCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(P.status, DEV_LAYOUT);
+    return;
+  }
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  uint4* msk = reinterpret_cast<uint4*>(smem + C::OFF_MSK);  // [128 rows]
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + C::OFF_RING);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int LD_WARP = 8, MMA_WARP = 9;
+
+  if (tid == 0) {
+    // Q is read by the unit's S products only, dO by its dP products: each is
+    // free for the next unit as soon as its last reader is done
+    mbar_init(bar(Q_QFULL), 1);
+    mbar_init(bar(Q_QEMPTY), 1);
+    mbar_init(bar(Q_OFULL), 1);
+    mbar_init(bar(Q_OEMPTY), 1);
+    for (int s = 0; s < C::KSTAGES; ++s) {
+      mbar_init(bar(Q_READY0 + s), 1 + 8);  // the loader's expect-tx + 8 compute warps
+      mbar_init(bar(Q_KEMPTY0 + s), 1);
+    }
+    for (int s = 0; s < C::VSTAGES; ++s) mbar_init(bar(Q_VEMPTY0 + s), 1);
+    mbar_init(bar(Q_BFULL), 1);
+    mbar_init(bar(Q_BEMPTY), 8);  // one arrival per compute warp
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(Q_SFULL0 + s), 1);
+      mbar_init(bar(Q_DSREADY0 + s), 8);
+    }
+    mbar_init(bar(Q_DPFULL), 1);
+    mbar_init(bar(Q_DQFULL), 1);
+    mbar_init(bar(Q_DQEMPTY), 8);
+    mbar_init(bar(Q_DRAIN), 1);
+    for (int r = 0; r < UNIT_RING; ++r) {
+      mbar_init(bar(Q_UFULL0 + r), 1);
+      mbar_init(bar(Q_UEMPTY0 + r), Q_READERS);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(smem_u32(tmem_slot), C::T_COLS);
+    tmem_relinquish();
+  }
+  if (warp == LD_WARP && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmDO);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const int rows_pad = P.nQ * kTile;
+  const bool ragged = (P.Skv & (kTile - 1)) != 0;
+
+  auto wait = [&](int b, uint32_t parity) -> bool {
+    if (*abort_flag) return false;
+    if (!mbar_wait(bar(b), parity, P.status, P.wait_ns)) {
+      *abort_flag = 1;
+      return false;
+    }
+    return true;
+  };
+  auto wait_all = [&](int b, uint32_t parity) -> bool {
+    const bool ok = wait(b, parity);
+    return __all_sync(0xffffffffu, ok);
+  };
+  // unit u = (b*H + h)*nQ + qi -> its row of k-tiles
+  auto unit_info = [&](int idx, int& b, int& h, int& qi, int& row, const int32_t*& list) {
+    const int u = P.order[idx];
+    const int bh = u / P.nQ;
+    qi = u - bh * P.nQ;
+    b = bh / P.H;
+    h = bh - b * P.H;
+    row = (b * P.Hm + (P.Hm == 1 ? 0 : h)) * P.nQ + qi;
+    list = P.list + static_cast<size_t>(row) * P.nK;
+    return P.list_count[row];
+  };
+  auto claimed_one = [&](uint32_t& n) -> int {
+    int idx = -1;
+    const int r = n % UNIT_RING;
+    if (wait(Q_UFULL0 + r, (n / UNIT_RING) & 1)) {
+      idx = ring[r];
+      mbar_arrive(bar(Q_UEMPTY0 + r));
+    }
+    ++n;
+    return idx;
+  };
+  auto claimed_all = [&](uint32_t& n) -> int {
+    uint32_t m = n;
+    const int idx = lane == 0 ? claimed_one(m) : -1;
+    ++n;
+    return __shfl_sync(0xffffffffu, idx, 0);
+  };
+  // a tile is handled element by element when it is partial, or the ragged
+  // last k-tile
+  auto is_partial = [&](int ent) {
+    return (ent & 3) == CLS_PARTIAL || (ragged && (ent >> 2) == P.nK - 1);
+  };
+
+  if (warp >= LD_WARP) {
+  regs_decrease<C::REGS_PRODUCER>();
+  if (warp == LD_WARP) {
+    // ------------------------------------------------------------ Q / dO / K / bits loads
+    // Bits of a partial tile without a precomputed mask, built from the
+    // bounds: lane l holds columns l, l+32, l+64, l+96, so ballot x over the
+    // lanes is word x of a row; lane (r mod 32) keeps row r's words.
+    auto build_bits = [&](int bm, int kj, int qt, uint4* rows) {
+      const size_t base = static_cast<size_t>(bm) * P.Skv;
+      int4 v[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int j = kj * kTile + lane + 32 * x;
+        if (j < P.Skv) {
+          v[x].x = __ldg(P.bounds[0] + base + j);
+          v[x].y = __ldg(P.bounds[1] + base + j);
+          v[x].z = __ldg(P.bounds[2] + base + j);
+          v[x].w = __ldg(P.bounds[3] + base + j);
+        } else {
+          v[x] = make_int4(0, 0x7fffffff, 0, 0);  // beyond the keys: hidden from every row
+        }
+      }
+      for (int g = 0; g < 4; ++g) {
+        uint4 mine = make_uint4(0u, 0u, 0u, 0u);
+        for (int rr = 0; rr < 32; ++rr) {
+          const int qrow = qt * kTile + g * 32 + rr;
+          uint32_t w[4];
+#pragma unroll
+          for (int x = 0; x < 4; ++x)
+            w[x] = __ballot_sync(0xffffffffu, (v[x].x <= qrow && qrow < v[x].y) ||
+                                                  (v[x].z <= qrow && qrow < v[x].w));
+          if (lane == rr) mine = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        rows[g * 32 + lane] = mine;
+      }
+    };
+    // a q-tile row with no visible tile: its dQ rows are zero
+    auto finish_empty_row = [&](int b, int h, int qi) {
+      constexpr int WPR = D / 8;  // 16-byte words per dQ row
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      const int row0 = qi * kTile;
+      for (int i = lane; i < kTile * WPR; i += 32) {
+        const int row = row0 + i / WPR;
+        if (row < P.Sq)
+          reinterpret_cast<uint4*>(P.out0 + b * P.s0[0] + static_cast<int64_t>(row) * P.s0[1] +
+                                   h * P.s0[2])[i % WPR] = z;
+      }
+    };
+    uint32_t g = 0, un = 0, cn = 0, pc = 0;  // tiles, units, ring slots, partial tiles
+    uint32_t qn = 0, on = 0;                 // Q and dO loads issued (lane 0)
+    bool ok = true;
+    while (ok) {
+      // claim the next unit with tiles and publish it to the other roles;
+      // rows without tiles are finished here and never published
+      const int r = cn % UNIT_RING;
+      const uint32_t use = cn / UNIT_RING;
+      ++cn;
+      if (lane == 0 && use > 0 && !wait(Q_UEMPTY0 + r, (use - 1) & 1)) ok = false;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      int idx, b = 0, h = 0, qi = 0, row = 0, n = 0;
+      const int32_t* list = nullptr;
+      while (true) {
+        idx = -1;
+        if (lane == 0) {
+          idx = atomicAdd(P.next_unit, 1);
+          if (idx >= P.n_units) idx = -1;
+        }
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        if (idx < 0) break;
+        n = unit_info(idx, b, h, qi, row, list);
+        if (n > 0) break;
+        finish_empty_row(b, h, qi);
+      }
+      if (lane == 0) {
+        ring[r] = idx;
+        mbar_arrive(bar(Q_UFULL0 + r));
+      }
+      if (idx < 0) break;
+      if (lane == 0) {
+        if (un > 0 && !wait(Q_QEMPTY, (un - 1) & 1)) ok = false;
+        if (ok) {
+          mbar_arrive_expect_tx(bar(Q_QFULL), C::TILE);
+#pragma unroll
+          for (int x = 0; x < D / 64; ++x)
+            tma_load_4d(sbase + C::OFF_Q + x * 16384, &tmQ, bar(Q_QFULL), x * 64, h, qi * kTile, b);
+          ++qn;
+        }
+        if (ok && un > 0 && !wait(Q_OEMPTY, (un - 1) & 1)) ok = false;
+        if (ok) {
+          mbar_arrive_expect_tx(bar(Q_OFULL), C::TILE);
+#pragma unroll
+          for (int x = 0; x < D / 64; ++x)
+            tma_load_4d(sbase + C::OFF_DO + x * 16384, &tmDO, bar(Q_OFULL), x * 64, h, qi * kTile,
+                        b);
+          ++on;
+        }
+      }
+      ++un;
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const int mb = P.row_mask[row];
+      int mo = 0;  // partial tiles of the row so far
+      for (int t = 0; t < n; ++t, ++g) {
+        const int ent = list[t];
+        const int kj = ent >> 2;
+        const int ks = static_cast<int>(g % C::KSTAGES);
+        const uint32_t uk = g / C::KSTAGES;
+        const int vs = static_cast<int>(g & 1);
+        if (lane == 0) {
+          // K stage: dQ(g-3) done; V stage: dP(g-2) done (not implied by the
+          // former when tile g-2 opens a unit: its dP is issued after the
+          // previous unit's last dQ)
+          if (uk > 0 && !wait(Q_KEMPTY0 + ks, (uk - 1) & 1)) ok = false;
+          if (ok && g >= 2 && !wait(Q_VEMPTY0 + vs, ((g >> 1) - 1) & 1)) ok = false;
+          if (ok) {
+            const uint32_t rb = bar(Q_READY0 + ks);
+            mbar_arrive_expect_tx(rb, 2 * C::TILE);
+#pragma unroll
+            for (int x = 0; x < D / 64; ++x) {
+              tma_load_4d(sbase + C::OFF_K + ks * C::TILE + x * 16384, &tmK, rb, x * 64, h,
+                          kj * kTile, b);
+              tma_load_4d(sbase + C::OFF_V + vs * C::TILE + x * 16384, &tmV, rb, x * 64, h,
+                          kj * kTile, b);
+            }
+          }
+        }
+        if (!__all_sync(0xffffffffu, ok)) break;
+        if (is_partial(ent)) {
+          // the bits buffer, once the compute warps have read the previous
+          // partial tile's
+          if (pc > 0 && !wait_all(Q_BEMPTY, (pc - 1) & 1)) { ok = false; break; }
+          if (mb >= 0) {
+            if (lane == 0) {
+              mbar_arrive_expect_tx(bar(Q_BFULL), kMaskBytes);
+              bulk_load(smem_u32(msk), P.masks + static_cast<size_t>(mb + mo) * kMaskBytes,
+                        kMaskBytes, bar(Q_BFULL));
+            }
+          } else {
+            build_bits(row / P.nQ, kj, qi, msk);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(Q_BFULL));
+          }
+          ++mo;
+          ++pc;
+        }
+      }
+    }
+    // drain: every issued copy has landed before the CTA may exit (a tile's
+    // READY phase completes after its copies have)
+    if (lane == 0) {
+      const uint32_t back = g > static_cast<uint32_t>(C::KSTAGES) ? C::KSTAGES : g;
+      for (uint32_t x = g - back; x < g; ++x)
+        mbar_wait(bar(Q_READY0 + x % C::KSTAGES), (x / C::KSTAGES) & 1, P.status, P.wait_ns);
+      if (pc > 0) mbar_wait(bar(Q_BFULL), (pc - 1) & 1, P.status, P.wait_ns);
+      if (qn > 0) mbar_wait(bar(Q_QFULL), (qn - 1) & 1, P.status, P.wait_ns);
+      if (on > 0) mbar_wait(bar(Q_OFULL), (on - 1) & 1, P.status, P.wait_ns);
+    }
+    __syncwarp();
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S, dP
+      constexpr uint32_t idDQ = idesc_bf16(128, D, false, true);     // dQ (B = K MN-major)
+      const uint32_t dQ = sdesc_lo(sbase + C::OFF_Q, 16);
+      const uint32_t dO = sdesc_lo(sbase + C::OFF_DO, 16);
+      const uint32_t dK0 = sdesc_lo(sbase + C::OFF_K, 16);
+      const uint32_t dKm0 = sdesc_lo(sbase + C::OFF_K, 128 * 128);
+      const uint32_t dV0 = sdesc_lo(sbase + C::OFF_V, 16);
+      // S(gt) and then dP(gt): one READY check for both
+      auto issue_s = [&](uint32_t gt, bool last) -> bool {
+        const uint32_t ks = gt % C::KSTAGES;
+        if (!wait(Q_READY0 + ks, (gt / C::KSTAGES) & 1)) return false;
+        tc_fence_after();
+        const uint32_t dK = dK0 + ks * (C::TILE >> 4);
+        const int x = gt & 1;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tbase + C::T_S + 128 * x, sdesc_at(dQ, koff), sdesc_at(dK, koff), idSS,
+                 kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(Q_SFULL0 + x));
+        if (last) mma_commit(bar(Q_QEMPTY));  // the unit's last reader of Q
+        return true;
+      };
+      auto issue_dp = [&](uint32_t gt, bool last) -> bool {
+        const int st = gt & 1;
+        const uint32_t dV = dV0 + st * (C::TILE >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tbase + C::T_DP, sdesc_at(dO, koff), sdesc_at(dV, koff), idSS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(Q_DPFULL));
+        mma_commit(bar(Q_VEMPTY0 + st));  // V(gt) is read by this dP only
+        if (last) mma_commit(bar(Q_OEMPTY));  // the unit's last reader of dO
+        return true;
+      };
+      uint32_t g = 0, un = 0, cn = 0;
+      bool ok = true;
+      while (ok) {
+        const int idx = claimed_one(cn);
+        if (idx < 0) break;
+        int b, h, qi, row;
+        const int32_t* list;
+        const int n = unit_info(idx, b, h, qi, row, list);
+        if (!wait(Q_QFULL, un & 1) || !issue_s(g, n == 1)) break;
+        if (!wait(Q_OFULL, un & 1) || !issue_dp(g, n == 1)) break;
+        for (int t = 0; t < n; ++t) {
+          const uint32_t gt = g + t;
+          if (t + 1 < n && (!issue_s(gt + 1, t + 2 == n) || !issue_dp(gt + 1, t + 2 == n))) {
+            ok = false;
+            break;
+          }
+          if (!wait(Q_DSREADY0 + (gt & 1), (gt >> 1) & 1)) { ok = false; break; }
+          // the previous unit's dQ has been read by the epilogue
+          if (t == 0 && un > 0 && !wait(Q_DQEMPTY, (un - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t ks = gt % C::KSTAGES;
+          const uint32_t dKm = dKm0 + ks * (C::TILE >> 4);
+          const uint32_t tS = tbase + C::T_S + 128 * (gt & 1);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            // dS of keys 0..63 sits in TMEM columns [0,32), 64..127 in [64,96)
+            const uint32_t acol = (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+            mma_ts(tbase + C::T_DQ, tS + acol, sdesc_at(dKm, kk * 2048), idDQ,
+                   (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(Q_KEMPTY0 + ks));  // K(gt): read by S(gt) and this dQ
+        }
+        if (!ok) break;
+        g += n;
+        mma_commit(bar(Q_DQFULL));
+        ++un;
+      }
+      mma_commit(bar(Q_DRAIN));
+      mbar_wait(bar(Q_DRAIN), 0, P.status, P.wait_ns);
+    }
+    __syncwarp();
+  }
+  } else {
+    // ------------------------------------------------------------ compute warps
+    regs_increase<C::REGS_COMPUTE>();
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;  // TMEM lane: q row of S, dP, dQ
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int c0 = half * 64;           // this thread's 64 of the 128 key columns
+    uint32_t g = 0, un = 0, cn = 0, ep = 0, pc = 0;  // ep: epilogues done, pc: partial tiles
+    bool pending = false;                     // the previous unit's dQ waits in TMEM
+    int pb = 0, ph = 0, prow = 0;             // its batch, head and this thread's q row
+    // ---- epilogue of the previous unit: scale * dQ, this thread's half of
+    // the columns.  It runs after the next unit's first P, when the previous
+    // unit's last dQ has completed: its TMEM read then waits for nothing.
+    auto epilogue = [&]() -> bool {
+      if (!wait_all(Q_DQFULL, ep & 1)) return false;
+      ++ep;
+      tc_fence_after();
+      uint32_t rq[D / 2];
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tmem_ld32(tbase + lane_off + C::T_DQ + half * (D / 2) + c * 32, rq + 32 * c);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive_warp(bar(Q_DQEMPTY));
+      if (prow < P.Sq) {
+        uint4* dst = reinterpret_cast<uint4*>(P.out0 + pb * P.s0[0] +
+                                              static_cast<int64_t>(prow) * P.s0[1] + ph * P.s0[2] +
+                                              half * (D / 2));
+        const float sc = P.scale;
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i)
+          dst[i] = make_uint4(pack_bf16(__uint_as_float(rq[8 * i + 0]) * sc, __uint_as_float(rq[8 * i + 1]) * sc),
+                              pack_bf16(__uint_as_float(rq[8 * i + 2]) * sc, __uint_as_float(rq[8 * i + 3]) * sc),
+                              pack_bf16(__uint_as_float(rq[8 * i + 4]) * sc, __uint_as_float(rq[8 * i + 5]) * sc),
+                              pack_bf16(__uint_as_float(rq[8 * i + 6]) * sc, __uint_as_float(rq[8 * i + 7]) * sc));
+      }
+      pending = false;
+      return true;
+    };
+    bool ok = true;
+    mbar_arrive_warp(bar(Q_READY0));  // tile 0 has no previous dP to wait for
+    while (ok) {
+      const int idx = claimed_all(cn);
+      if (idx < 0) break;
+      int b, h, qi, row;
+      const int32_t* list;
+      const int n = unit_info(idx, b, h, qi, row, list);
+      const int qrow = qi * kTile + r;
+      const size_t bh_row = (static_cast<size_t>(b) * P.H + h) * rows_pad + qrow;
+      const float lse2 = P.lse_log2[bh_row];  // -LSE*log2(e), -inf past Sq / no key
+      const float drow = P.delta[bh_row];
+      const uint64_t sc2 = splat2(P.scale_log2), l2 = splat2(lse2);
+      for (int t = 0; t < n; ++t) {
+        const uint32_t gt = g + t;
+        const int ent = list[t];
+        const bool partial = is_partial(ent);
+        const int x = gt & 1;
+        const uint32_t tS = tbase + lane_off + C::T_S + 128 * x;
+        // ---- P = exp2(S * scale*log2e - LSE*log2e), hidden entries 0
+        if (!wait_all(Q_SFULL0 + x, (gt >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        float p[64];
+        {
+          uint32_t raw[64];
+          tmem_ld64(tS + c0, raw);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float a0, a1;
+            fma2_bc(a0, a1, __uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]), sc2, l2);
+            p[2 * i] = ex2(a0);
+            p[2 * i + 1] = ex2(a1);
+          }
+        }
+        if (partial) {
+          // this row's 64 column bits of the tile (set = hidden)
+          if (!wait_all(Q_BFULL, pc & 1)) { ok = false; break; }
+          ++pc;
+          const uint4 mw = msk[r];
+          const uint32_t m0 = half ? mw.z : mw.x, m1 = half ? mw.w : mw.y;
+          mbar_arrive_warp(bar(Q_BEMPTY));
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            p[c] = ((m0 >> c) & 1u) ? 0.f : p[c];
+            p[c + 32] = ((m1 >> c) & 1u) ? 0.f : p[c + 32];
+          }
+        }
+        if (t == 0 && pending && !epilogue()) { ok = false; break; }
+        // ---- dS = P o (dP - D), packed bf16 over this thread's S columns
+        if (!wait_all(Q_DPFULL, gt & 1)) { ok = false; break; }
+        tc_fence_after();
+        {
+          uint32_t raw[64];
+          tmem_ld64(tbase + lane_off + C::T_DP + c0, raw);
+          tmem_wait_ld();
+          // dP is in registers: the next dP may overwrite the region
+          tc_fence_before();
+          mbar_arrive_warp(bar(Q_READY0 + (gt + 1) % C::KSTAGES));
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            float s0, s1;
+            mulsub2(s0, s1, p[2 * c], p[2 * c + 1], __uint_as_float(raw[2 * c]),
+                    __uint_as_float(raw[2 * c + 1]), drow, drow);
+            pk[c] = pack_bf16(s0, s1);
+          }
+          // keys c0 .. c0+63 packed two per column into the first half of
+          // the columns this thread read, [c0, c0 + 32): the other half of
+          // the warps may still be reading S from theirs
+          tmem_st32(tS + c0, pk);
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive_warp(bar(Q_DSREADY0 + x));
+      }
+      if (!ok) break;
+      g += n;
+      pending = true;
+      pb = b;
+      ph = h;
+      prow = qrow;
+      ++un;
+    }
+    if (ok && pending) epilogue();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::T_COLS);
+  }
+}
+
+template <typename Kern>
+static fm_status prepare(Kern kern, int smem, int min_regs) {
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return FM_ERR_CUDA;
+  // the setmaxnreg split must fit in the registers the block launches with
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return FM_ERR_CUDA;
+  if (fa.numRegs < min_regs) return FM_ERR_UNSUPPORTED;
+  return FM_OK;
+}
+
 template <int D>
 static fm_status launch_bwd_d(const Plan& p, const fm_desc& desc, const TensorArgs& t, char* ws,
                               cudaStream_t s) {
-  using C = BwdCfg<D>;
   const int rows_pad = p.nQ * kTile;
   float* delta = reinterpret_cast<float*>(ws + p.L.delta);
   float* lse2 = reinterpret_cast<float*>(ws + p.L.lse_log2);
-  float* acc = reinterpret_cast<float*>(ws + p.L.dq_acc);
   {
     // four warps per block, one warp per 16 rows (rows_pad is a multiple of 128)
     const long long rows = static_cast<long long>(p.B) * p.H * rows_pad;
@@ -809,7 +1274,7 @@ static fm_status launch_bwd_d(const Plan& p, const fm_desc& desc, const TensorAr
     bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 128, 0, s>>>(
         static_cast<const __nv_bfloat16*>(t.o), static_cast<const __nv_bfloat16*>(t.dout),
         desc.o_stride[0], desc.o_stride[1], desc.o_stride[2], t.lse_in, p.B, p.H, p.Sq, rows_pad,
-        delta, lse2, acc);
+        delta, lse2);
     prof_end(K_BWD_PRE, s);
     if (cudaGetLastError() != cudaSuccess) return FM_ERR_CUDA;
   }
@@ -819,53 +1284,61 @@ static fm_status launch_bwd_d(const Plan& p, const fm_desc& desc, const TensorAr
       !make_tmap_bshd(&tv, t.v, p.B, p.Skv, p.H, D, desc.v_stride, 128) ||
       !make_tmap_bshd(&tdo, t.dout, p.B, p.Sq, p.H, D, desc.o_stride, 128))
     return FM_ERR_CUDA;
+  const TestHooks th = test_hooks();
   BwdParams P{};
   P.B = p.B; P.H = p.H; P.Hm = p.Hm; P.Sq = p.Sq; P.Skv = p.Skv; P.nQ = p.nQ; P.nK = p.nK;
-  P.n_units = p.B * p.H * p.nK;
   P.scale = t.scale;
   P.scale_log2 = t.scale * 1.4426950408889634f;
   for (int i = 0; i < 4; ++i) P.bounds[i] = t.bounds[i];
-  P.col_count = reinterpret_cast<const int32_t*>(ws + p.L.col_count);
-  P.col_list = reinterpret_cast<const int32_t*>(ws + p.L.col_list);
-  P.order = reinterpret_cast<const int32_t*>(ws + p.L.bwd_order);
-  P.next_unit = reinterpret_cast<int*>(ws + p.L.status) + 1;
   P.delta = delta;
   P.lse_log2 = lse2;
-  P.dq_acc = acc;
-  P.dk = static_cast<__nv_bfloat16*>(t.dk);
-  P.dv = static_cast<__nv_bfloat16*>(t.dv);
-  for (int i = 0; i < 3; ++i) {
-    P.k_stride[i] = desc.k_stride[i];
-    P.v_stride[i] = desc.v_stride[i];
-  }
   P.status = reinterpret_cast<int*>(ws + p.L.status);
-  const TestHooks th = test_hooks();
   P.wait_ns = th.wait_ns;
-  P.withhold = th.withhold;
-  auto kern = bwd_kernel<D>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-      cudaSuccess)
-    return FM_ERR_CUDA;
+  fm_status st;
   {
-    // the setmaxnreg split must fit in the registers the block launches with
-    cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return FM_ERR_CUDA;
-    if (fa.numRegs < C::MIN_LAUNCH_REGS) return FM_ERR_UNSUPPORTED;
+    // dK, dV over k-tile columns
+    BwdParams A = P;
+    A.n_units = p.B * p.H * p.nK;
+    A.list_count = reinterpret_cast<const int32_t*>(ws + p.L.col_count);
+    A.list = reinterpret_cast<const int32_t*>(ws + p.L.col_list);
+    A.order = reinterpret_cast<const int32_t*>(ws + p.L.bwd_order);
+    A.next_unit = reinterpret_cast<int*>(ws + p.L.status) + 1;
+    A.out0 = static_cast<__nv_bfloat16*>(t.dk);
+    A.out1 = static_cast<__nv_bfloat16*>(t.dv);
+    for (int i = 0; i < 3; ++i) {
+      A.s0[i] = desc.k_stride[i];
+      A.s1[i] = desc.v_stride[i];
+    }
+    A.withhold = th.withhold;
+    using C = KvCfg<D>;
+    auto kern = bwd_kv_kernel<D>;
+    if ((st = prepare(kern, C::SMEM, C::MIN_LAUNCH_REGS)) != FM_OK) return st;
+    const int grid = A.n_units < num_sms() ? A.n_units : num_sms();
+    prof_begin(K_BWD, s);
+    kern<<<grid, C::THREADS, C::SMEM, s>>>(A, tq, tk, tv, tdo);
+    prof_end(K_BWD, s);
+    if (cudaGetLastError() != cudaSuccess) return FM_ERR_CUDA;
   }
-  const int grid = P.n_units < num_sms() ? P.n_units : num_sms();
-  prof_begin(K_BWD, s);
-  kern<<<grid, C::THREADS, C::SMEM, s>>>(P, tq, tk, tv, tdo);
-  prof_end(K_BWD, s);
-  if (cudaGetLastError() != cudaSuccess) return FM_ERR_CUDA;
   {
-    const long long n_vec = static_cast<long long>(p.B) * p.H * p.Sq * (D / 8);
-    const long long want = (n_vec + 255) / 256;
-    const int blocks = static_cast<int>(want < 8192 ? want : 8192);
-    prof_begin(K_DQ_CONVERT, s);
-    dq_convert_kernel<D><<<blocks, 256, 0, s>>>(acc, static_cast<__nv_bfloat16*>(t.dq),
-                                                desc.q_stride[0], desc.q_stride[1],
-                                                desc.q_stride[2], p.H, p.Sq, n_vec);
-    prof_end(K_DQ_CONVERT, s);
+    // dQ over q-tile rows
+    BwdParams Q = P;
+    Q.n_units = p.B * p.H * p.nQ;
+    Q.list_count = reinterpret_cast<const int32_t*>(ws + p.L.row_count);
+    Q.list = reinterpret_cast<const int32_t*>(ws + p.L.row_list);
+    Q.order = reinterpret_cast<const int32_t*>(ws + p.L.row_order);
+    Q.next_unit = reinterpret_cast<int*>(ws + p.L.status) + 4;
+    Q.row_mask = reinterpret_cast<const int32_t*>(ws + p.L.row_mask);
+    Q.masks = reinterpret_cast<const uint8_t*>(ws + p.L.masks);
+    Q.out0 = static_cast<__nv_bfloat16*>(t.dq);
+    for (int i = 0; i < 3; ++i) Q.s0[i] = desc.q_stride[i];
+    Q.withhold = 0;
+    using C = DqCfg<D>;
+    auto kern = bwd_dq_kernel<D>;
+    if ((st = prepare(kern, C::SMEM, C::MIN_LAUNCH_REGS)) != FM_OK) return st;
+    const int grid = Q.n_units < num_sms() ? Q.n_units : num_sms();
+    prof_begin(K_BWD_DQ, s);
+    kern<<<grid, C::THREADS, C::SMEM, s>>>(Q, tq, tk, tv, tdo);
+    prof_end(K_BWD_DQ, s);
     if (cudaGetLastError() != cudaSuccess) return FM_ERR_CUDA;
   }
   return FM_OK;

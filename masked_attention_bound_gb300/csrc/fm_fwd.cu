@@ -170,18 +170,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       mbar_init(bar(B_QFULL0 + s), 1);
       mbar_init(bar(B_QEMPTY0 + s), 1);
       mbar_init(bar(B_SFULL0 + s), 1);
-      mbar_init(bar(B_PFULL0 + s), 128);
+      mbar_init(bar(B_PFULL0 + s), 4);  // one arrival per softmax warp of the slot
       mbar_init(bar(B_PVDONE0 + s), 1);
-      mbar_init(bar(B_OEMPTY0 + s), 128);
+      mbar_init(bar(B_OEMPTY0 + s), 4);
       mbar_init(bar(B_KFULL0 + s), 1);
       mbar_init(bar(B_VFULL0 + s), 1);
       // stage s of K, V (and the bits) is free again once both MMA threads
       // are past its PV: one commit per MMA thread per entry
       mbar_init(bar(B_KVEMPTY0 + s), 2);
-      // per stage: 128 arrivals for each slot, from its softmax threads when
-      // the slot's tile there is partial (they read the bits), else from the
-      // load warp on the slot's behalf
-      mbar_init(bar(B_MEMPTY0 + s), 256);
+      // per stage: 4 arrivals for each slot, from its softmax warps when the
+      // slot's tile there is partial (they read the bits), else from the load
+      // warp on the slot's behalf
+      mbar_init(bar(B_MEMPTY0 + s), 8);
     }
     mbar_init(bar(B_DRAIN), 2);
     for (int r = 0; r < UNIT_RING; ++r) {
@@ -392,8 +392,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             tma_load_4d(sbase + C::OFF_K + st * C::TILE + x * 16384, &tmK, bar(B_KFULL0 + st),
                         x * 64, u.h, kj * kTile, u.b);
           // a slot whose tile here is not partial never reads this stage's bits
-          if (ca != CLS_PARTIAL) mbar_arrive_count(bar(B_MEMPTY0 + st), 128);
-          if (cb != CLS_PARTIAL) mbar_arrive_count(bar(B_MEMPTY0 + st), 128);
+          if (ca != CLS_PARTIAL) mbar_arrive_count(bar(B_MEMPTY0 + st), 4);
+          if (cb != CLS_PARTIAL) mbar_arrive_count(bar(B_MEMPTY0 + st), 4);
         }
       }
     }
@@ -617,7 +617,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             sv[c + 64] = ((mw.z >> c) & 1u) ? -INFINITY : sv[c + 64];
             sv[c + 96] = ((mw.w >> c) & 1u) ? -INFINITY : sv[c + 96];
           }
-          mbar_arrive(bar(B_MEMPTY0 + st));  // done with this stage's bits
+          mbar_arrive_warp(bar(B_MEMPTY0 + st));  // done with this stage's bits
         }
         // row maximum: eight independent chains of three-input max
         float mx8[8];
@@ -681,7 +681,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         // (a test of the wait limit withholds the first P-ready arrival of
         // slot a: the slot's MMA thread then gives up on it and the launch
         // unwinds with DEV_TIMEOUT)
-        if (!(P.withhold == 1 && slot == 0 && j == 0)) mbar_arrive(bar(B_PFULL0 + slot));
+        if (!(P.withhold == 1 && slot == 0 && j == 0)) mbar_arrive_warp(bar(B_PFULL0 + slot));
         ++j;
         ++done;
       }
@@ -697,7 +697,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + c * 32, ro + 32 * c);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(bar(B_OEMPTY0 + slot));
+      mbar_arrive_warp(bar(B_OEMPTY0 + slot));
       if (qrow < P.Sq) {
         uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll

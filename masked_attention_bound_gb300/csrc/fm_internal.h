@@ -34,7 +34,10 @@ fm_status make_plan(const fm_desc* desc, int for_bwd, Plan* p, size_t limit = SI
 cudaError_t launch_summary(const Plan& p, const int32_t* lts, const int32_t* lte,
                            const int32_t* uts, const int32_t* ute, char* ws, cudaStream_t s);
 cudaError_t launch_classify(const Plan& p, char* ws, int for_bwd, cudaStream_t s);
-cudaError_t launch_order(const Plan& p, char* ws, int for_bwd, cudaStream_t s);
+// unit orders: ORDER_PAIRS (forward, q-tile pairs), ORDER_COLS (dK/dV, k-tile
+// columns), ORDER_ROWS (dQ, q-tile rows)
+enum : int { ORDER_PAIRS = 0, ORDER_COLS, ORDER_ROWS };
+cudaError_t launch_order(const Plan& p, char* ws, int which, cudaStream_t s);
 cudaError_t launch_tile_masks(const Plan& p, const int32_t* lts, const int32_t* lte,
                               const int32_t* uts, const int32_t* ute, char* ws, cudaStream_t s);
 
@@ -72,7 +75,7 @@ TestHooks test_hooks();
 
 // Kernel ids for the timing hooks (fm_profile_*).
 enum KernelId : int { K_SUMMARY = 0, K_CLASSIFY, K_ORDER, K_LOCALIZE, K_FWD, K_BWD_PRE, K_BWD,
-                      K_DQ_CONVERT, K_TILE_MASKS, K_COUNT };
+                      K_BWD_DQ, K_TILE_MASKS, K_COUNT };
 void prof_begin(int id, cudaStream_t s);
 void prof_end(int id, cudaStream_t s);
 

@@ -399,14 +399,13 @@ cudaError_t launch_classify(const Plan& p, char* ws, int for_bwd, cudaStream_t s
   const int32_t* summ = reinterpret_cast<const int32_t*>(ws + p.L.summary);
   uint8_t* table = reinterpret_cast<uint8_t*>(ws + p.L.table);
   prof_begin(K_CLASSIFY, s);
+  // q-tile rows (with their mask slots): the forward's pairs are built from
+  // them, and the dQ pass walks them
+  classify_rows_kernel<<<ceil_div(nBH * p.nQ, 8), 256, 0, s>>>(
+      summ, nBH, p.nQ, p.nK, p.Sq, p.Skv, table, reinterpret_cast<int32_t*>(ws + p.L.row_count),
+      reinterpret_cast<int32_t*>(ws + p.L.row_list), reinterpret_cast<int32_t*>(ws + p.L.row_mask),
+      reinterpret_cast<unsigned long long*>(ws + p.L.status + 8), p.mask_cap);
   if (!for_bwd) {
-    const int warps = nBH * p.nQ;
-    classify_rows_kernel<<<ceil_div(warps, 8), 256, 0, s>>>(
-        summ, nBH, p.nQ, p.nK, p.Sq, p.Skv, table,
-        reinterpret_cast<int32_t*>(ws + p.L.row_count),
-        reinterpret_cast<int32_t*>(ws + p.L.row_list),
-        reinterpret_cast<int32_t*>(ws + p.L.row_mask),
-        reinterpret_cast<unsigned long long*>(ws + p.L.status + 8), p.mask_cap);
     const int pwarps = nBH * p.nP;
     classify_pairs_kernel<<<ceil_div(pwarps, 8), 256, 0, s>>>(
         table, nBH, p.nQ, p.nK, p.nP, p.Skv, reinterpret_cast<int4*>(ws + p.L.pair_info),
@@ -432,15 +431,26 @@ cudaError_t launch_tile_masks(const Plan& p, const int32_t* lts, const int32_t* 
   return cudaGetLastError();
 }
 
-cudaError_t launch_order(const Plan& p, char* ws, int for_bwd, cudaStream_t s) {
-  // backward: k-tile columns, cost = their non-empty tiles; forward: q-tile
-  // pairs, cost = the non-empty tiles of both rows (pair_info[.][3])
-  const int nT = for_bwd ? p.nK : p.nP;          // units per (b, h)
-  const int maxc = for_bwd ? p.nQ : 2 * p.nK;    // largest possible cost
-  const int stride = for_bwd ? 1 : 4;
-  const int32_t* counts = for_bwd ? reinterpret_cast<const int32_t*>(ws + p.L.col_count)
-                                  : reinterpret_cast<const int32_t*>(ws + p.L.pair_info) + 3;
-  int32_t* order = reinterpret_cast<int32_t*>(ws + (for_bwd ? p.L.bwd_order : p.L.fwd_order));
+cudaError_t launch_order(const Plan& p, char* ws, int which, cudaStream_t s) {
+  // forward: q-tile pairs, cost = the non-empty tiles of both rows
+  // (pair_info[.][3]); dK/dV: k-tile columns, dQ: q-tile rows, cost = their
+  // non-empty tiles
+  int nT, maxc, stride = 1;
+  const int32_t* counts;
+  int32_t* order;
+  if (which == ORDER_PAIRS) {
+    nT = p.nP; maxc = 2 * p.nK; stride = 4;
+    counts = reinterpret_cast<const int32_t*>(ws + p.L.pair_info) + 3;
+    order = reinterpret_cast<int32_t*>(ws + p.L.fwd_order);
+  } else if (which == ORDER_COLS) {
+    nT = p.nK; maxc = p.nQ;
+    counts = reinterpret_cast<const int32_t*>(ws + p.L.col_count);
+    order = reinterpret_cast<int32_t*>(ws + p.L.bwd_order);
+  } else {
+    nT = p.nQ; maxc = p.nK;
+    counts = reinterpret_cast<const int32_t*>(ws + p.L.row_count);
+    order = reinterpret_cast<int32_t*>(ws + p.L.row_order);
+  }
   const size_t smem = static_cast<size_t>(maxc + 1 + nT) * 4;
   const size_t limit = 200 * 1024;
   if (smem > limit) return cudaErrorInvalidValue;

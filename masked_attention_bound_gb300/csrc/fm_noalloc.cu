@@ -61,11 +61,11 @@ extern "C" fm_status fm_fwd_static(const fm_desc* desc, const void* q, const voi
   char* ws = nullptr;
   if ((st = scratch_for_current_device(&ws)) != FM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws + p.L.status, 0, 16, s) != cudaSuccess) return FM_ERR_CUDA;
+  if (cudaMemsetAsync(ws + p.L.status, 0, 32, s) != cudaSuccess) return FM_ERR_CUDA;
   if (launch_summary(p, lts, lte, uts, ute, ws, s) != cudaSuccess) return FM_ERR_CUDA;
   if (launch_classify(p, ws, 0, s) != cudaSuccess) return FM_ERR_CUDA;
   if (launch_tile_masks(p, lts, lte, uts, ute, ws, s) != cudaSuccess) return FM_ERR_CUDA;
-  if (launch_order(p, ws, 0, s) != cudaSuccess) return FM_ERR_CUDA;
+  if (launch_order(p, ws, ORDER_PAIRS, s) != cudaSuccess) return FM_ERR_CUDA;
   TensorArgs t{};
   t.q = q; t.k = k; t.v = v; t.o_out = o; t.lse_out = lse;
   t.bounds[0] = lts; t.bounds[1] = lte; t.bounds[2] = uts; t.bounds[3] = ute;

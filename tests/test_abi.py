@@ -54,8 +54,8 @@ def test_workspace_size_and_layout(L):
     offs = [getattr(lay, f) for f, _ in _abi.FmWsLayout._fields_]
     assert all(o % 256 == 0 for o in offs)
     assert lay.total == n1
-    # dq_acc holds B*H*Sq*d floats
-    assert lay.total - lay.dq_acc >= 1 * 2 * 256 * 64 * 4
+    # the dQ pass's unit order holds B*H*nQ entries before the bit-mask region
+    assert lay.masks - lay.row_order >= 1 * 2 * 2 * 4
 
 
 @pytest.mark.parametrize("field,value,code", [

@@ -21,7 +21,8 @@ KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "
 def _report(world=1, ms=2.0, e2e_ms=7.0):
     args = types.SimpleNamespace(steps=10, warmup=3, no_e2e=False, no_cpu_baseline=True)
     W = dict(bench.WORKLOAD)
-    prof = {"fwd_kernel": (6.0, 10), "bwd_kernel": (13.0, 10), "bwd_pre_kernel": (1.7, 10)}
+    prof = {"fwd_kernel": (6.0, 10), "bwd_kv_kernel": (8.0, 10), "bwd_dq_kernel": (5.0, 10),
+            "bwd_pre_kernel": (1.7, 10)}
     buf = io.StringIO()
     with contextlib.redirect_stdout(buf):
         bench.report(args, W, world, 0, ms, prof, 3.0e11, 7.5e11, 123456, e2e_ms, 1000, 2000,
@@ -37,13 +38,15 @@ def test_device_arm_line():
     assert d["higher_is_better"] is True and d["scaling"] == "weak" and d["n_gpus"] == 1
     r = d["roofline"]
     assert {"bound", "achieved", "peak", "unit", "frac", "traffic"} <= r.keys()
-    assert r["kernel"] == "bwd_kernel"          # the larger share of device time
-    assert r["achieved"] == pytest.approx(7.5e11 / 1.3e-3 / 1e12, rel=1e-3)
+    assert r["kernel"] == "bwd_kv_kernel"       # the largest share of device time
+    # its own work: four GEMMs of 2 * d flop per visible entry, d * entries = 3e11 / 4
+    assert r["achieved"] == pytest.approx(8 * 3.0e11 / 4 / 0.8e-3 / 1e12, rel=1e-3)
+    assert d["bwd_tflops"] == pytest.approx(7.5e11 / 1.3e-3 / 1e12, rel=1e-3)
     assert r["frac"] == pytest.approx(r["achieved"] / r["peak"], rel=1e-3)
     e = d["e2e"]
     assert e["value"] == pytest.approx(1.05e12 / 7e-3 / 1e12, rel=1e-3)
     assert e["h2d_bytes_per_step"] == 1000 and e["d2h_bytes_per_step"] == 2000
-    assert d["gpu_launches"] == 30
+    assert d["gpu_launches"] == 40
     assert d["config"] == bench._config(bench.WORKLOAD, 123456, 1)
 
 

@@ -1,9 +1,9 @@
 """Mask-analysis kernels against the oracle, bit for bit (GPU).
 
 Block summary + tile classification + work lists (per q-tile row, per
-q-tile pair, per k-tile column) + longest-first order + the partial tiles'
-visibility bit masks (fm_plan), bound validation, and localisation
-(fm_localize).
+q-tile pair, per k-tile column) + longest-first orders (forward pairs, dK/dV
+columns, dQ rows) + the partial tiles' visibility bit masks (fm_plan), bound
+validation, and localisation (fm_localize).
 """
 import numpy as np
 import pytest
@@ -89,13 +89,16 @@ def _check_plan(bounds, Sq, H=2, d=64):
         assert fm.device_status(ws) == 0
         table = _ws_view(ws, L.table, B * Hm * nQ * nK, torch.uint8).view(B, Hm, nQ, nK).cpu().numpy()
         assert np.array_equal(table, ref_table)
+        # q-tile rows and their partial tiles' bit masks: the forward builds
+        # its pairs from them, the backward's dQ pass walks them
+        cnt = _ws_view(ws, L.row_count, B * Hm * nQ, torch.int32).view(B, Hm, nQ).cpu().numpy()
+        lst = _ws_view(ws, L.row_list, B * Hm * nQ * nK, torch.int32).view(B, Hm, nQ, nK).cpu().numpy()
+        assert np.array_equal(cnt, ref_rc)
+        for (b, hm, qi), ent in ref_rl.items():
+            want = [(kj << 2) | c for kj, c in ent]
+            assert lst[b, hm, qi, :len(want)].tolist() == want
+        _check_tile_masks(ws, L, bounds, Sq, ref_rl)
         if not for_bwd:
-            cnt = _ws_view(ws, L.row_count, B * Hm * nQ, torch.int32).view(B, Hm, nQ).cpu().numpy()
-            lst = _ws_view(ws, L.row_list, B * Hm * nQ * nK, torch.int32).view(B, Hm, nQ, nK).cpu().numpy()
-            assert np.array_equal(cnt, ref_rc)
-            for (b, hm, qi), ent in ref_rl.items():
-                want = [(kj << 2) | c for kj, c in ent]
-                assert lst[b, hm, qi, :len(want)].tolist() == want
             nP = (nQ + 1) // 2
             ref_pc, ref_cost, ref_pl = om.pair_lists(ref_table, Skv)
             info = _ws_view(ws, L.pair_info, B * Hm * nP * 4, torch.int32).view(B, Hm, nP, 4).cpu().numpy()
@@ -109,7 +112,6 @@ def _check_plan(bounds, Sq, H=2, d=64):
                 assert info[b, hm, p, 2] == sum(cb != 0 for _, _, cb in ent)
             order = _ws_view(ws, L.fwd_order, B * H * nP, torch.int32).cpu().numpy()
             assert np.array_equal(order, om.unit_order(ref_cost, H))
-            _check_tile_masks(ws, L, bounds, Sq, ref_rl)
         else:
             cnt = _ws_view(ws, L.col_count, B * Hm * nK, torch.int32).view(B, Hm, nK).cpu().numpy()
             lst = _ws_view(ws, L.col_list, B * Hm * nK * nQ, torch.int32).view(B, Hm, nK, nQ).cpu().numpy()
@@ -119,6 +121,8 @@ def _check_plan(bounds, Sq, H=2, d=64):
                 assert lst[b, hm, kj, :len(want)].tolist() == want
             order = _ws_view(ws, L.bwd_order, B * H * nK, torch.int32).cpu().numpy()
             assert np.array_equal(order, om.unit_order(ref_cc, H))
+            order = _ws_view(ws, L.row_order, B * H * nQ, torch.int32).cpu().numpy()
+            assert np.array_equal(order, om.unit_order(ref_rc, H))
 
 
 def test_plan_tiny():
