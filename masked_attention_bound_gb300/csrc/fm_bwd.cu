@@ -737,11 +737,11 @@ struct DqCfg {
 
 enum { Q_QFULL = 0, Q_QEMPTY, Q_OFULL, Q_OEMPTY, Q_READY0, Q_KEMPTY0 = Q_READY0 + 3,
        Q_VEMPTY0 = Q_KEMPTY0 + 3, Q_BFULL = Q_VEMPTY0 + 2, Q_BEMPTY, Q_SFULL0,
-       Q_DPFULL = Q_SFULL0 + 2, Q_DSREADY0, Q_DQFULL = Q_DSREADY0 + 2, Q_DQEMPTY, Q_DRAIN,
-       Q_UFULL0, Q_UEMPTY0 = Q_UFULL0 + 4 };
-// every slot of the unit ring is read by the MMA warp and the eight compute
-// warps
-constexpr int Q_READERS = 9;
+       Q_DPFULL = Q_SFULL0 + 2, Q_DPFREE, Q_DSREADY0, Q_DQFULL = Q_DSREADY0 + 2, Q_DQEMPTY, Q_DRAIN_A,
+       Q_DRAIN_B, Q_UFULL0, Q_UEMPTY0 = Q_UFULL0 + 4 };
+// every slot of the unit ring is read by the two MMA warps and the eight
+// compute warps
+constexpr int Q_READERS = 10;
 
 // One unit = q-tile qi of one (batch, head), walking its row of non-empty
 // k-tiles (g = the CTA's running tile count: TMEM S region g & 1, K stage
@@ -750,12 +750,16 @@ constexpr int Q_READERS = 9;
 //   dP(t+1) = dO V^T -> DP          [the compute warps have loaded dP(t)]
 //   dQ += dS(t) K(t)                 [dS(t) is in S[t & 1]]
 // so dS(t) has the time of S(t+1) and dP(t+1) to be ready.
-// The MMA thread checks two barriers per tile, READY(t+1) and DSREADY(t):
-// each check waits behind the MMAs it has issued, so every condition S(t+1)
-// and dP(t+1) need sits on the one READY barrier of tile t+1 (ring of three,
-// by g mod 3): the K and V copies of the tile (one expect-tx arrival of the
-// loader), and one arrival per compute warp once it has loaded dP(t) out of
-// the single dP region.  K(t) is read by S(t) and dQ(t), a period apart: the
+// Two threads issue the MMAs: A the S and dP products, B the dQ products.  A
+// barrier check waits behind the MMAs its thread has issued, and leaves the
+// tensor pipe idle until the thread issues again; with two issuers the
+// other's queued MMAs cover it.  B checks DSREADY(t) per tile.  A checks
+// READY(t) before S(t) (ring of three, by g mod 3): the K and V copies of the
+// tile (one expect-tx arrival of the loader) and B's commit after dQ(t-2),
+// the last reader of the S region S(t) overwrites; and DPFREE before dP(t):
+// one arrival per compute warp once it has loaded dP(t-1) out of the single
+// dP region.  S(t) thus never waits for the compute warps.  K(t) is read by
+// S(t) and dQ(t), a period apart: the
 // loader fills tile t+1's K stage once dQ(t-2) is done and its V stage once
 // dP(t-1) is done.  The bits
 // of a partial tile have their own one-tile buffer, filled after the compute
@@ -782,7 +786,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr int LD_WARP = 8, MMA_WARP = 9;
+  constexpr int LD_WARP = 8, MMA_WARP = 9, DQ_WARP = 10;
 
   if (tid == 0) {
     // Q is read by the unit's S products only, dO by its dP products: each is
@@ -792,7 +796,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     mbar_init(bar(Q_OFULL), 1);
     mbar_init(bar(Q_OEMPTY), 1);
     for (int s = 0; s < C::KSTAGES; ++s) {
-      mbar_init(bar(Q_READY0 + s), 1 + 8);  // the loader's expect-tx + 8 compute warps
+      // the loader's expect-tx and the dQ issuer's commit
+      mbar_init(bar(Q_READY0 + s), 2);
       mbar_init(bar(Q_KEMPTY0 + s), 1);
     }
     for (int s = 0; s < C::VSTAGES; ++s) mbar_init(bar(Q_VEMPTY0 + s), 1);
@@ -803,9 +808,11 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       mbar_init(bar(Q_DSREADY0 + s), 8);
     }
     mbar_init(bar(Q_DPFULL), 1);
+    mbar_init(bar(Q_DPFREE), 8);  // one arrival per compute warp
     mbar_init(bar(Q_DQFULL), 1);
     mbar_init(bar(Q_DQEMPTY), 8);
-    mbar_init(bar(Q_DRAIN), 1);
+    mbar_init(bar(Q_DRAIN_A), 1);
+    mbar_init(bar(Q_DRAIN_B), 1);
     for (int r = 0; r < UNIT_RING; ++r) {
       mbar_init(bar(Q_UFULL0 + r), 1);
       mbar_init(bar(Q_UEMPTY0 + r), Q_READERS);
@@ -1034,16 +1041,13 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ MMA issuer A: S, dP
     if (lane == 0) {
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S, dP
-      constexpr uint32_t idDQ = idesc_bf16(128, D, false, true);     // dQ (B = K MN-major)
       const uint32_t dQ = sdesc_lo(sbase + C::OFF_Q, 16);
       const uint32_t dO = sdesc_lo(sbase + C::OFF_DO, 16);
       const uint32_t dK0 = sdesc_lo(sbase + C::OFF_K, 16);
-      const uint32_t dKm0 = sdesc_lo(sbase + C::OFF_K, 128 * 128);
       const uint32_t dV0 = sdesc_lo(sbase + C::OFF_V, 16);
-      // S(gt) and then dP(gt): one READY check for both
       auto issue_s = [&](uint32_t gt, bool last) -> bool {
         const uint32_t ks = gt % C::KSTAGES;
         if (!wait(Q_READY0 + ks, (gt / C::KSTAGES) & 1)) return false;
@@ -1062,6 +1066,9 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       };
       auto issue_dp = [&](uint32_t gt, bool last) -> bool {
         const int st = gt & 1;
+        // the compute warps have loaded dP(gt - 1) out of the region
+        if (gt > 0 && !wait(Q_DPFREE, (gt - 1) & 1)) return false;
+        tc_fence_after();
         const uint32_t dV = dV0 + st * (C::TILE >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -1083,12 +1090,38 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         const int n = unit_info(idx, b, h, qi, row, list);
         if (!wait(Q_QFULL, un & 1) || !issue_s(g, n == 1)) break;
         if (!wait(Q_OFULL, un & 1) || !issue_dp(g, n == 1)) break;
-        for (int t = 0; t < n; ++t) {
-          const uint32_t gt = g + t;
-          if (t + 1 < n && (!issue_s(gt + 1, t + 2 == n) || !issue_dp(gt + 1, t + 2 == n))) {
+        for (int t = 1; t < n; ++t) {
+          if (!issue_s(g + t, t + 1 == n) || !issue_dp(g + t, t + 1 == n)) {
             ok = false;
             break;
           }
+        }
+        if (!ok) break;
+        g += n;
+        ++un;
+      }
+      mma_commit(bar(Q_DRAIN_A));
+      mbar_wait(bar(Q_DRAIN_A), 0, P.status, P.wait_ns);
+    }
+    __syncwarp();
+  } else if (warp == DQ_WARP) {
+    // ------------------------------------------------------------ MMA issuer B: dQ
+    if (lane == 0) {
+      constexpr uint32_t idDQ = idesc_bf16(128, D, false, true);  // dQ (B = K MN-major)
+      const uint32_t dKm0 = sdesc_lo(sbase + C::OFF_K, 128 * 128);
+      // S(0) and S(1) overwrite no dS
+      mbar_arrive(bar(Q_READY0));
+      mbar_arrive(bar(Q_READY0 + 1));
+      uint32_t g = 0, un = 0, cn = 0;
+      bool ok = true;
+      while (ok) {
+        const int idx = claimed_one(cn);
+        if (idx < 0) break;
+        int b, h, qi, row;
+        const int32_t* list;
+        const int n = unit_info(idx, b, h, qi, row, list);
+        for (int t = 0; t < n; ++t) {
+          const uint32_t gt = g + t;
           if (!wait(Q_DSREADY0 + (gt & 1), (gt >> 1) & 1)) { ok = false; break; }
           // the previous unit's dQ has been read by the epilogue
           if (t == 0 && un > 0 && !wait(Q_DQEMPTY, (un - 1) & 1)) { ok = false; break; }
@@ -1104,14 +1137,16 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
                    (t > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(bar(Q_KEMPTY0 + ks));  // K(gt): read by S(gt) and this dQ
+          // the S region of tile gt is free for S(gt + 2)
+          mma_commit(bar(Q_READY0 + (gt + 2) % C::KSTAGES));
         }
         if (!ok) break;
         g += n;
         mma_commit(bar(Q_DQFULL));
         ++un;
       }
-      mma_commit(bar(Q_DRAIN));
-      mbar_wait(bar(Q_DRAIN), 0, P.status, P.wait_ns);
+      mma_commit(bar(Q_DRAIN_B));
+      mbar_wait(bar(Q_DRAIN_B), 0, P.status, P.wait_ns);
     }
     __syncwarp();
   }
@@ -1155,7 +1190,6 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       return true;
     };
     bool ok = true;
-    mbar_arrive_warp(bar(Q_READY0));  // tile 0 has no previous dP to wait for
     while (ok) {
       const int idx = claimed_all(cn);
       if (idx < 0) break;
@@ -1212,7 +1246,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
           tmem_wait_ld();
           // dP is in registers: the next dP may overwrite the region
           tc_fence_before();
-          mbar_arrive_warp(bar(Q_READY0 + (gt + 1) % C::KSTAGES));
+          mbar_arrive_warp(bar(Q_DPFREE));
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
