@@ -177,18 +177,20 @@ def run_ours(args):
     lse = torch.empty(B, H, S, dtype=torch.float32, device="cuda")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     desc = fm.make_desc(q, k, v, o)
-    ws_f = fm.workspace(desc, False)
-    ws_b = fm.workspace(desc, True)
+    # one step workspace: the mask analysis runs once per step, for both passes
+    ws = fm.workspace(desc, fm.WS_STEP)
     stream = torch.cuda.current_stream()
 
     def step():
-        fm.forward(q, k, v, bounds, scale, o=o, lse=lse, ws=ws_f, stream=stream)
-        fm.backward(q, k, v, o, lse, do, bounds, scale, dq=dq, dk=dk, dv=dv, ws=ws_b, stream=stream)
+        fm.plan(q, k, bounds, ws=ws, for_bwd=fm.WS_STEP, stream=stream)
+        fm.forward(q, k, v, bounds, scale, o=o, lse=lse, ws=ws, stream=stream, planned=True)
+        fm.backward(q, k, v, o, lse, do, bounds, scale, dq=dq, dk=dk, dv=dv, ws=ws, stream=stream,
+                    planned=True)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    if fm.device_status(ws_f) != 0 or fm.device_status(ws_b) != 0:
+    if fm.device_status(ws) != 0:
         raise RuntimeError("device status not OK after warm-up")
 
     # ---- timed region: K steps, inputs (1 GiB of Q/K/V/dO) larger than L2
@@ -216,21 +218,23 @@ def run_ours(args):
         e2e_ms, h2d, d2h = float("nan"), 0, 0
     else:
         e2e_ms, h2d, d2h = run_e2e(args, fm, q, k, v, do, bounds, scale, o, lse, dq, dk, dv,
-                                   ws_f, ws_b, stream, world)
+                                   ws, stream, world)
+    # the secondary (exp2) ceiling, measured outside the timed regions
+    exp2_rate = fm.measure_exp2_rate(stream) if rank == 0 else None
     per_mask = None
     if not args.no_per_mask and rank == 0:
-        del q, k, v, do, o, lse, dq, dk, dv, ws_f, ws_b
+        del q, k, v, do, o, lse, dq, dk, dv, ws
         torch.cuda.empty_cache()
         per_mask = run_per_mask(args, fm)
     if world > 1:
         dist.barrier()
     report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2d, d2h, clk,
-           per_mask)
+           per_mask, exp2_rate)
     if world > 1:
         dist.destroy_process_group()
 
 
-def run_e2e(args, fm, q, k, v, do, bounds, scale, o, lse, dq, dk, dv, ws_f, ws_b, stream, world):
+def run_e2e(args, fm, q, k, v, do, bounds, scale, o, lse, dq, dk, dv, ws, stream, world):
     """Same step through the public API with pinned HOST inputs and outputs:
     every step copies Q, K, V, dO and the bounds host-to-device and O, LSE,
     dQ, dK, dV device-to-host, all inside the timed region.  The copies run
@@ -267,9 +271,11 @@ def run_e2e(args, fm, q, k, v, do, bounds, scale, o, lse, dq, dk, dv, ws_f, ws_b
         stream.wait_event(in_done[n])
         if i >= 2:
             stream.wait_event(out_done[n])  # step i-2's outputs have left this set
-        fm.forward(dq_in, dk_in, dv_in, db, scale, o=o_n, lse=lse_n, ws=ws_f, stream=stream)
+        fm.plan(dq_in, dk_in, db, ws=ws, for_bwd=fm.WS_STEP, stream=stream)
+        fm.forward(dq_in, dk_in, dv_in, db, scale, o=o_n, lse=lse_n, ws=ws, stream=stream,
+                   planned=True)
         fm.backward(dq_in, dk_in, dv_in, o_n, lse_n, ddo_in, db, scale, dq=dq_n, dk=dk_n, dv=dv_n,
-                    ws=ws_b, stream=stream)
+                    ws=ws, stream=stream, planned=True)
         comp_done[n].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[n])
@@ -296,7 +302,7 @@ def run_e2e(args, fm, q, k, v, do, bounds, scale, o, lse, dq, dk, dv, ws_f, ws_b
     if world > 1:
         dist.barrier()
     e2e_ms = _max_over_ranks(ev0.elapsed_time(ev1) / e_steps, world, "cuda")
-    if fm.device_status(ws_f) != 0 or fm.device_status(ws_b) != 0:
+    if fm.device_status(ws) != 0:
         raise RuntimeError("device status not OK after the end-to-end steps")
     # the forward is deterministic: the last step's host copies of O and LSE
     # equal the outputs the device-timed leg left in buffer set 0
@@ -343,25 +349,27 @@ def run_per_mask(args, fm):
                 lse = torch.empty(B, H, ql.shape[1], dtype=torch.float32, device="cuda")
                 desc = fm.make_desc(ql, k, v, o)
                 bufs.append((ql, dol, bl, o, lse, torch.empty_like(ql), torch.empty_like(k),
-                             torch.empty_like(v), fm.workspace(desc, False), fm.workspace(desc, True)))
+                             torch.empty_like(v), fm.workspace(desc, fm.WS_STEP)))
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(4 * args.mask_steps)]
             for i in range(2 + args.mask_steps):
                 timed = i >= 2
                 j = (i - 2) * 4
                 if timed:
                     ev[j].record(stream)
-                for ql, dol, bl, o, lse, dq, dk, dv, wf, wb in bufs:
-                    fm.forward(ql, k, v, bl, scale, o=o, lse=lse, ws=wf, stream=stream)
+                # the forward's time includes the step's one mask analysis
+                for ql, dol, bl, o, lse, dq, dk, dv, w in bufs:
+                    fm.plan(ql, k, bl, ws=w, for_bwd=fm.WS_STEP, stream=stream)
+                    fm.forward(ql, k, v, bl, scale, o=o, lse=lse, ws=w, stream=stream, planned=True)
                 if timed:
                     ev[j + 1].record(stream)
-                for ql, dol, bl, o, lse, dq, dk, dv, wf, wb in bufs:
-                    fm.backward(ql, k, v, o, lse, dol, bl, scale, dq=dq, dk=dk, dv=dv, ws=wb,
-                                stream=stream)
+                for ql, dol, bl, o, lse, dq, dk, dv, w in bufs:
+                    fm.backward(ql, k, v, o, lse, dol, bl, scale, dq=dq, dk=dk, dv=dv, ws=w,
+                                stream=stream, planned=True)
                 if timed:
                     ev[j + 2].record(stream)
             torch.cuda.synchronize()
             for b_ in bufs:
-                if fm.device_status(b_[8]) != 0 or fm.device_status(b_[9]) != 0:
+                if fm.device_status(b_[8]) != 0:
                     raise RuntimeError(f"device status not OK for {name}/{mask}")
             n = args.mask_steps
             fwd_ms = sum(ev[4 * i].elapsed_time(ev[4 * i + 1]) for i in range(n)) / n
@@ -437,8 +445,23 @@ def _traffic(kernel: str):
     return int(rec["bytes_per_launch"]) if m.hexdigest() == rec["sources_sha256"] else None
 
 
+def exp2_ceiling(rate, d):
+    """Effective-TFLOP/s ceilings set by a measured exp2 rate (evaluations per
+    second): one exp2 per visible entry in the forward (4 * d flop), two in
+    the backward (its dK/dV and dQ kernels each recompute P; 10 * d flop),
+    three per step (14 * d flop)."""
+    if not rate:
+        return None
+    return {"exp2_per_s": float(f"{rate:.4g}"),
+            "fwd_tflops": round(rate * 4 * d / 1e12, 1),
+            "bwd_tflops": round(rate * 10 * d / 2 / 1e12, 1),
+            "step_tflops": round(rate * 14 * d / 3 / 1e12, 1),
+            "how": "fm_measure_exp2_rate: one 1024-thread block per SM, eight independent "
+                   "ex2.approx.f32 chains per thread, CUDA events"}
+
+
 def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2d, d2h, clk,
-           per_mask=None):
+           per_mask=None, exp2_rate=None):
     B, H, S, d = W["B"], W["H"], W["S"], W["d"]
     flop_step = flop_fwd + flop_bwd
     if rank == 0:
@@ -483,7 +506,8 @@ def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2
                          "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                          "peak_source": f"bf16_tflops (burst) of {peak_src}",
                          "traffic": _traffic(dom) if (W["H"] == 32 and world >= 1) else None,
-                         "traffic_unit": "bytes per launch (ncu dram read + write)"},
+                         "traffic_unit": "bytes per launch (ncu dram read + write)",
+                         "exp2_ceiling": exp2_ceiling(exp2_rate, d)},
             "kernel_ms_per_step": {n: round(t / args.steps, 4) for n, (t, c) in prof.items() if c},
             "kernel_launches_per_step": {n: c // args.steps for n, (t, c) in prof.items() if c},
             "kernel_time_share": {n: round(t / total_kernel_ms, 4) for n, (t, c) in prof.items() if c},

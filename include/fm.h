@@ -104,23 +104,35 @@ typedef struct {
   size_t total;      /* bytes needed */
 } fm_ws_layout;
 
-/* Workspace bytes needed by fm_fwd (for_bwd = 0) or fm_bwd (for_bwd = 1).
- * Returns 0 for an invalid description. */
-size_t fm_workspace_size(const fm_desc* desc, int for_bwd);
+/* Workspace kinds (the `mode` argument below; 0 and 1 may also be read as
+ * "for_bwd"): the forward's, the backward's, or a step workspace that holds
+ * the regions of both and the analysis of both passes. */
+#define FM_WS_FWD 0
+#define FM_WS_BWD 1
+#define FM_WS_STEP 2
 
-/* Fill `out` with the region offsets fm_workspace_size() accounts for. */
-fm_status fm_workspace_layout(const fm_desc* desc, int for_bwd, fm_ws_layout* out);
+/* Workspace bytes needed by fm_fwd (mode FM_WS_FWD), fm_bwd (FM_WS_BWD), or
+ * fm_fwd_planned and fm_bwd_planned (FM_WS_STEP).  Returns 0 for an invalid
+ * description or mode. */
+size_t fm_workspace_size(const fm_desc* desc, int mode);
+
+/* Fill `out` with the region offsets fm_workspace_size() accounts for;
+ * regions a mode does not have are 0. */
+fm_status fm_workspace_layout(const fm_desc* desc, int mode, fm_ws_layout* out);
 
 /* Mask analysis into `ws`: validate the bounds (status word), the per-k-block
  * summary, the tile table, the q-tile row lists with the partial tiles' bit
- * masks, and then for for_bwd = 0 the q-tile pair lists and the forward's
- * longest-first unit order, for for_bwd = 1 the k-tile column lists and the
- * longest-first orders of the dK/dV units (columns) and the dQ units (rows).
- * fm_fwd and fm_bwd call this themselves; it is exported so the tables can
- * be inspected. */
+ * masks, and then for FM_WS_FWD the q-tile pair lists and the forward's
+ * longest-first unit order, for FM_WS_BWD the k-tile column lists and the
+ * longest-first orders of the dK/dV units (columns) and the dQ units (rows),
+ * and for FM_WS_STEP all of these.  fm_fwd and fm_bwd run it themselves; a
+ * training step runs it once with FM_WS_STEP and then calls fm_fwd_planned
+ * and fm_bwd_planned (FlashMask-3 page, introduction: the bounds do not
+ * change between the forward and the backward pass).  Zeroes the whole
+ * status word first. */
 fm_status fm_plan(const fm_desc* desc, const int32_t* lts, const int32_t* lte,
                   const int32_t* uts, const int32_t* ute, void* ws, size_t ws_bytes,
-                  int for_bwd, void* stream);
+                  int mode, void* stream);
 
 /* Forward pass.  q [B][Sq][H][d], k and v [B][Skv][H][d] bf16 (inputs);
  * o [B][Sq][H][d] bf16 and lse [B][H][Sq] fp32 (outputs, natural log of the
@@ -142,6 +154,24 @@ fm_status fm_bwd(const fm_desc* desc, const void* q, const void* k, const void* 
                  const void* o, const float* lse, const void* dout, const int32_t* lts,
                  const int32_t* lte, const int32_t* uts, const int32_t* ute, float scale,
                  void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
+
+/* fm_fwd and fm_bwd without the mask analysis: `ws` is a step workspace
+ * (fm_workspace_size(desc, FM_WS_STEP) bytes) on which fm_plan(FM_WS_STEP)
+ * has run, on `stream` or before it, with this `desc` and these bounds, and
+ * which nothing has written since but fm_fwd_planned and fm_bwd_planned.
+ * The bounds are still read (per-key masks of partial tiles).  Each call
+ * zeroes only its kernels' unit counters in the status word, so the
+ * analysis' device status bits stay for fm_device_status.  Results are
+ * identical to fm_fwd / fm_bwd's.  Same arguments and errors otherwise. */
+fm_status fm_fwd_planned(const fm_desc* desc, const void* q, const void* k, const void* v,
+                         const int32_t* lts, const int32_t* lte, const int32_t* uts,
+                         const int32_t* ute, float scale, void* o, float* lse, void* ws,
+                         size_t ws_bytes, void* stream);
+fm_status fm_bwd_planned(const fm_desc* desc, const void* q, const void* k, const void* v,
+                         const void* o, const float* lse, const void* dout,
+                         const int32_t* lts, const int32_t* lte, const int32_t* uts,
+                         const int32_t* ute, float scale, void* dq, void* dk, void* dv,
+                         void* ws, size_t ws_bytes, void* stream);
 
 /* Size of the fixed device scratch used by fm_fwd_static (8 MiB per GPU). */
 #define FM_STATIC_SCRATCH_BYTES (8u << 20)
@@ -207,6 +237,16 @@ fm_status fm_localize(const int32_t* bounds, int B, int Hm, int Skv,
 fm_status fm_profile_enable(int on);
 fm_status fm_profile_read(double* total_ms, int* launches, int n);
 const char* fm_kernel_name(int id);
+
+/* Measured exp2 throughput of this GPU: a kernel of one 1024-thread block
+ * per SM, each thread eight independent chains of ex2.approx.f32 (the
+ * instruction that computes P in the attention kernels), timed with CUDA
+ * events on `stream` (synchronises it).  Writes exp2 evaluations per second
+ * for the whole GPU; the host turns it into a ceiling on effective TFLOP/s
+ * (one exp2 per visible entry in the forward, two in the backward).  No
+ * counterpart on the pages: it measures the secondary (non-matmul) limit
+ * the FlashAttention-2 page's «Три способа повысить загрузку GPU» is about. */
+fm_status fm_measure_exp2_rate(double* per_second, void* stream);
 
 /* Test hooks for the device-side wait limit (process-wide; they apply to
  * every launch made after the call).  Every mbarrier wait in the attention

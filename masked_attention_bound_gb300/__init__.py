@@ -54,21 +54,27 @@ def make_desc(q, k, v=None, o=None, Hm: int = 1) -> FmDesc:
     return D
 
 
-def workspace_size(desc: FmDesc, for_bwd: bool) -> int:
-    n = lib().fm_workspace_size(ctypes.byref(desc), int(bool(for_bwd)))
+# workspace kinds: the forward's, the backward's, and a step workspace with
+# both passes' regions (one mask analysis per training step)
+WS_FWD, WS_BWD, WS_STEP = 0, 1, 2
+
+
+def workspace_size(desc: FmDesc, for_bwd) -> int:
+    """Bytes of workspace; ``for_bwd`` is False/True or one of WS_FWD, WS_BWD, WS_STEP."""
+    n = lib().fm_workspace_size(ctypes.byref(desc), int(for_bwd))
     if n == 0:
         raise FMError(1, "fm_workspace_size")
     return n
 
 
-def workspace_layout(desc: FmDesc, for_bwd: bool) -> FmWsLayout:
+def workspace_layout(desc: FmDesc, for_bwd) -> FmWsLayout:
     out = FmWsLayout()
-    check(lib().fm_workspace_layout(ctypes.byref(desc), int(bool(for_bwd)), ctypes.byref(out)),
+    check(lib().fm_workspace_layout(ctypes.byref(desc), int(for_bwd), ctypes.byref(out)),
           "fm_workspace_layout")
     return out
 
 
-def workspace(desc: FmDesc, for_bwd: bool, device="cuda") -> torch.Tensor:
+def workspace(desc: FmDesc, for_bwd, device="cuda") -> torch.Tensor:
     """A byte tensor large enough (and 256-byte aligned) for the call."""
     return torch.empty(workspace_size(desc, for_bwd), dtype=torch.uint8, device=device)
 
@@ -81,17 +87,21 @@ def _bounds_ptrs(bounds):
 
 
 def plan(q, k, bounds, ws=None, for_bwd=False, stream=None):
-    """Run the mask analysis only; returns (workspace tensor, layout)."""
+    """Run the mask analysis only; returns (workspace tensor, layout).  With
+    ``for_bwd=WS_STEP`` it prepares a step workspace for
+    ``forward(..., planned=True)`` and ``backward(..., planned=True)``."""
     desc = make_desc(q, k, Hm=bounds.shape[2])
     if ws is None:
         ws = workspace(desc, for_bwd, q.device)
     check(lib().fm_plan(ctypes.byref(desc), *_bounds_ptrs(bounds), _p(ws), ws.numel(),
-                        int(bool(for_bwd)), _stream_ptr(stream)), "fm_plan")
+                        int(for_bwd), _stream_ptr(stream)), "fm_plan")
     return ws, workspace_layout(desc, for_bwd)
 
 
-def forward(q, k, v, bounds, scale, o=None, lse=None, ws=None, stream=None):
-    """O [B][Sq][H][d] bf16 and LSE [B][H][Sq] fp32 (natural log)."""
+def forward(q, k, v, bounds, scale, o=None, lse=None, ws=None, stream=None, planned=False):
+    """O [B][Sq][H][d] bf16 and LSE [B][H][Sq] fp32 (natural log).  ``planned``:
+    ``ws`` is a step workspace that ``plan(..., for_bwd=WS_STEP)`` prepared for
+    these bounds; the mask analysis is then not run again."""
     B, Sq, H, d = q.shape
     if o is None:
         o = torch.empty_like(q)
@@ -99,16 +109,20 @@ def forward(q, k, v, bounds, scale, o=None, lse=None, ws=None, stream=None):
         lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
     desc = make_desc(q, k, v, o, Hm=bounds.shape[2])
     if ws is None:
+        if planned:
+            raise ValueError("planned=True needs the step workspace plan() prepared")
         ws = workspace(desc, False, q.device)
-    check(lib().fm_fwd(ctypes.byref(desc), _p(q), _p(k), _p(v), *_bounds_ptrs(bounds),
-                       ctypes.c_float(scale), _p(o), _p(lse), _p(ws), ws.numel(),
-                       _stream_ptr(stream)), "fm_fwd")
+    name = "fm_fwd_planned" if planned else "fm_fwd"
+    check(getattr(lib(), name)(ctypes.byref(desc), _p(q), _p(k), _p(v), *_bounds_ptrs(bounds),
+                               ctypes.c_float(scale), _p(o), _p(lse), _p(ws), ws.numel(),
+                               _stream_ptr(stream)), name)
     return o, lse
 
 
 def backward(q, k, v, o, lse, do, bounds, scale, dq=None, dk=None, dv=None, ws=None,
-             stream=None):
-    """dQ, dK, dV (bf16) for the loss whose gradient with respect to O is dO."""
+             stream=None, planned=False):
+    """dQ, dK, dV (bf16) for the loss whose gradient with respect to O is dO.
+    ``planned`` as for ``forward``."""
     if do.stride() != o.stride():
         do = do.contiguous() if o.is_contiguous() else do
         if do.stride() != o.stride():
@@ -121,10 +135,13 @@ def backward(q, k, v, o, lse, do, bounds, scale, dq=None, dk=None, dv=None, ws=N
             raise ValueError("gradient tensors must have the strides of their inputs")
     desc = make_desc(q, k, v, o, Hm=bounds.shape[2])
     if ws is None:
+        if planned:
+            raise ValueError("planned=True needs the step workspace plan() prepared")
         ws = workspace(desc, True, q.device)
-    check(lib().fm_bwd(ctypes.byref(desc), _p(q), _p(k), _p(v), _p(o), _p(lse), _p(do),
-                       *_bounds_ptrs(bounds), ctypes.c_float(scale), _p(dq), _p(dk), _p(dv),
-                       _p(ws), ws.numel(), _stream_ptr(stream)), "fm_bwd")
+    name = "fm_bwd_planned" if planned else "fm_bwd"
+    check(getattr(lib(), name)(ctypes.byref(desc), _p(q), _p(k), _p(v), _p(o), _p(lse), _p(do),
+                               *_bounds_ptrs(bounds), ctypes.c_float(scale), _p(dq), _p(dk),
+                               _p(dv), _p(ws), ws.numel(), _stream_ptr(stream)), name)
     return dq, dk, dv
 
 
@@ -161,3 +178,11 @@ def profile_read():
     n = (ctypes.c_int * KERNEL_IDS)()
     check(lib().fm_profile_read(ms, n, KERNEL_IDS), "fm_profile_read")
     return {lib().fm_kernel_name(i).decode(): (ms[i], n[i]) for i in range(KERNEL_IDS)}
+
+
+def measure_exp2_rate(stream=None) -> float:
+    """exp2 evaluations per second of this GPU (ex2.approx.f32, all SMs)."""
+    out = ctypes.c_double(0.0)
+    check(lib().fm_measure_exp2_rate(ctypes.byref(out), _stream_ptr(stream)),
+          "fm_measure_exp2_rate")
+    return out.value

@@ -55,6 +55,10 @@ SIGNATURES = {
                               ctypes.c_float, P, P, P, ctypes.c_size_t, P]),
     "fm_bwd": (ctypes.c_int, [ctypes.POINTER(FmDesc), P, P, P, P, P, P, I32P, I32P, I32P, I32P,
                               ctypes.c_float, P, P, P, P, ctypes.c_size_t, P]),
+    "fm_fwd_planned": (ctypes.c_int, [ctypes.POINTER(FmDesc), P, P, P, I32P, I32P, I32P, I32P,
+                                      ctypes.c_float, P, P, P, ctypes.c_size_t, P]),
+    "fm_bwd_planned": (ctypes.c_int, [ctypes.POINTER(FmDesc), P, P, P, P, P, P, I32P, I32P, I32P,
+                                      I32P, ctypes.c_float, P, P, P, P, ctypes.c_size_t, P]),
     "fm_fwd_static": (ctypes.c_int, [ctypes.POINTER(FmDesc), P, P, P, I32P, I32P, I32P, I32P,
                                      ctypes.c_float, P, P, P]),
     "fm_localize": (ctypes.c_int, [I32P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
@@ -66,6 +70,7 @@ SIGNATURES = {
     "fm_profile_enable": (ctypes.c_int, [ctypes.c_int]),
     "fm_profile_read": (ctypes.c_int, [P, P, ctypes.c_int]),
     "fm_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),
+    "fm_measure_exp2_rate": (ctypes.c_int, [P, P]),
 }
 
 KERNEL_IDS = 9

@@ -32,8 +32,9 @@ static bool strides_ok(const int64_t* st) {
   return true;
 }
 
-fm_status make_plan(const fm_desc* desc, int for_bwd, Plan* p, size_t limit) {
+fm_status make_plan(const fm_desc* desc, int mode, Plan* p, size_t limit) {
   if (!desc || !p) return FM_ERR_INVALID;
+  if (mode < FM_WS_FWD || mode > FM_WS_STEP) return FM_ERR_INVALID;
   const fm_desc& D = *desc;
   if (D.B < 1 || D.H < 1 || D.Sq < 1 || D.Skv < 1 || D.d < 1) return FM_ERR_INVALID;
   if (D.Hm != 1 && D.Hm != D.H) return FM_ERR_INVALID;
@@ -61,15 +62,12 @@ fm_status make_plan(const fm_desc* desc, int for_bwd, Plan* p, size_t limit) {
   L.fwd_order = take(BH * p->nQ * 4);
   L.bwd_order = take(BH * p->nK * 4);
   L.row_mask = take(BHm * p->nQ * 4);
-  if (!for_bwd) {
+  L.pair_info = L.pair_list = L.delta = L.lse_log2 = L.row_order = 0;
+  if (mode != FM_WS_BWD) {
     L.pair_info = take(BHm * p->nP * 16);
     L.pair_list = take(BHm * p->nP * p->nK * 4);
-    L.delta = 0;
-    L.lse_log2 = 0;
-    L.row_order = 0;
-  } else {
-    L.pair_info = 0;
-    L.pair_list = 0;
+  }
+  if (mode != FM_WS_FWD) {
     L.delta = take(BH * p->nQ * kTile * 4);
     L.lse_log2 = take(BH * p->nQ * kTile * 4);
     L.row_order = take(BH * p->nQ * 4);
@@ -99,18 +97,25 @@ static bool aligned16(const void* ptr) {
 }
 
 static fm_status run_plan(const Plan& p, const int32_t* lts, const int32_t* lte,
-                          const int32_t* uts, const int32_t* ute, char* ws, int for_bwd,
+                          const int32_t* uts, const int32_t* ute, char* ws, int mode,
                           cudaStream_t s) {
   if (cudaMemsetAsync(ws + p.L.status, 0, 32, s) != cudaSuccess) return FM_ERR_CUDA;
   if (launch_summary(p, lts, lte, uts, ute, ws, s) != cudaSuccess) return FM_ERR_CUDA;
-  if (launch_classify(p, ws, for_bwd, s) != cudaSuccess) return FM_ERR_CUDA;
+  if (launch_classify(p, ws, mode, s) != cudaSuccess) return FM_ERR_CUDA;
   if (launch_tile_masks(p, lts, lte, uts, ute, ws, s) != cudaSuccess) return FM_ERR_CUDA;
-  if (!for_bwd) {
-    if (launch_order(p, ws, ORDER_PAIRS, s) != cudaSuccess) return FM_ERR_CUDA;
-  } else if (launch_order(p, ws, ORDER_COLS, s) != cudaSuccess ||
-             launch_order(p, ws, ORDER_ROWS, s) != cudaSuccess) {
+  if (mode != FM_WS_BWD && launch_order(p, ws, ORDER_PAIRS, s) != cudaSuccess) return FM_ERR_CUDA;
+  if (mode != FM_WS_FWD && (launch_order(p, ws, ORDER_COLS, s) != cudaSuccess ||
+                            launch_order(p, ws, ORDER_ROWS, s) != cudaSuccess))
     return FM_ERR_CUDA;
-  }
+  return FM_OK;
+}
+
+// Zero the status words that count the attention kernels' claimed units
+// ([1]: the forward's and the dK/dV pass's, [4]: the dQ pass's), keeping the
+// analysis' device status bits and mask-slot count.
+static fm_status reset_claims(const Plan& p, char* ws, int bwd, cudaStream_t s) {
+  if (cudaMemsetAsync(ws + p.L.status + 4, 0, 4, s) != cudaSuccess) return FM_ERR_CUDA;
+  if (bwd && cudaMemsetAsync(ws + p.L.status + 16, 0, 4, s) != cudaSuccess) return FM_ERR_CUDA;
   return FM_OK;
 }
 
@@ -120,16 +125,16 @@ using namespace fm;
 
 extern "C" {
 
-size_t fm_workspace_size(const fm_desc* desc, int for_bwd) {
+size_t fm_workspace_size(const fm_desc* desc, int mode) {
   Plan p;
-  if (make_plan(desc, for_bwd, &p) != FM_OK) return 0;
+  if (make_plan(desc, mode, &p) != FM_OK) return 0;
   return p.L.total;
 }
 
-fm_status fm_workspace_layout(const fm_desc* desc, int for_bwd, fm_ws_layout* out) {
+fm_status fm_workspace_layout(const fm_desc* desc, int mode, fm_ws_layout* out) {
   if (!out) return FM_ERR_INVALID;
   Plan p;
-  fm_status st = make_plan(desc, for_bwd, &p);
+  fm_status st = make_plan(desc, mode, &p);
   if (st != FM_OK) return st;
   *out = p.L;
   return FM_OK;
@@ -137,29 +142,32 @@ fm_status fm_workspace_layout(const fm_desc* desc, int for_bwd, fm_ws_layout* ou
 
 fm_status fm_plan(const fm_desc* desc, const int32_t* lts, const int32_t* lte,
                   const int32_t* uts, const int32_t* ute, void* ws, size_t ws_bytes,
-                  int for_bwd, void* stream) {
+                  int mode, void* stream) {
   Plan p;
-  fm_status st = make_plan(desc, for_bwd, &p);
+  fm_status st = make_plan(desc, mode, &p);
   if (st != FM_OK) return st;
   if (!lts || !lte || !uts || !ute) return FM_ERR_INVALID;
   if ((st = check_ws(p, ws, ws_bytes)) != FM_OK) return st;
-  return run_plan(p, lts, lte, uts, ute, static_cast<char*>(ws), for_bwd,
+  return run_plan(p, lts, lte, uts, ute, static_cast<char*>(ws), mode,
                   static_cast<cudaStream_t>(stream));
 }
 
-fm_status fm_fwd(const fm_desc* desc, const void* q, const void* k, const void* v,
-                 const int32_t* lts, const int32_t* lte, const int32_t* uts,
-                 const int32_t* ute, float scale, void* o, float* lse, void* ws,
-                 size_t ws_bytes, void* stream) {
+// The forward with its own analysis (planned = 0, FM_WS_FWD layout) or on a
+// step workspace whose analysis fm_plan(FM_WS_STEP) made (planned = 1).
+static fm_status run_forward(const fm_desc* desc, const void* q, const void* k, const void* v,
+                         const int32_t* lts, const int32_t* lte, const int32_t* uts,
+                         const int32_t* ute, float scale, void* o, float* lse, void* ws,
+                         size_t ws_bytes, void* stream, int planned) {
   Plan p;
-  fm_status st = make_plan(desc, 0, &p);
+  fm_status st = make_plan(desc, planned ? FM_WS_STEP : FM_WS_FWD, &p);
   if (st != FM_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !lse) return FM_ERR_INVALID;
   if (!lts || !lte || !uts || !ute) return FM_ERR_INVALID;
   if ((st = check_ws(p, ws, ws_bytes)) != FM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
-  if ((st = run_plan(p, lts, lte, uts, ute, w, 0, s)) != FM_OK) return st;
+  st = planned ? reset_claims(p, w, 0, s) : run_plan(p, lts, lte, uts, ute, w, FM_WS_FWD, s);
+  if (st != FM_OK) return st;
   TensorArgs t{};
   t.q = q; t.k = k; t.v = v; t.o_out = o; t.lse_out = lse;
   t.bounds[0] = lts; t.bounds[1] = lte; t.bounds[2] = uts; t.bounds[3] = ute;
@@ -167,12 +175,13 @@ fm_status fm_fwd(const fm_desc* desc, const void* q, const void* k, const void* 
   return launch_fwd(p, *desc, t, w, s);
 }
 
-fm_status fm_bwd(const fm_desc* desc, const void* q, const void* k, const void* v,
-                 const void* o, const float* lse, const void* dout, const int32_t* lts,
-                 const int32_t* lte, const int32_t* uts, const int32_t* ute, float scale,
-                 void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+static fm_status run_backward(const fm_desc* desc, const void* q, const void* k, const void* v,
+                          const void* o, const float* lse, const void* dout,
+                          const int32_t* lts, const int32_t* lte, const int32_t* uts,
+                          const int32_t* ute, float scale, void* dq, void* dk, void* dv,
+                          void* ws, size_t ws_bytes, void* stream, int planned) {
   Plan p;
-  fm_status st = make_plan(desc, 1, &p);
+  fm_status st = make_plan(desc, planned ? FM_WS_STEP : FM_WS_BWD, &p);
   if (st != FM_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !lse)
@@ -181,13 +190,45 @@ fm_status fm_bwd(const fm_desc* desc, const void* q, const void* k, const void* 
   if ((st = check_ws(p, ws, ws_bytes)) != FM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
-  if ((st = run_plan(p, lts, lte, uts, ute, w, 1, s)) != FM_OK) return st;
+  st = planned ? reset_claims(p, w, 1, s) : run_plan(p, lts, lte, uts, ute, w, FM_WS_BWD, s);
+  if (st != FM_OK) return st;
   TensorArgs t{};
   t.q = q; t.k = k; t.v = v; t.o = o; t.dout = dout; t.lse_in = lse;
   t.dq = dq; t.dk = dk; t.dv = dv;
   t.bounds[0] = lts; t.bounds[1] = lte; t.bounds[2] = uts; t.bounds[3] = ute;
   t.scale = scale;
   return launch_bwd(p, *desc, t, w, s);
+}
+
+fm_status fm_fwd(const fm_desc* desc, const void* q, const void* k, const void* v,
+                 const int32_t* lts, const int32_t* lte, const int32_t* uts,
+                 const int32_t* ute, float scale, void* o, float* lse, void* ws,
+                 size_t ws_bytes, void* stream) {
+  return run_forward(desc, q, k, v, lts, lte, uts, ute, scale, o, lse, ws, ws_bytes, stream, 0);
+}
+
+fm_status fm_fwd_planned(const fm_desc* desc, const void* q, const void* k, const void* v,
+                         const int32_t* lts, const int32_t* lte, const int32_t* uts,
+                         const int32_t* ute, float scale, void* o, float* lse, void* ws,
+                         size_t ws_bytes, void* stream) {
+  return run_forward(desc, q, k, v, lts, lte, uts, ute, scale, o, lse, ws, ws_bytes, stream, 1);
+}
+
+fm_status fm_bwd(const fm_desc* desc, const void* q, const void* k, const void* v,
+                 const void* o, const float* lse, const void* dout, const int32_t* lts,
+                 const int32_t* lte, const int32_t* uts, const int32_t* ute, float scale,
+                 void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+  return run_backward(desc, q, k, v, o, lse, dout, lts, lte, uts, ute, scale, dq, dk, dv, ws,
+                  ws_bytes, stream, 0);
+}
+
+fm_status fm_bwd_planned(const fm_desc* desc, const void* q, const void* k, const void* v,
+                         const void* o, const float* lse, const void* dout,
+                         const int32_t* lts, const int32_t* lte, const int32_t* uts,
+                         const int32_t* ute, float scale, void* dq, void* dk, void* dv,
+                         void* ws, size_t ws_bytes, void* stream) {
+  return run_backward(desc, q, k, v, o, lse, dout, lts, lte, uts, ute, scale, dq, dk, dv, ws,
+                  ws_bytes, stream, 1);
 }
 
 fm_status fm_localize(const int32_t* bounds, int B, int Hm, int Skv,

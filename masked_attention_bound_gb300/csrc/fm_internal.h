@@ -28,12 +28,13 @@ struct Plan {
 // limit: the most bytes the forward layout may take; the visibility-mask
 // region shrinks to fit (rows without slots fall back to bits built in the
 // forward kernel).  Other regions do not shrink.
-fm_status make_plan(const fm_desc* desc, int for_bwd, Plan* p, size_t limit = SIZE_MAX);
+// mode: FM_WS_FWD, FM_WS_BWD or FM_WS_STEP (both passes)
+fm_status make_plan(const fm_desc* desc, int mode, Plan* p, size_t limit = SIZE_MAX);
 
 // Mask analysis kernels (fm_mask.cu).
 cudaError_t launch_summary(const Plan& p, const int32_t* lts, const int32_t* lte,
                            const int32_t* uts, const int32_t* ute, char* ws, cudaStream_t s);
-cudaError_t launch_classify(const Plan& p, char* ws, int for_bwd, cudaStream_t s);
+cudaError_t launch_classify(const Plan& p, char* ws, int mode, cudaStream_t s);
 // unit orders: ORDER_PAIRS (forward, q-tile pairs), ORDER_COLS (dK/dV, k-tile
 // columns), ORDER_ROWS (dQ, q-tile rows)
 enum : int { ORDER_PAIRS = 0, ORDER_COLS, ORDER_ROWS };

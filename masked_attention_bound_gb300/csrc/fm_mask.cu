@@ -394,7 +394,7 @@ cudaError_t launch_summary(const Plan& p, const int32_t* lts, const int32_t* lte
   return cudaGetLastError();
 }
 
-cudaError_t launch_classify(const Plan& p, char* ws, int for_bwd, cudaStream_t s) {
+cudaError_t launch_classify(const Plan& p, char* ws, int mode, cudaStream_t s) {
   const int nBH = p.B * p.Hm;
   const int32_t* summ = reinterpret_cast<const int32_t*>(ws + p.L.summary);
   uint8_t* table = reinterpret_cast<uint8_t*>(ws + p.L.table);
@@ -405,12 +405,13 @@ cudaError_t launch_classify(const Plan& p, char* ws, int for_bwd, cudaStream_t s
       summ, nBH, p.nQ, p.nK, p.Sq, p.Skv, table, reinterpret_cast<int32_t*>(ws + p.L.row_count),
       reinterpret_cast<int32_t*>(ws + p.L.row_list), reinterpret_cast<int32_t*>(ws + p.L.row_mask),
       reinterpret_cast<unsigned long long*>(ws + p.L.status + 8), p.mask_cap);
-  if (!for_bwd) {
+  if (mode != FM_WS_BWD) {
     const int pwarps = nBH * p.nP;
     classify_pairs_kernel<<<ceil_div(pwarps, 8), 256, 0, s>>>(
         table, nBH, p.nQ, p.nK, p.nP, p.Skv, reinterpret_cast<int4*>(ws + p.L.pair_info),
         reinterpret_cast<int32_t*>(ws + p.L.pair_list));
-  } else {
+  }
+  if (mode != FM_WS_FWD) {
     const int warps = nBH * p.nK;
     classify_cols_kernel<<<ceil_div(warps, 8), 256, 0, s>>>(
         summ, nBH, p.nQ, p.nK, p.Sq, table, reinterpret_cast<int32_t*>(ws + p.L.col_count),

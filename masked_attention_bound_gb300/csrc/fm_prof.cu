@@ -2,6 +2,7 @@
 #include <vector>
 
 #include "fm_internal.h"
+#include "fm_ptx.cuh"
 
 namespace fm {
 
@@ -46,11 +47,50 @@ void prof_end(int id, cudaStream_t s) {
   g_open = -1;
 }
 
+// exp2 throughput: every thread runs eight independent chains of
+// ex2.approx (the instruction the attention kernels use for P), so the
+// MUFU, not the chains' latency, bounds the rate.
+__global__ void __launch_bounds__(1024) ex2_rate_kernel(int iters, float* sink) {
+  float x[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) x[j] = -1e-3f * static_cast<float>(threadIdx.x + j);
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = ex2(x[j]) - 1.0f;
+  }
+  float t = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) t += x[j];
+  if (t == 12345.0f) sink[blockIdx.x] = t;  // never true; keeps the chains live
+}
+
 }  // namespace fm
 
 using namespace fm;
 
 extern "C" {
+
+fm_status fm_measure_exp2_rate(double* per_second, void* stream) {
+  if (!per_second) return FM_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int blocks = num_sms(), threads = 1024, iters = 4096;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) return FM_ERR_CUDA;
+  fm_status st = FM_OK;
+  ex2_rate_kernel<<<blocks, threads, 0, s>>>(iters / 8, nullptr);  // warm-up
+  cudaEventRecord(e0, s);
+  ex2_rate_kernel<<<blocks, threads, 0, s>>>(iters, nullptr);
+  cudaEventRecord(e1, s);
+  float ms = 0.f;
+  if (cudaGetLastError() != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+      cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess || ms <= 0.f)
+    st = FM_ERR_CUDA;
+  else
+    *per_second = static_cast<double>(blocks) * threads * iters * 8.0 / (ms * 1e-3);
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  return st;
+}
 
 fm_status fm_profile_enable(int on) {
   g_on = on != 0;

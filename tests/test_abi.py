@@ -58,6 +58,29 @@ def test_workspace_size_and_layout(L):
     assert lay.masks - lay.row_order >= 1 * 2 * 2 * 4
 
 
+def test_step_workspace_holds_both_passes(L):
+    """A step workspace (mode 2) has every region of the forward's and of the
+    backward's layout; mode 3 is rejected."""
+    D = _desc()
+    n0, n1, n2 = (L.fm_workspace_size(ctypes.byref(D), m) for m in (0, 1, 2))
+    assert n2 >= max(n0, n1)
+    lays = []
+    for m in (0, 1, 2):
+        lay = _abi.FmWsLayout()
+        assert L.fm_workspace_layout(ctypes.byref(D), m, ctypes.byref(lay)) == 0
+        lays.append(lay)
+    f, b, st = lays
+    assert f.pair_info and f.pair_list and not f.delta and not f.row_order
+    assert b.delta and b.lse_log2 and b.row_order and not b.pair_info
+    assert st.pair_info and st.pair_list and st.delta and st.lse_log2 and st.row_order
+    assert st.total == n2
+    # regions in order, none overlapping the next
+    offs = sorted(getattr(st, fld) for fld, _ in _abi.FmWsLayout._fields_ if fld != "total")
+    assert len(set(offs)) == len(offs)
+    assert L.fm_workspace_size(ctypes.byref(D), 3) == 0
+    assert L.fm_workspace_layout(ctypes.byref(D), -1, ctypes.byref(_abi.FmWsLayout())) == 1
+
+
 @pytest.mark.parametrize("field,value,code", [
     ("d", 96, 3), ("d", 0, 1), ("Hm", 3, 1), ("B", 0, 1), ("Sq", 0, 1), ("Skv", -1, 1)])
 def test_bad_descriptions(L, field, value, code):

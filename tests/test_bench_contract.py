@@ -26,7 +26,8 @@ def _report(world=1, ms=2.0, e2e_ms=7.0):
     buf = io.StringIO()
     with contextlib.redirect_stdout(buf):
         bench.report(args, W, world, 0, ms, prof, 3.0e11, 7.5e11, 123456, e2e_ms, 1000, 2000,
-                     {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3})
+                     {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3},
+                     exp2_rate=1.0e13)
     return json.loads(buf.getvalue().strip().splitlines()[-1])
 
 
@@ -43,6 +44,12 @@ def test_device_arm_line():
     assert r["achieved"] == pytest.approx(8 * 3.0e11 / 4 / 0.8e-3 / 1e12, rel=1e-3)
     assert d["bwd_tflops"] == pytest.approx(7.5e11 / 1.3e-3 / 1e12, rel=1e-3)
     assert r["frac"] == pytest.approx(r["achieved"] / r["peak"], rel=1e-3)
+    # exp2 ceiling: 1e13 exp2/s, one per entry forward (4d), two backward (10d)
+    c = r["exp2_ceiling"]
+    d_ = bench.WORKLOAD["d"]
+    assert c["fwd_tflops"] == pytest.approx(1e13 * 4 * d_ / 1e12, rel=1e-3)
+    assert c["bwd_tflops"] == pytest.approx(1e13 * 5 * d_ / 1e12, rel=1e-3)
+    assert c["step_tflops"] == pytest.approx(1e13 * 14 * d_ / 3 / 1e12, rel=1e-2)
     e = d["e2e"]
     assert e["value"] == pytest.approx(1.05e12 / 7e-3 / 1e12, rel=1e-3)
     assert e["h2d_bytes_per_step"] == 1000 and e["d2h_bytes_per_step"] == 2000

@@ -32,6 +32,41 @@ def test_tiny_config():
     compare_bwd(q, k, v, do, bounds, TINY.scale, dq, dk, dv)
 
 
+@pytest.mark.parametrize("name", ["causal_document", "share_question", "random_eviction"])
+def test_planned_step_equals_separate_calls(name):
+    """One mask analysis per step (fm_plan on a step workspace, then
+    fm_fwd_planned and fm_bwd_planned) gives bit-identical O, LSE, dQ, dK, dV
+    to fm_fwd and fm_bwd with their own analyses, and launches each analysis
+    kernel once per step; repeated on the same workspace, it stays identical."""
+    B, S, H, d = 1, 2 * 1024 + 77, 4, 128
+    scale = d ** -0.5
+    q, k, v, do = qkv_do(B, S, S, H, d, seed=5, device="cuda")
+    bounds = mask_bounds(name, B, S, device="cuda")
+    o, lse, dq, dk, dv = _run(q, k, v, do, bounds, scale)
+    desc = fm.make_desc(q, k, v, q)
+    ws = fm.workspace(desc, fm.WS_STEP)
+    got = None
+    fm.profile_read()  # clears the counters
+    for rep in range(2):
+        fm.profile_enable(True)
+        fm.plan(q, k, bounds, ws=ws, for_bwd=fm.WS_STEP)
+        o2, lse2 = fm.forward(q, k, v, bounds, scale, ws=ws, planned=True)
+        dq2, dk2, dv2 = fm.backward(q, k, v, o2, lse2, do, bounds, scale, ws=ws, planned=True)
+        torch.cuda.synchronize()
+        fm.profile_enable(False)
+        prof = fm.profile_read()
+        assert fm.device_status(ws) == 0
+        for kname in ("summary_kernel", "classify_kernel", "tile_mask_kernel", "fwd_kernel",
+                      "bwd_pre_kernel", "bwd_kv_kernel", "bwd_dq_kernel"):
+            assert prof[kname][1] == 1, (kname, prof[kname])
+        assert prof["order_kernel"][1] == 3  # forward pairs, dK/dV columns, dQ rows
+        for a, b_ in ((o, o2), (lse, lse2), (dq, dq2), (dk, dk2), (dv, dv2)):
+            assert torch.equal(a, b_)
+        if got is not None:
+            assert all(torch.equal(a, b_) for a, b_ in zip(got, (o2, lse2, dq2, dk2, dv2)))
+        got = (o2, lse2, dq2, dk2, dv2)
+
+
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("S", [1, 77, 128, 300, 1000])
 @pytest.mark.parametrize("name", ["full", "causal", "causal_document", "qk_sparse",
