@@ -16,7 +16,14 @@ oracle is the plain definition, one (batch, head) at a time:
 
 Tensors are BSHD ([batch][seq][head][d]) float64 arrays holding the bf16
 values exactly; bounds are [4][B][Hm][Skv] (head h uses mask head 0 when
-Hm == 1, else h).  Rows are independent: ``slice_rows`` only bounds the size of
+Hm == 1, else h).
+
+Grouped-query attention (the ROCm page lists GQA among the key features of
+current attention kernels; it gives no formula): K and V may have Hkv heads
+with H = G * Hkv query heads; query head h attends with K/V head h // G
+(consecutive query heads share one K/V head), and, since a shared head enters
+G per-query-head losses, its gradients dK and dV are the sums of the G
+per-head gradients (chain rule).  Hkv = H is ordinary multi-head attention.  Rows are independent: ``slice_rows`` only bounds the size of
 the dense score block held at once; with it the row sums in dK and dV are
 accumulated one row group after another.
 """
@@ -125,14 +132,24 @@ def backward_head(q, k, v, do, mvec, scale, slice_rows=None, skip_hidden=False):
     return dq, dk, dv, o, lse, D
 
 
+def kv_head(h: int, H: int, Hkv: int) -> int:
+    """The K/V head query head h reads: h // G with G = H / Hkv."""
+    if Hkv < 1 or H % Hkv:
+        raise ValueError("the K/V head count must divide the query head count")
+    return h // (H // Hkv)
+
+
 def forward(q, k, v, bounds, scale, slice_rows=None):
-    """O [B][Sq][H][d] and LSE [B][H][Sq] for BSHD float64 inputs."""
+    """O [B][Sq][H][d] and LSE [B][H][Sq] for BSHD float64 inputs (k, v may
+    have fewer heads than q: grouped-query attention)."""
     B, Sq, H, d = q.shape
+    Hkv = k.shape[2]
     o = np.zeros((B, Sq, H, v.shape[3]))
     lse = np.zeros((B, H, Sq))
     for b in range(B):
         for h in range(H):
-            ob, lb = forward_head(q[b, :, h], k[b, :, h], v[b, :, h],
+            hk = kv_head(h, H, Hkv)
+            ob, lb = forward_head(q[b, :, h], k[b, :, hk], v[b, :, hk],
                                   _mask_vectors(bounds, b, h), scale, slice_rows=slice_rows)
             o[b, :, h] = ob
             lse[b, h] = lb
@@ -140,15 +157,21 @@ def forward(q, k, v, bounds, scale, slice_rows=None):
 
 
 def backward(q, k, v, do, bounds, scale, slice_rows=None):
-    """(dq, dk, dv, o, lse, D) for BSHD float64 inputs; D is [B][H][Sq]."""
+    """(dq, dk, dv, o, lse, D) for BSHD float64 inputs; D is [B][H][Sq].  With
+    fewer K/V heads than query heads, dk and dv of a K/V head sum over the
+    query heads that read it."""
     B, Sq, H, d = q.shape
+    Hkv = k.shape[2]
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     o = np.zeros((B, Sq, H, v.shape[3]))
     lse = np.zeros((B, H, Sq))
     D = np.zeros((B, H, Sq))
     for b in range(B):
         for h in range(H):
-            r = backward_head(q[b, :, h], k[b, :, h], v[b, :, h], do[b, :, h],
+            hk = kv_head(h, H, Hkv)
+            r = backward_head(q[b, :, h], k[b, :, hk], v[b, :, hk], do[b, :, h],
                               _mask_vectors(bounds, b, h), scale, slice_rows=slice_rows)
-            dq[b, :, h], dk[b, :, h], dv[b, :, h], o[b, :, h], lse[b, h], D[b, h] = r
+            dq[b, :, h], gk, gv, o[b, :, h], lse[b, h], D[b, h] = r
+            dk[b, :, hk] += gk
+            dv[b, :, hk] += gv
     return dq, dk, dv, o, lse, D

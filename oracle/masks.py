@@ -172,23 +172,28 @@ def pair_lists(table: np.ndarray, Skv: int, Bk: int = 128):
     return counts, costs, lists
 
 
-def unit_order(counts: np.ndarray, H: int) -> np.ndarray:
-    """Work units (b, h, tile), numbered u = (b*H + h)*nT + tile, ordered by
-    (b, h) ascending and, within one (b, h), by cost (non-empty tiles of the
-    unit's q-tile pair or k-tile column) descending, ties by tile ascending.  Within a head
-    this is the longest-processing-time-first order that balances units by
-    work rather than by position (the sparsity-aware balancing the FlashMask-3
-    page names in «Ключевые факты», applied to one GPU's work units); keeping
-    heads in order makes the units that run at the same time share one head.
-    ``counts`` is [B][Hm][nT]; head h reads mask head 0 if Hm == 1 else h."""
+def unit_order(counts: np.ndarray, H: int, G: int = 1) -> np.ndarray:
+    """Work units (b, h, tile), numbered u = (b*Hu + h)*nT + tile with Hu = H / G,
+    ordered by (b, h) ascending and, within one (b, h), by cost (non-empty
+    tiles of the unit's q-tile pair, k-tile column or q-tile row) descending,
+    ties by tile ascending.  Within a head this is the
+    longest-processing-time-first order that balances units by work rather
+    than by position (the sparsity-aware balancing the FlashMask-3 page names
+    in «Ключевые факты», applied to one GPU's work units); keeping heads in
+    order makes the units that run at the same time share one head.
+    ``counts`` is [B][Hm][nT]; query head h reads mask head 0 if Hm == 1 else h.
+    G > 1: the units belong to K/V heads shared by G query heads (grouped-query
+    attention; unit head h covers query heads h*G .. h*G+G-1) and a unit's cost
+    is the sum of its query heads' counts."""
     B, Hm, nT = counts.shape
+    Hu = H // G
     units = []
     for b in range(B):
-        for h in range(H):
-            hm = 0 if Hm == 1 else h
+        for h in range(Hu):
             for t in range(nT):
-                u = (b * H + h) * nT + t
-                units.append(((b, h), -int(counts[b, hm, t]), u))
+                cost = sum(int(counts[b, 0 if Hm == 1 else h * G + j, t]) for j in range(G))
+                u = (b * Hu + h) * nT + t
+                units.append(((b, h), -cost, u))
     units.sort()
     return np.array([u for _, _, u in units], dtype=np.int32)
 

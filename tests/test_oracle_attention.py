@@ -198,3 +198,62 @@ def test_skip_hidden_columns_changes_nothing(name):
         assert np.allclose(x, y, rtol=0, atol=1e-12, equal_nan=True)
     fo = oa.forward_head(q[0, :, 0], k[0, :, 0], v[0, :, 0], b, 0.3, slice_rows=50, skip_hidden=True)
     assert np.allclose(fo[0], a[3], rtol=0, atol=1e-12)
+
+
+def _gqa_inputs(S, H, Hkv, d, seed):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((1, S, H, d))
+    k = rng.standard_normal((1, S, Hkv, d))
+    v = rng.standard_normal((1, S, Hkv, d))
+    do = rng.standard_normal((1, S, H, d))
+    # a different mask per query head, so a wrong mask-head mapping shows too
+    names = ["causal", "sliding_window", "full", "prefix_lm", "causal", "full"]
+    b = np.stack([np.stack([np.asarray(x) for x in gen.make_mask(names[h % len(names)], S)])
+                  for h in range(H)], axis=1)[:, None]  # [4][1][H][S]
+    return q, k, v, do, b
+
+
+def test_gqa_equals_mha_with_repeated_kv():
+    """Grouped-query attention equals multi-head attention on K/V repeated so
+    that query head h sees copy h // G (consecutive query heads share a K/V
+    head); dQ agrees, and a K/V head's dK, dV are the sums of its copies'."""
+    S, H, Hkv, d, scale = 48, 6, 2, 8, 0.5
+    G = H // Hkv
+    q, k, v, do, b = _gqa_inputs(S, H, Hkv, d, 11)
+    kr, vr = np.repeat(k, G, axis=2), np.repeat(v, G, axis=2)
+    o_g, l_g = oa.forward(q, k, v, b, scale)
+    o_m, l_m = oa.forward(q, kr, vr, b, scale)
+    assert np.allclose(o_g, o_m, rtol=0, atol=1e-13) and np.allclose(l_g, l_m, rtol=0, atol=1e-13)
+    dq_g, dk_g, dv_g, *_ = oa.backward(q, k, v, do, b, scale)
+    dq_m, dk_m, dv_m, *_ = oa.backward(q, kr, vr, do, b, scale)
+    assert np.allclose(dq_g, dq_m, rtol=0, atol=1e-12)
+    assert np.allclose(dk_g, dk_m.reshape(1, S, Hkv, G, d).sum(axis=3), rtol=0, atol=1e-12)
+    assert np.allclose(dv_g, dv_m.reshape(1, S, Hkv, G, d).sum(axis=3), rtol=0, atol=1e-12)
+    # the other plausible mapping (h % Hkv) differs on this input
+    kw = np.concatenate([k] * G, axis=2)
+    o_w, _ = oa.forward(q, kw, np.concatenate([v] * G, axis=2), b, scale)
+    assert not np.allclose(o_g, o_w, atol=1e-6)
+
+
+def test_gqa_gradients_by_finite_differences():
+    """dK and dV of shared K/V heads against central differences of
+    sum(O * dO): independent of the group-sum rule."""
+    S, H, Hkv, d, scale = 16, 4, 2, 4, 0.6
+    q, k, v, do, b = _gqa_inputs(S, H, Hkv, d, 12)
+    _, dk, dv, *_ = oa.backward(q, k, v, do, b, scale)
+
+    def loss(kk, vv):
+        o, _ = oa.forward(q, kk, vv, b, scale)
+        return float((o * do).sum())
+
+    eps = 1e-6
+    for X, Gr, which in ((k, dk, 0), (v, dv, 1)):
+        num = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            Xp, Xm = X.copy(), X.copy()
+            Xp[idx] += eps
+            Xm[idx] -= eps
+            num[idx] = ((loss(Xp, v) - loss(Xm, v)) if which == 0 else
+                        (loss(k, Xp) - loss(k, Xm))) / (2 * eps)
+        rel = np.abs(num - Gr).max() / np.abs(Gr).max()
+        assert rel < 1e-6, (which, rel)

@@ -245,6 +245,20 @@ def test_lists_and_unit_order():
             cost[a] > cost[a + 1] or (cost[a] == cost[a + 1] and order[a] < order[a + 1])))
 
 
+def test_unit_order_for_shared_kv_heads_by_hand():
+    """Units of K/V heads shared by G = 2 query heads: a unit's cost sums its
+    two query heads' counts.  counts [1][4][3] (per-head masks):
+        query head 0: 1 3 0    query head 1: 2 0 0    -> unit head 0 costs 3 3 0
+        query head 2: 0 1 1    query head 3: 0 0 2    -> unit head 1 costs 0 1 3
+    so the order is 0, 1, 2 (ties by index) then 3+2, 3+1, 3+0."""
+    counts = np.array([[[1, 3, 0], [2, 0, 0], [0, 1, 1], [0, 0, 2]]], dtype=np.int32)
+    assert om.unit_order(counts, 4, 2).tolist() == [0, 1, 2, 5, 4, 3]
+    # one mask for all heads: each unit costs G times its column
+    one = np.array([[[1, 3, 2]]], dtype=np.int32)
+    assert om.unit_order(one, 4, 2).tolist() == [1, 2, 0, 4, 5, 3]
+    assert om.unit_order(one, 4, 1).tolist() == [1, 2, 0, 4, 5, 3, 7, 8, 6, 10, 11, 9]
+
+
 def _table_of(b, S):
     bounds = np.stack([np.stack([np.asarray(x)[None]]) for x in b])  # [4][1][1][S]
     return om.tile_table(bounds, S)
