@@ -49,7 +49,11 @@ PER_MASK_POINTS = (
       "global_sliding", "qk_sparse", "block_sparse"), {}),
     ("long_128k", 1, 8, 131072, 128, ("causal_document_window",), {"window": 8192}),
     ("localize_64k", 1, 16, 65536, 128, ("causal_document",), {}),
+    ("long_128k_gqa", 1, 8, 131072, 128, ("causal_document_window",), {"window": 8192}),
 )
+# points run with fewer K/V heads than query heads (grouped-query attention):
+# the 128K workload's 8 query heads over 2 K/V heads
+GQA_POINTS = {"long_128k_gqa": ("long_128k", 2)}
 
 
 # GEMMs of 2 * d flop per visible entry in each attention kernel: the
@@ -330,6 +334,9 @@ def run_per_mask(args, fm):
             continue
         scale = d ** -0.5
         q, k, v, do = qkv_do(B, S, S, H, d, seed=0, device="cuda")
+        Hkv = GQA_POINTS[name][1] if name in GQA_POINTS else H
+        if Hkv != H:
+            k, v = k[:, :, :Hkv].contiguous(), v[:, :, :Hkv].contiguous()
         for mask in masks:
             bounds = mask_bounds(mask, B, S, device="cuda", **params)
             bounds_np = bounds.cpu().numpy()
@@ -376,7 +383,7 @@ def run_per_mask(args, fm):
             bwd_ms = sum(ev[4 * i + 1].elapsed_time(ev[4 * i + 2]) for i in range(n)) / n
             ff, fb = 4.0 * d * n_vis, 10.0 * d * n_vis
             tot = (ff + fb) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12
-            row = {"workload": name, "mask": mask, "B": B, "H": H, "S": S, "d": d,
+            row = {"workload": name, "mask": mask, "B": B, "H": H, "Hkv": Hkv, "S": S, "d": d,
                    "visible_entries": n_vis,
                    "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4),
                    "fwd_tflops": round(ff / (fwd_ms * 1e-3) / 1e12, 1),

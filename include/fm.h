@@ -56,11 +56,17 @@ typedef enum {
   FM_ERR_TIMEOUT = 6       /* a device-side wait expired; outputs are undefined */
 } fm_status;
 
-/* Problem description.  Hm is 1 or H; d (head_dim) is 64 or 128; Sq, Skv >= 1.
- * Strides are in elements, for the (b, s, h) axes.  For the backward pass
- * dO uses o_stride, dQ uses q_stride, dK uses k_stride and dV uses v_stride. */
+/* Problem description.  H query heads; Hkv K/V heads (grouped-query
+ * attention, listed as a key feature on the ROCm page): Hkv divides H, query
+ * head h reads K/V head h / (H / Hkv), and the backward's dK and dV of a K/V
+ * head sum over its query heads; Hkv = 0 means Hkv = H (multi-head).  q, o,
+ * dO, dQ have H heads, k, v, dK, dV have Hkv.  Hm (mask heads, per query
+ * head) is 1 or H; d (head_dim) is 64 or 128; Sq, Skv >= 1.  Strides are in
+ * elements, for the (b, s, h) axes.  For the backward pass dO uses o_stride,
+ * dQ uses q_stride, dK uses k_stride and dV uses v_stride. */
 typedef struct {
   int B, H, Hm, Sq, Skv, d;
+  int Hkv;
   int64_t q_stride[3];
   int64_t k_stride[3];
   int64_t v_stride[3];
@@ -83,7 +89,9 @@ typedef struct {
   size_t col_list;   /* int32 [B][Hm][nK][nQ]: ascending q-tiles of each column       */
   size_t fwd_order;  /* int32 [B*H*nP], nP = ceil(nQ/2): forward units u=(b*H+h)*nP+p
                         (q-tiles 2p and 2p+1), longest first                       */
-  size_t bwd_order;  /* int32 [B*H*nK]: backward units u=(b*H+h)*nK+kj, longest first */
+  size_t bwd_order;  /* int32 [B*Hkv*nK]: dK/dV units u=(b*Hkv+hk)*nK+kj, longest
+                        first; a unit walks the k-tile column of each of the H/Hkv
+                        query heads that read K/V head hk, and costs their sum */
   size_t row_mask;   /* int32 [B][Hm][nQ]: first visibility-mask slot of the row's partial
                         tiles (consecutive in list order), -1 if none              */
   size_t masks;      /* uint8 [cap][128][16], cap = min(B*Hm*nQ*nK, 65536): per partial

@@ -42,11 +42,12 @@ def _strides(t):
 
 
 def make_desc(q, k, v=None, o=None, Hm: int = 1) -> FmDesc:
-    """Problem description from BSHD tensors (v defaults to k's strides, o to q's)."""
+    """Problem description from BSHD tensors (v defaults to k's strides, o to q's).
+    k and v may have fewer heads than q (grouped-query attention)."""
     B, Sq, H, d = q.shape
-    Skv = k.shape[1]
+    Skv, Hkv = k.shape[1], k.shape[2]
     D = FmDesc()
-    D.B, D.H, D.Hm, D.Sq, D.Skv, D.d = B, H, Hm, Sq, Skv, d
+    D.B, D.H, D.Hm, D.Sq, D.Skv, D.d, D.Hkv = B, H, Hm, Sq, Skv, d, Hkv
     D.q_stride[:] = _strides(q)
     D.k_stride[:] = _strides(k)
     D.v_stride[:] = _strides(v if v is not None else k)

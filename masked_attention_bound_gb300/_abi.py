@@ -21,6 +21,7 @@ STATUS_NAMES = {
 class FmDesc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("Hm", ctypes.c_int),
                 ("Sq", ctypes.c_int), ("Skv", ctypes.c_int), ("d", ctypes.c_int),
+                ("Hkv", ctypes.c_int),
                 ("q_stride", ctypes.c_int64 * 3), ("k_stride", ctypes.c_int64 * 3),
                 ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3)]
 

@@ -38,12 +38,15 @@ fm_status make_plan(const fm_desc* desc, int mode, Plan* p, size_t limit) {
   const fm_desc& D = *desc;
   if (D.B < 1 || D.H < 1 || D.Sq < 1 || D.Skv < 1 || D.d < 1) return FM_ERR_INVALID;
   if (D.Hm != 1 && D.Hm != D.H) return FM_ERR_INVALID;
+  const int Hkv = D.Hkv == 0 ? D.H : D.Hkv;
+  if (Hkv < 1 || Hkv > D.H || D.H % Hkv != 0) return FM_ERR_INVALID;
   if (D.d != 64 && D.d != 128) return FM_ERR_UNSUPPORTED;
   if (!strides_ok(D.q_stride) || !strides_ok(D.k_stride) || !strides_ok(D.v_stride) ||
       !strides_ok(D.o_stride))
     return FM_ERR_INVALID;
   if (D.Sq > (1 << 24) || D.Skv > (1 << 24)) return FM_ERR_UNSUPPORTED;
   p->B = D.B; p->H = D.H; p->Hm = D.Hm; p->Sq = D.Sq; p->Skv = D.Skv; p->d = D.d;
+  p->Hkv = Hkv; p->G = D.H / Hkv;
   p->nQ = ceil_div(D.Sq, kTile);
   p->nK = ceil_div(D.Skv, kTile);
   p->nP = ceil_div(p->nQ, 2);

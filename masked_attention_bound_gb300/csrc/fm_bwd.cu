@@ -123,6 +123,7 @@ constexpr int UNIT_RING = 4;
 
 struct BwdParams {
   int B, H, Hm, Sq, Skv, nQ, nK, n_units;
+  int Hkv, G;  // K/V heads; query heads per K/V head (head h reads K/V head h / G)
   float scale, scale_log2;
   const int32_t* bounds[4];
   const int32_t* list_count;  // units' tile counts: columns (dK/dV) or rows (dQ)
@@ -274,16 +275,20 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     const bool ok = wait(b, parity);
     return __all_sync(0xffffffffu, ok);
   };
-  // unit u = (b*H + h)*nK + kj -> its column of q-tiles
-  auto unit_info = [&](int idx, int& b, int& h, int& kj, const int32_t*& list) {
+  // k-tile column kj of query head h (its mask head)
+  auto col_of = [&](int b, int h, int kj) { return (b * P.Hm + (P.Hm == 1 ? 0 : h)) * P.nK + kj; };
+  // unit u = (b*Hkv + hk)*nK + kj -> the columns of q-tiles of the G query
+  // heads h = hk*G + j that read K/V head hk, walked one head after another;
+  // returns their total tile count
+  auto unit_info = [&](int idx, int& b, int& hk, int& kj) {
     const int u = P.order[idx];
     const int bh = u / P.nK;
     kj = u - bh * P.nK;
-    b = bh / P.H;
-    h = bh - b * P.H;
-    const int col = (b * P.Hm + (P.Hm == 1 ? 0 : h)) * P.nK + kj;
-    list = P.list + static_cast<size_t>(col) * P.nQ;
-    return P.list_count[col];
+    b = bh / P.Hkv;
+    hk = bh - b * P.Hkv;
+    int n = 0;
+    for (int j = 0; j < P.G; ++j) n += P.list_count[col_of(b, hk * P.G + j, kj)];
+    return n;
   };
   // the n-th claimed unit (-1: none left, or the launch was aborted).
   // claimed_one: one thread of the warp reads and releases the ring slot;
@@ -317,9 +322,8 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       while (true) {
         const int idx = claimed_one(cn);
         if (idx < 0) break;
-        int b, h, kj;
-        const int32_t* list;
-        const int n = unit_info(idx, b, h, kj, list);
+        int b, h, kj;  // h: the K/V head
+        const int n = unit_info(idx, b, h, kj);
         if (n == 0) continue;
         if (un > 0 && !wait(A_KEMPTY, (un - 1) & 1)) break;
         mbar_arrive_expect_tx(bar(A_KFULL), C::TILE);
@@ -360,27 +364,33 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         ring[r] = idx;
         mbar_arrive(bar(A_UFULL0 + r));
         if (idx < 0) break;
-        int b, h, kj;
-        const int32_t* list;
-        const int n = unit_info(idx, b, h, kj, list);
-        const size_t bh_row = (static_cast<size_t>(b) * P.H + h) * rows_pad;
-        for (int t = 0; t < n; ++t, ++it) {
-          const int qi = list[t] >> 2;
-          const int st = it & 1;
-          const uint32_t use = it >> 1;
-          if (use > 0 && !wait(A_QEMPTY0 + st, (use - 1) & 1)) { ok = false; break; }
-          const uint32_t fb = bar(A_QFULL0 + st);
-          mbar_arrive_expect_tx(fb, 2 * C::TILE + 1024);
-          const uint32_t sQ = sbase + C::OFF_Q + st * C::TILE;
-          const uint32_t sDO = sbase + C::OFF_DO + st * C::TILE;
+        int b, hk, kj;
+        unit_info(idx, b, hk, kj);
+        // the q-tile columns of the G query heads reading K/V head hk
+        for (int j = 0; j < P.G && ok; ++j) {
+          const int h = hk * P.G + j;
+          const int col = col_of(b, h, kj);
+          const int32_t* list = P.list + static_cast<size_t>(col) * P.nQ;
+          const int nj = P.list_count[col];
+          const size_t bh_row = (static_cast<size_t>(b) * P.H + h) * rows_pad;
+          for (int t = 0; t < nj; ++t, ++it) {
+            const int qi = list[t] >> 2;
+            const int st = it & 1;
+            const uint32_t use = it >> 1;
+            if (use > 0 && !wait(A_QEMPTY0 + st, (use - 1) & 1)) { ok = false; break; }
+            const uint32_t fb = bar(A_QFULL0 + st);
+            mbar_arrive_expect_tx(fb, 2 * C::TILE + 1024);
+            const uint32_t sQ = sbase + C::OFF_Q + st * C::TILE;
+            const uint32_t sDO = sbase + C::OFF_DO + st * C::TILE;
 #pragma unroll
-          for (int s = 0; s < D / 64; ++s) {
-            tma_load_4d(sQ + s * 16384, &tmQ, fb, s * 64, h, qi * kTile, b);
-            tma_load_4d(sDO + s * 16384, &tmDO, fb, s * 64, h, qi * kTile, b);
+            for (int s = 0; s < D / 64; ++s) {
+              tma_load_4d(sQ + s * 16384, &tmQ, fb, s * 64, h, qi * kTile, b);
+              tma_load_4d(sDO + s * 16384, &tmDO, fb, s * 64, h, qi * kTile, b);
+            }
+            const uint32_t sLD = sbase + C::OFF_LD + st * 1024;
+            bulk_load(sLD, P.lse_log2 + bh_row + qi * kTile, 512, fb);
+            bulk_load(sLD + 512, P.delta + bh_row + qi * kTile, 512, fb);
           }
-          const uint32_t sLD = sbase + C::OFF_LD + st * 1024;
-          bulk_load(sLD, P.lse_log2 + bh_row + qi * kTile, 512, fb);
-          bulk_load(sLD + 512, P.delta + bh_row + qi * kTile, 512, fb);
         }
       }
       // drain every issued copy before exit
@@ -421,8 +431,7 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         const int idx = claimed_one(cn);
         if (idx < 0) break;
         int b, h, kj;
-        const int32_t* list;
-        const int n = unit_info(idx, b, h, kj, list);
+        const int n = unit_info(idx, b, h, kj);
         if (n == 0) continue;
         if (!wait(A_KFULL, un & 1)) break;
         for (int t = 0; t < n; ++t, ++it) {
@@ -570,14 +579,13 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     while (ok) {
       const int idx = claimed_all(cn);
       if (idx < 0) break;
-      int b, h, kj;
-      const int32_t* list;
-      const int n = unit_info(idx, b, h, kj, list);
+      int b, hk, kj;  // hk: the K/V head
+      const int n = unit_info(idx, b, hk, kj);
       const int key = kj * kTile + r;
       __nv_bfloat16* dk_row = P.out0 + b * P.s0[0] + static_cast<int64_t>(key) * P.s0[1] +
-                              h * P.s0[2] + half * (D / 2);
+                              hk * P.s0[2] + half * (D / 2);
       __nv_bfloat16* dv_row = P.out1 + b * P.s1[0] + static_cast<int64_t>(key) * P.s1[1] +
-                              h * P.s1[2] + half * (D / 2);
+                              hk * P.s1[2] + half * (D / 2);
       if (n == 0) {
         if (key < P.Skv) {
           const uint4 z = make_uint4(0, 0, 0, 0);
@@ -589,18 +597,31 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         }
         continue;
       }
-      // this thread's key column bounds (beyond Skv: hidden from every row)
+      // this thread's key column bounds (beyond Skv: hidden from every row),
+      // read again when the walk moves to a query head with its own mask
       int lts = 0, lte = 0x7fffffff, uts = 0, ute = 0;
-      if (key < P.Skv) {
-        const size_t at = static_cast<size_t>(b * P.Hm + (P.Hm == 1 ? 0 : h)) * P.Skv + key;
-        lts = __ldg(P.bounds[0] + at);
-        lte = __ldg(P.bounds[1] + at);
-        uts = __ldg(P.bounds[2] + at);
-        ute = __ldg(P.bounds[3] + at);
-      }
       const bool key_ragged = (kj == P.nK - 1) && (P.Skv & (kTile - 1));
+      // the walk over the group's query heads: head j's column `list`, nj
+      // tiles, position i in it
+      int j = -1, nj = 0, i = 0;
+      const int32_t* list = nullptr;
       for (int t = 0; t < n; ++t, ++it) {
-        const int e = list[t];
+        while (i == nj) {  // next query head with tiles (n counts them all)
+          ++j;
+          const int h = hk * P.G + j;
+          const int col = col_of(b, h, kj);
+          list = P.list + static_cast<size_t>(col) * P.nQ;
+          nj = P.list_count[col];
+          i = 0;
+          if ((j == 0 || P.Hm > 1) && key < P.Skv) {
+            const size_t at = static_cast<size_t>(b * P.Hm + (P.Hm == 1 ? 0 : h)) * P.Skv + key;
+            lts = __ldg(P.bounds[0] + at);
+            lte = __ldg(P.bounds[1] + at);
+            uts = __ldg(P.bounds[2] + at);
+            ute = __ldg(P.bounds[3] + at);
+          }
+        }
+        const int e = list[i++];
         const int qi = e >> 2;
         const bool partial = ((e & 3) == CLS_PARTIAL) || key_ragged;
         const int st = it & 1;
@@ -693,7 +714,7 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       if (!ok) break;
       pending = true;
       pb = b;
-      ph = h;
+      ph = hk;
       pkj = kj;
       ++un;
     }
@@ -1001,10 +1022,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             mbar_arrive_expect_tx(rb, 2 * C::TILE);
 #pragma unroll
             for (int x = 0; x < D / 64; ++x) {
-              tma_load_4d(sbase + C::OFF_K + ks * C::TILE + x * 16384, &tmK, rb, x * 64, h,
-                          kj * kTile, b);
-              tma_load_4d(sbase + C::OFF_V + vs * C::TILE + x * 16384, &tmV, rb, x * 64, h,
-                          kj * kTile, b);
+              tma_load_4d(sbase + C::OFF_K + ks * C::TILE + x * 16384, &tmK, rb, x * 64,
+                          h / P.G, kj * kTile, b);
+              tma_load_4d(sbase + C::OFF_V + vs * C::TILE + x * 16384, &tmV, rb, x * 64,
+                          h / P.G, kj * kTile, b);
             }
           }
         }
@@ -1314,13 +1335,14 @@ static fm_status launch_bwd_d(const Plan& p, const fm_desc& desc, const TensorAr
   }
   CUtensorMap tq, tk, tv, tdo;
   if (!make_tmap_bshd(&tq, t.q, p.B, p.Sq, p.H, D, desc.q_stride, 128) ||
-      !make_tmap_bshd(&tk, t.k, p.B, p.Skv, p.H, D, desc.k_stride, 128) ||
-      !make_tmap_bshd(&tv, t.v, p.B, p.Skv, p.H, D, desc.v_stride, 128) ||
+      !make_tmap_bshd(&tk, t.k, p.B, p.Skv, p.Hkv, D, desc.k_stride, 128) ||
+      !make_tmap_bshd(&tv, t.v, p.B, p.Skv, p.Hkv, D, desc.v_stride, 128) ||
       !make_tmap_bshd(&tdo, t.dout, p.B, p.Sq, p.H, D, desc.o_stride, 128))
     return FM_ERR_CUDA;
   const TestHooks th = test_hooks();
   BwdParams P{};
   P.B = p.B; P.H = p.H; P.Hm = p.Hm; P.Sq = p.Sq; P.Skv = p.Skv; P.nQ = p.nQ; P.nK = p.nK;
+  P.Hkv = p.Hkv; P.G = p.G;
   P.scale = t.scale;
   P.scale_log2 = t.scale * 1.4426950408889634f;
   for (int i = 0; i < 4; ++i) P.bounds[i] = t.bounds[i];
@@ -1332,7 +1354,7 @@ static fm_status launch_bwd_d(const Plan& p, const fm_desc& desc, const TensorAr
   {
     // dK, dV over k-tile columns
     BwdParams A = P;
-    A.n_units = p.B * p.H * p.nK;
+    A.n_units = p.B * p.Hkv * p.nK;
     A.list_count = reinterpret_cast<const int32_t*>(ws + p.L.col_count);
     A.list = reinterpret_cast<const int32_t*>(ws + p.L.col_list);
     A.order = reinterpret_cast<const int32_t*>(ws + p.L.bwd_order);

@@ -92,6 +92,7 @@ constexpr uint32_t E_END = 256u;
 
 struct FwdParams {
   int B, H, Hm, Sq, Skv, nQ, nK, nP, n_units;
+  int G;             // query heads per K/V head: head h reads K/V head h / G
   float scale_log2;  // scale * log2(e)
   const int32_t* bounds[4];
   const int4* pair_info;    // per pair row: entries, tiles of 2p, tiles of 2p+1, sum
@@ -390,7 +391,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
           for (int x = 0; x < C::SLABS; ++x)
             tma_load_4d(sbase + C::OFF_K + st * C::TILE + x * 16384, &tmK, bar(B_KFULL0 + st),
-                        x * 64, u.h, kj * kTile, u.b);
+                        x * 64, u.h / P.G, kj * kTile, u.b);
           // a slot whose tile here is not partial never reads this stage's bits
           if (ca != CLS_PARTIAL) mbar_arrive_count(bar(B_MEMPTY0 + st), 4);
           if (cb != CLS_PARTIAL) mbar_arrive_count(bar(B_MEMPTY0 + st), 4);
@@ -440,7 +441,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
           for (int x = 0; x < C::SLABS; ++x)
             tma_load_4d(sbase + C::OFF_V + st * C::TILE + x * 16384, &tmV, bar(B_VFULL0 + st),
-                        x * 64, u.h, kj * kTile, u.b);
+                        x * 64, u.h / P.G, kj * kTile, u.b);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -726,11 +727,12 @@ static fm_status launch_fwd_d(const Plan& p, const fm_desc& desc, const TensorAr
   using C = FwdCfg<D>;
   CUtensorMap tq, tk, tv;
   if (!make_tmap_bshd(&tq, t.q, p.B, p.Sq, p.H, D, desc.q_stride, 128) ||
-      !make_tmap_bshd(&tk, t.k, p.B, p.Skv, p.H, D, desc.k_stride, 128) ||
-      !make_tmap_bshd(&tv, t.v, p.B, p.Skv, p.H, D, desc.v_stride, 128))
+      !make_tmap_bshd(&tk, t.k, p.B, p.Skv, p.Hkv, D, desc.k_stride, 128) ||
+      !make_tmap_bshd(&tv, t.v, p.B, p.Skv, p.Hkv, D, desc.v_stride, 128))
     return FM_ERR_CUDA;
   FwdParams P{};
   P.B = p.B; P.H = p.H; P.Hm = p.Hm; P.Sq = p.Sq; P.Skv = p.Skv; P.nQ = p.nQ; P.nK = p.nK;
+  P.G = p.G;
   P.nP = p.nP;
   P.n_units = p.B * p.H * p.nP;
   P.scale_log2 = t.scale * 1.4426950408889634f;

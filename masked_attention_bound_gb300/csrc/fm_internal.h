@@ -19,6 +19,7 @@ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 struct Plan {
   int B, H, Hm, Sq, Skv, d, nQ, nK;
+  int Hkv, G;    // K/V heads and query heads per K/V head (H = G * Hkv)
   int nP;        // q-tile pairs, ceil(nQ / 2)
   int mask_cap;  // forward: slots in the visibility-mask region
   fm_ws_layout L;

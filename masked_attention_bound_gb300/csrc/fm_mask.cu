@@ -298,19 +298,29 @@ __global__ void __launch_bounds__(256) classify_cols_kernel(const int32_t* __res
 // counts[b][hm][t] in [0, maxc] descending, ties by t ascending (longest
 // first).  One CTA per (b, h): histogram, scan in descending cost, stable
 // scatter by one warp in t order.
+// One block per (b, unit head h); Hu = H / G unit heads.  G > 1: the units
+// belong to K/V heads, each shared by query heads h*G .. h*G+G-1, and a
+// unit's cost is the sum of their counts (maxc covers the sum).
 __global__ void __launch_bounds__(256) order_kernel(const int32_t* __restrict__ counts,
-                                                    int stride, int H, int Hm, int nT, int maxc,
-                                                    int32_t* order) {
+                                                    int stride, int H, int Hm, int G, int nT,
+                                                    int maxc, int32_t* order) {
   extern __shared__ int sh[];
   int* hist = sh;             // maxc + 1
   int* cst = sh + maxc + 1;   // nT costs of this (b, h)
   __shared__ int wsum[8];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int Hu = H / G;
   const int bh = blockIdx.x;
-  const int b = bh / H, h = bh - b * H;
-  const int32_t* src = counts + static_cast<size_t>(b * Hm + (Hm == 1 ? 0 : h)) * nT * stride;
+  const int b = bh / Hu, h = bh - b * Hu;
   for (int i = tid; i <= maxc; i += blockDim.x) hist[i] = 0;
-  for (int t = tid; t < nT; t += blockDim.x) cst[t] = src[static_cast<size_t>(t) * stride];
+  for (int t = tid; t < nT; t += blockDim.x) {
+    int c = 0;
+    for (int j = 0; j < G; ++j) {
+      const int hm = Hm == 1 ? 0 : h * G + j;
+      c += counts[(static_cast<size_t>(b * Hm + hm) * nT + t) * stride];
+    }
+    cst[t] = c;
+  }
   __syncthreads();
   for (int t = tid; t < nT; t += blockDim.x) atomicAdd(&hist[cst[t]], 1);
   __syncthreads();
@@ -436,7 +446,7 @@ cudaError_t launch_order(const Plan& p, char* ws, int which, cudaStream_t s) {
   // forward: q-tile pairs, cost = the non-empty tiles of both rows
   // (pair_info[.][3]); dK/dV: k-tile columns, dQ: q-tile rows, cost = their
   // non-empty tiles
-  int nT, maxc, stride = 1;
+  int nT, maxc, stride = 1, G = 1;
   const int32_t* counts;
   int32_t* order;
   if (which == ORDER_PAIRS) {
@@ -444,7 +454,8 @@ cudaError_t launch_order(const Plan& p, char* ws, int which, cudaStream_t s) {
     counts = reinterpret_cast<const int32_t*>(ws + p.L.pair_info) + 3;
     order = reinterpret_cast<int32_t*>(ws + p.L.fwd_order);
   } else if (which == ORDER_COLS) {
-    nT = p.nK; maxc = p.nQ;
+    // dK/dV units belong to K/V heads: G query heads' columns each
+    nT = p.nK; maxc = p.G * p.nQ; G = p.G;
     counts = reinterpret_cast<const int32_t*>(ws + p.L.col_count);
     order = reinterpret_cast<int32_t*>(ws + p.L.bwd_order);
   } else {
@@ -459,7 +470,8 @@ cudaError_t launch_order(const Plan& p, char* ws, int which, cudaStream_t s) {
                                        static_cast<int>(limit));
   if (e != cudaSuccess) return e;
   prof_begin(K_ORDER, s);
-  order_kernel<<<p.B * p.H, 256, smem, s>>>(counts, stride, p.H, p.Hm, nT, maxc, order);
+  order_kernel<<<p.B * (p.H / G), 256, smem, s>>>(counts, stride, p.H, p.Hm, G, nT, maxc,
+                                                 order);
   prof_end(K_ORDER, s);
   return cudaGetLastError();
 }

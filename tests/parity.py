@@ -55,11 +55,13 @@ def compare_fwd(q, k, v, bounds, scale, o, lse, heads=None, rows=None, seed=0, s
     """Check O and LSE of the given (b, h) pairs (default all) on ``rows``
     sampled query rows per head (default all).  Returns the worst errors."""
     B, Sq, H, _ = q.shape
+    Hkv = k.shape[2]
     heads = [(b, h) for b in range(B) for h in range(H)] if heads is None else heads
     worst_o = worst_l = 0.0
     for n, (b, h) in enumerate(heads):
         r = sample_rows(Sq, rows, seed + n)
-        ro, rl = oa.forward_head(head_slice(q, b, h), head_slice(k, b, h), head_slice(v, b, h),
+        hk = oa.kv_head(h, H, Hkv)
+        ro, rl = oa.forward_head(head_slice(q, b, h), head_slice(k, b, hk), head_slice(v, b, hk),
                                  mask_vec(bounds, b, h), scale, rows=r, slice_rows=slice_rows,
                                  skip_hidden=True)
         go = o[b, r, h].float().cpu().numpy()
@@ -76,21 +78,34 @@ def compare_fwd(q, k, v, bounds, scale, o, lse, heads=None, rows=None, seed=0, s
 
 
 def compare_bwd(q, k, v, do, bounds, scale, dq, dk, dv, heads=None, slice_rows=1024):
-    """Check dQ, dK, dV of the given (b, h) pairs in full against the oracle."""
+    """Check dQ of the given (b, h) query-head pairs (default all), and dK, dV
+    of the K/V heads they read, in full against the oracle.  With fewer K/V
+    heads than query heads, a K/V head's reference gradients sum over all the
+    query heads that read it (oracle.attention, grouped-query attention)."""
     B, Sq, H, _ = q.shape
+    Hkv = k.shape[2]
+    G = H // Hkv
     heads = [(b, h) for b in range(B) for h in range(H)] if heads is None else heads
     worst = {"dq": 0.0, "dk": 0.0, "dv": 0.0}
-    for b, h in heads:
-        rq, rk, rv, *_ = oa.backward_head(head_slice(q, b, h), head_slice(k, b, h),
-                                          head_slice(v, b, h), head_slice(do, b, h),
-                                          mask_vec(bounds, b, h), scale, slice_rows=slice_rows,
-                                          skip_hidden=True)
-        for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
-            g = got[b, :, h].float().cpu().numpy()
-            err = float(np.abs(g - ref).max())
-            scale_ref = float(np.abs(ref).max())
-            rel = err / scale_ref if scale_ref > 0 else err
-            worst[name] = max(worst[name], rel)
-            assert err <= GRAD_REL * max(scale_ref, GRAD_FLOOR), \
-                f"{name} error {err} vs max|ref| {scale_ref} at (b={b}, h={h})"
+
+    def check(name, g, ref, b, h):
+        err = float(np.abs(g - ref).max())
+        scale_ref = float(np.abs(ref).max())
+        rel = err / scale_ref if scale_ref > 0 else err
+        worst[name] = max(worst[name], rel)
+        assert err <= GRAD_REL * max(scale_ref, GRAD_FLOOR), \
+            f"{name} error {err} vs max|ref| {scale_ref} at (b={b}, head={h})"
+
+    for b, hk in sorted({(b, oa.kv_head(h, H, Hkv)) for b, h in heads}):
+        sk = sv = 0.0
+        for h in range(hk * G, hk * G + G):
+            rq, rk, rv, *_ = oa.backward_head(head_slice(q, b, h), head_slice(k, b, hk),
+                                              head_slice(v, b, hk), head_slice(do, b, h),
+                                              mask_vec(bounds, b, h), scale, slice_rows=slice_rows,
+                                              skip_hidden=True)
+            if (b, h) in heads:
+                check("dq", dq[b, :, h].float().cpu().numpy(), rq, b, h)
+            sk, sv = sk + rk, sv + rv
+        check("dk", dk[b, :, hk].float().cpu().numpy(), sk, b, hk)
+        check("dv", dv[b, :, hk].float().cpu().numpy(), sv, b, hk)
     return worst
