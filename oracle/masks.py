@@ -199,6 +199,28 @@ def unit_order(counts: np.ndarray, H: int, G: int = 1) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------
+# packed variable-length batches
+# --------------------------------------------------------------------------
+
+def varlen_bounds(cu_seqlens, causal: bool) -> np.ndarray:
+    """Bounds [4][total] of a packed batch: sequence s holds rows and keys
+    [cu[s], cu[s+1]) of one axis of length total = cu[-1], and a row sees only
+    keys of its own sequence (and, if causal, only keys at or before it).  So
+    key j of sequence [a, b) is seen by rows [j, b) (causal) or [a, b): the
+    lower hidden interval is [b, total), the upper one [0, j) or [0, a).
+    Sequences of length 0 hold nothing.  This is the FlashAttention-2 page's
+    fixed-token batch («Как понимать заявленное ускорение»: 16K tokens per
+    batch) written in the column-bound form of the FlashMask-3 page."""
+    cu = [int(x) for x in cu_seqlens]
+    total = cu[-1]
+    out = np.empty((4, total), dtype=np.int64)
+    for a, b in zip(cu[:-1], cu[1:]):
+        for j in range(a, b):
+            out[:, j] = (b, total, 0, j if causal else a)
+    return out
+
+
+# --------------------------------------------------------------------------
 # localisation to a rank's query chunks
 # --------------------------------------------------------------------------
 

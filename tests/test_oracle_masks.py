@@ -377,3 +377,24 @@ def test_localize_rejects_unsorted_chunks():
         om.localize_bounds(b, [(32, 16), (0, 16)])
     with pytest.raises(ValueError):
         om.localize_bounds(b, [(0, 20), (10, 16)])
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_varlen_bounds_are_the_block_diagonal_mask(causal):
+    """A packed batch's bounds give exactly the block-diagonal mask built
+    entry by entry from the sequence boundaries (zero-length sequences too)."""
+    cu = [0, 5, 5, 17, 18, 40]
+    total = cu[-1]
+    seq = np.empty(total, dtype=int)
+    for s_, (a, b) in enumerate(zip(cu[:-1], cu[1:])):
+        seq[a:b] = s_
+    want = np.zeros((total, total), dtype=bool)  # True = hidden
+    for i in range(total):
+        for j in range(total):
+            want[i, j] = seq[i] != seq[j] or (causal and j > i)
+    b = om.varlen_bounds(cu, causal)
+    assert np.array_equal(om.dense_mask(*b, total), want)
+    # the same as a document mask of those lengths (the input generators')
+    lengths = [y - x for x, y in zip(cu[:-1], cu[1:]) if y > x]
+    g = (gen.causal_document if causal else gen.bidirectional_document)(total, lengths)
+    assert np.array_equal(om.dense_mask(*g, total), want)
