@@ -50,7 +50,29 @@ PER_MASK_POINTS = (
     ("long_128k", 1, 8, 131072, 128, ("causal_document_window",), {"window": 8192}),
     ("localize_64k", 1, 16, 65536, 128, ("causal_document",), {}),
     ("long_128k_gqa", 1, 8, 131072, 128, ("causal_document_window",), {"window": 8192}),
+    # packed variable-length batches of 16K tokens (sequence lengths drawn
+    # U[512, 4096], the last one cut), hidden size 2048: the FlashAttention-2
+    # page's benchmark shape, with d 128 and 64
+    ("varlen_16k_d128", 1, 16, 16384, 128, ("varlen_causal", "varlen_full"), {}),
+    ("varlen_16k_d64", 1, 32, 16384, 64, ("varlen_causal", "varlen_full"), {}),
 )
+
+
+def _point_bounds(fm, mask, B, S, params):
+    """Bounds of one per-mask point: a named mask (fm_inputs), or a packed
+    batch built through fm_varlen_bounds from seeded sequence lengths."""
+    import numpy as np
+    import torch
+
+    from fm_inputs.tensors import mask_bounds
+    if not mask.startswith("varlen_"):
+        return mask_bounds(mask, B, S, device="cuda", **params)
+    rng = np.random.default_rng(0)
+    cu = [0]
+    while cu[-1] < S:
+        cu.append(min(S, cu[-1] + int(rng.integers(512, 4097))))
+    return fm.varlen_bounds(torch.tensor(cu, dtype=torch.int32, device="cuda"),
+                            causal=mask == "varlen_causal")
 # points run with fewer K/V heads than query heads (grouped-query attention):
 # the 128K workload's 8 query heads over 2 K/V heads
 GQA_POINTS = {"long_128k_gqa": ("long_128k", 2)}
@@ -325,7 +347,7 @@ def run_per_mask(args, fm):
     import torch
 
     from fm_inputs.configs import LOCALIZE_RANKS, dual_chunk_map
-    from fm_inputs.tensors import mask_bounds, qkv_do
+    from fm_inputs.tensors import qkv_do
     peak = float(_peaks()[0]["bf16_tflops"])
     stream = torch.cuda.current_stream()
     out = []
@@ -338,7 +360,7 @@ def run_per_mask(args, fm):
         if Hkv != H:
             k, v = k[:, :, :Hkv].contiguous(), v[:, :, :Hkv].contiguous()
         for mask in masks:
-            bounds = mask_bounds(mask, B, S, device="cuda", **params)
+            bounds = _point_bounds(fm, mask, B, S, params)
             bounds_np = bounds.cpu().numpy()
             n_vis = _visible_entries(bounds_np, S, H)
             if name == "localize_64k":

@@ -231,6 +231,21 @@ fm_status fm_localize(const int32_t* bounds, int B, int Hm, int Skv,
                       const int32_t* chunk_start, const int32_t* chunk_len, int n_chunks,
                       int32_t* local_bounds, void* stream);
 
+/* Bounds of a packed variable-length batch: the FlashAttention-2 page's
+ * fixed-token batch («Как понимать заявленное ускорение»: 16K tokens per
+ * batch) in the column-bound form of the FlashMask-3 page.  Sequence s holds
+ * rows and keys [cu_seqlens[s], cu_seqlens[s+1]) of one axis of `total`
+ * tokens; a row sees only keys of its own sequence, and with `causal` only
+ * keys at or before it.  cu_seqlens: device int32 [n_seqs + 1], 0 first,
+ * non-decreasing, `total` last (zero-length sequences allowed).  bounds:
+ * device int32 [4][total] (LTS, LTE, UTS, UTE; the [4][B=1][Hm=1][Skv] layout
+ * of fm_fwd with Sq = Skv = total), written by a kernel on `stream`.  `bad`
+ * (device int, may be null) has 1 or-ed into it if cu_seqlens is not such a
+ * partition; keys then outside every sequence are hidden from all rows.
+ * Returns FM_ERR_INVALID for null pointers or sizes out of range. */
+fm_status fm_varlen_bounds(const int32_t* cu_seqlens, int n_seqs, int total, int causal,
+                           int32_t* bounds, int* bad, void* stream);
+
 /* Kernel timing, for benchmarks.  While enabled, every kernel the library
  * launches is bracketed by a pair of CUDA events recorded on its own stream
  * (event objects are created on first use and reused; no device memory is

@@ -146,6 +146,27 @@ def backward(q, k, v, o, lse, do, bounds, scale, dq=None, dk=None, dv=None, ws=N
     return dq, dk, dv
 
 
+def varlen_bounds(cu_seqlens, total=None, causal=True, stream=None, validate=True):
+    """Bounds [4][1][1][total] of a packed variable-length batch (fm_varlen_bounds):
+    sequence s holds tokens [cu_seqlens[s], cu_seqlens[s+1]) and sees only itself
+    (causally if ``causal``).  ``cu_seqlens``: int32 device tensor [n + 1].
+    ``total`` defaults to cu_seqlens[-1] (a device read).  With ``validate``, a
+    cu_seqlens that is not a partition of [0, total) raises ValueError."""
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens must be a 1-D int32 tensor with at least two entries")
+    cu = cu_seqlens.contiguous()
+    if total is None:
+        total = int(cu[-1].item())
+    out = torch.empty(4, 1, 1, total, dtype=torch.int32, device=cu.device)
+    bad = torch.zeros(1, dtype=torch.int32, device=cu.device) if validate else None
+    check(lib().fm_varlen_bounds(_p(cu), cu.numel() - 1, int(total), int(bool(causal)), _p(out),
+                                 _p(bad) if bad is not None else None, _stream_ptr(stream)),
+          "fm_varlen_bounds")
+    if bad is not None and int(bad.item()) != 0:
+        raise ValueError("cu_seqlens is not a partition of [0, total)")
+    return out
+
+
 def localize(bounds, chunks, out=None, stream=None):
     """Bounds local to a rank holding query chunks ``chunks`` = [(global_start, length), ...]
     (ascending, non-overlapping), for local-Q x full-KV attention."""

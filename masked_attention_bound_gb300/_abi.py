@@ -62,6 +62,8 @@ SIGNATURES = {
                                       I32P, ctypes.c_float, P, P, P, P, ctypes.c_size_t, P]),
     "fm_fwd_static": (ctypes.c_int, [ctypes.POINTER(FmDesc), P, P, P, I32P, I32P, I32P, I32P,
                                      ctypes.c_float, P, P, P]),
+    "fm_varlen_bounds": (ctypes.c_int, [I32P, ctypes.c_int, ctypes.c_int, ctypes.c_int, I32P, P,
+                                        P]),
     "fm_localize": (ctypes.c_int, [I32P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
                                    ctypes.c_int, I32P, P]),
     "fm_device_status": (ctypes.c_int, [P, P]),

@@ -234,6 +234,15 @@ fm_status fm_bwd_planned(const fm_desc* desc, const void* q, const void* k, cons
                   ws_bytes, stream, 1);
 }
 
+fm_status fm_varlen_bounds(const int32_t* cu_seqlens, int n_seqs, int total, int causal,
+                           int32_t* bounds, int* bad, void* stream) {
+  if (!cu_seqlens || !bounds || n_seqs < 1 || total < 1 || total > (1 << 24)) return FM_ERR_INVALID;
+  if (launch_varlen_bounds(cu_seqlens, n_seqs, total, causal != 0, bounds, bad,
+                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FM_ERR_CUDA;
+  return FM_OK;
+}
+
 fm_status fm_localize(const int32_t* bounds, int B, int Hm, int Skv,
                       const int32_t* chunk_start, const int32_t* chunk_len, int n_chunks,
                       int32_t* local_bounds, void* stream) {

@@ -279,15 +279,19 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
   auto col_of = [&](int b, int h, int kj) { return (b * P.Hm + (P.Hm == 1 ? 0 : h)) * P.nK + kj; };
   // unit u = (b*Hkv + hk)*nK + kj -> the columns of q-tiles of the G query
   // heads h = hk*G + j that read K/V head hk, walked one head after another;
-  // returns their total tile count
-  auto unit_info = [&](int idx, int& b, int& hk, int& kj) {
+  // returns their total tile count, and the first head's column and count
+  // (so that a walk starts without loading them again)
+  auto unit_info = [&](int idx, int& b, int& hk, int& kj, const int32_t*& list0, int& n0) {
     const int u = P.order[idx];
     const int bh = u / P.nK;
     kj = u - bh * P.nK;
     b = bh / P.Hkv;
     hk = bh - b * P.Hkv;
-    int n = 0;
-    for (int j = 0; j < P.G; ++j) n += P.list_count[col_of(b, hk * P.G + j, kj)];
+    const int col0 = col_of(b, hk * P.G, kj);
+    list0 = P.list + static_cast<size_t>(col0) * P.nQ;
+    n0 = P.list_count[col0];
+    int n = n0;
+    for (int j = 1; j < P.G; ++j) n += P.list_count[col_of(b, hk * P.G + j, kj)];
     return n;
   };
   // the n-th claimed unit (-1: none left, or the launch was aborted).
@@ -322,8 +326,9 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       while (true) {
         const int idx = claimed_one(cn);
         if (idx < 0) break;
-        int b, h, kj;  // h: the K/V head
-        const int n = unit_info(idx, b, h, kj);
+        int b, h, kj, n0;  // h: the K/V head
+        const int32_t* list0;
+        const int n = unit_info(idx, b, h, kj, list0, n0);
         if (n == 0) continue;
         if (un > 0 && !wait(A_KEMPTY, (un - 1) & 1)) break;
         mbar_arrive_expect_tx(bar(A_KFULL), C::TILE);
@@ -364,14 +369,17 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         ring[r] = idx;
         mbar_arrive(bar(A_UFULL0 + r));
         if (idx < 0) break;
-        int b, hk, kj;
-        unit_info(idx, b, hk, kj);
+        int b, hk, kj, nj;
+        const int32_t* list;
+        unit_info(idx, b, hk, kj, list, nj);
         // the q-tile columns of the G query heads reading K/V head hk
         for (int j = 0; j < P.G && ok; ++j) {
           const int h = hk * P.G + j;
-          const int col = col_of(b, h, kj);
-          const int32_t* list = P.list + static_cast<size_t>(col) * P.nQ;
-          const int nj = P.list_count[col];
+          if (j > 0) {
+            const int col = col_of(b, h, kj);
+            list = P.list + static_cast<size_t>(col) * P.nQ;
+            nj = P.list_count[col];
+          }
           const size_t bh_row = (static_cast<size_t>(b) * P.H + h) * rows_pad;
           for (int t = 0; t < nj; ++t, ++it) {
             const int qi = list[t] >> 2;
@@ -430,8 +438,9 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       while (ok) {
         const int idx = claimed_one(cn);
         if (idx < 0) break;
-        int b, h, kj;
-        const int n = unit_info(idx, b, h, kj);
+        int b, h, kj, n0;
+        const int32_t* list0;
+        const int n = unit_info(idx, b, h, kj, list0, n0);
         if (n == 0) continue;
         if (!wait(A_KFULL, un & 1)) break;
         for (int t = 0; t < n; ++t, ++it) {
@@ -579,8 +588,9 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     while (ok) {
       const int idx = claimed_all(cn);
       if (idx < 0) break;
-      int b, hk, kj;  // hk: the K/V head
-      const int n = unit_info(idx, b, hk, kj);
+      int b, hk, kj, nj;  // hk: the K/V head
+      const int32_t* list;  // the walk's current query-head column, nj tiles
+      const int n = unit_info(idx, b, hk, kj, list, nj);
       const int key = kj * kTile + r;
       __nv_bfloat16* dk_row = P.out0 + b * P.s0[0] + static_cast<int64_t>(key) * P.s0[1] +
                               hk * P.s0[2] + half * (D / 2);
@@ -600,116 +610,119 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       // this thread's key column bounds (beyond Skv: hidden from every row),
       // read again when the walk moves to a query head with its own mask
       int lts = 0, lte = 0x7fffffff, uts = 0, ute = 0;
+      auto load_bounds = [&](int h) {
+        if (key < P.Skv) {
+          const size_t at = static_cast<size_t>(b * P.Hm + (P.Hm == 1 ? 0 : h)) * P.Skv + key;
+          lts = __ldg(P.bounds[0] + at);
+          lte = __ldg(P.bounds[1] + at);
+          uts = __ldg(P.bounds[2] + at);
+          ute = __ldg(P.bounds[3] + at);
+        }
+      };
+      load_bounds(hk * P.G);
       const bool key_ragged = (kj == P.nK - 1) && (P.Skv & (kTile - 1));
-      // the walk over the group's query heads: head j's column `list`, nj
-      // tiles, position i in it
-      int j = -1, nj = 0, i = 0;
-      const int32_t* list = nullptr;
-      for (int t = 0; t < n; ++t, ++it) {
-        while (i == nj) {  // next query head with tiles (n counts them all)
-          ++j;
+      // the walk over the group's query heads: head j's column, tile t of
+      // the unit
+      int t = 0;
+      for (int j = 0; j < P.G && ok; ++j) {
+        if (j > 0) {
           const int h = hk * P.G + j;
           const int col = col_of(b, h, kj);
           list = P.list + static_cast<size_t>(col) * P.nQ;
           nj = P.list_count[col];
-          i = 0;
-          if ((j == 0 || P.Hm > 1) && key < P.Skv) {
-            const size_t at = static_cast<size_t>(b * P.Hm + (P.Hm == 1 ? 0 : h)) * P.Skv + key;
-            lts = __ldg(P.bounds[0] + at);
-            lte = __ldg(P.bounds[1] + at);
-            uts = __ldg(P.bounds[2] + at);
-            ute = __ldg(P.bounds[3] + at);
-          }
+          if (P.Hm > 1) load_bounds(h);
         }
-        const int e = list[i++];
-        const int qi = e >> 2;
-        const bool partial = ((e & 3) == CLS_PARTIAL) || key_ragged;
-        const int st = it & 1;
-        const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LD + st * 1024) + c0;
-        const float* del_s = lse_s + 128;
-        // ---- P^T = exp2(S^T * scale*log2e - LSE*log2e), hidden entries 0
-        if (!wait_all(A_SFULL, it & 1)) { ok = false; break; }
-        // the LSE/D of this stage arrived with the Q/dO tiles
-        if (!wait_all(A_QFULL0 + st, (it >> 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-        float p[64];
-        {
-          uint32_t raw[64];
-          tmem_ld64(tbase + lane_off + C::T_A + c0, raw);
-          tmem_wait_ld();
-          // two columns per packed FMA: S^T * scale*log2e + (-LSE*log2e)
-          const uint64_t sc2 = splat2(P.scale_log2);
+        for (int i = 0; i < nj; ++i, ++t, ++it) {
+          const int e = list[i];
+          const int qi = e >> 2;
+          const bool partial = ((e & 3) == CLS_PARTIAL) || key_ragged;
+          const int st = it & 1;
+          const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LD + st * 1024) + c0;
+          const float* del_s = lse_s + 128;
+          // ---- P^T = exp2(S^T * scale*log2e - LSE*log2e), hidden entries 0
+          if (!wait_all(A_SFULL, it & 1)) { ok = false; break; }
+          // the LSE/D of this stage arrived with the Q/dO tiles
+          if (!wait_all(A_QFULL0 + st, (it >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          float p[64];
+          {
+            uint32_t raw[64];
+            tmem_ld64(tbase + lane_off + C::T_A + c0, raw);
+            tmem_wait_ld();
+            // two columns per packed FMA: S^T * scale*log2e + (-LSE*log2e)
+            const uint64_t sc2 = splat2(P.scale_log2);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float4 L = *reinterpret_cast<const float4*>(lse_s + 4 * i);
-            float a0, a1, a2, a3;
-            fma2_bv(a0, a1, __uint_as_float(raw[4 * i + 0]), __uint_as_float(raw[4 * i + 1]), sc2,
-                    L.x, L.y);
-            fma2_bv(a2, a3, __uint_as_float(raw[4 * i + 2]), __uint_as_float(raw[4 * i + 3]), sc2,
-                    L.z, L.w);
-            p[4 * i + 0] = ex2(a0);
-            p[4 * i + 1] = ex2(a1);
-            p[4 * i + 2] = ex2(a2);
-            p[4 * i + 3] = ex2(a3);
-          }
-        }
-        if (partial) {
-          // the rows q0 .. q0+63 hidden from this key form at most two
-          // intervals: one 64-bit mask, then a bit test per entry
-          const int q0 = qi * kTile + c0;
-          const uint64_t hm = row_span(lts - q0, lte - q0) | row_span(uts - q0, ute - q0);
-          if (hm != 0) {
-            const uint32_t m0 = static_cast<uint32_t>(hm), m1 = static_cast<uint32_t>(hm >> 32);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              p[c] = ((m0 >> c) & 1u) ? 0.f : p[c];
-              p[c + 32] = ((m1 >> c) & 1u) ? 0.f : p[c + 32];
+            for (int i = 0; i < 16; ++i) {
+              const float4 L = *reinterpret_cast<const float4*>(lse_s + 4 * i);
+              float a0, a1, a2, a3;
+              fma2_bv(a0, a1, __uint_as_float(raw[4 * i + 0]), __uint_as_float(raw[4 * i + 1]), sc2,
+                      L.x, L.y);
+              fma2_bv(a2, a3, __uint_as_float(raw[4 * i + 2]), __uint_as_float(raw[4 * i + 3]), sc2,
+                      L.z, L.w);
+              p[4 * i + 0] = ex2(a0);
+              p[4 * i + 1] = ex2(a1);
+              p[4 * i + 2] = ex2(a2);
+              p[4 * i + 3] = ex2(a3);
             }
           }
-        }
-        {
-          uint32_t pk[32];
+          if (partial) {
+            // the rows q0 .. q0+63 hidden from this key form at most two
+            // intervals: one 64-bit mask, then a bit test per entry
+            const int q0 = qi * kTile + c0;
+            const uint64_t hm = row_span(lts - q0, lte - q0) | row_span(uts - q0, ute - q0);
+            if (hm != 0) {
+              const uint32_t m0 = static_cast<uint32_t>(hm), m1 = static_cast<uint32_t>(hm >> 32);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(p[2 * c], p[2 * c + 1]);
-          // into the TMEM columns this thread read: [c0, c0 + 32)
-          tmem_st32(tbase + lane_off + C::T_A + c0, pk);
-          tmem_wait_st();
-        }
-        tc_fence_before();
-        // (a test of the wait limit withholds the first P-ready arrival: the
-        // MMA thread then gives up on it and the launch unwinds with DEV_TIMEOUT)
-        if (!(P.withhold == 2 && it == 0)) mbar_arrive_warp(bar(A_PREADY));
-        if (t == 0 && pending && !epilogue()) { ok = false; break; }
-        // ---- dS^T = P^T o (dP^T - D), to smem as bf16 [key][q] (slab = half)
-        if (!wait_all(A_DPFULL, it & 1)) { ok = false; break; }
-        tc_fence_after();
-        {
-          uint32_t raw[64];
-          tmem_ld64(tbase + lane_off + C::T_B + c0, raw);
-          tmem_wait_ld();
-          const uint32_t row_base = sDS + half * 16384 + r * 128;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const float4 Dv = *reinterpret_cast<const float4*>(del_s + 8 * j + 4 * i);
-              const int c = 8 * j + 4 * i;
-              float s0, s1, s2, s3;
-              mulsub2(s0, s1, p[c + 0], p[c + 1], __uint_as_float(raw[c + 0]),
-                      __uint_as_float(raw[c + 1]), Dv.x, Dv.y);
-              mulsub2(s2, s3, p[c + 2], p[c + 3], __uint_as_float(raw[c + 2]),
-                      __uint_as_float(raw[c + 3]), Dv.z, Dv.w);
-              w[2 * i] = pack_bf16(s0, s1);
-              w[2 * i + 1] = pack_bf16(s2, s3);
+              for (int c = 0; c < 32; ++c) {
+                p[c] = ((m0 >> c) & 1u) ? 0.f : p[c];
+                p[c + 32] = ((m1 >> c) & 1u) ? 0.f : p[c + 32];
+              }
             }
-            const uint32_t chunk = static_cast<uint32_t>(j) ^ static_cast<uint32_t>(r & 7);
-            st_shared_v4(row_base + chunk * 16, w[0], w[1], w[2], w[3]);
           }
+          {
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(p[2 * c], p[2 * c + 1]);
+            // into the TMEM columns this thread read: [c0, c0 + 32)
+            tmem_st32(tbase + lane_off + C::T_A + c0, pk);
+            tmem_wait_st();
+          }
+          tc_fence_before();
+          // (a test of the wait limit withholds the first P-ready arrival: the
+          // MMA thread then gives up on it and the launch unwinds with DEV_TIMEOUT)
+          if (!(P.withhold == 2 && it == 0)) mbar_arrive_warp(bar(A_PREADY));
+          if (t == 0 && pending && !epilogue()) { ok = false; break; }
+          // ---- dS^T = P^T o (dP^T - D), to smem as bf16 [key][q] (slab = half)
+          if (!wait_all(A_DPFULL, it & 1)) { ok = false; break; }
+          tc_fence_after();
+          {
+            uint32_t raw[64];
+            tmem_ld64(tbase + lane_off + C::T_B + c0, raw);
+            tmem_wait_ld();
+            const uint32_t row_base = sDS + half * 16384 + r * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint32_t w[4];
+#pragma unroll
+              for (int i = 0; i < 2; ++i) {
+                const float4 Dv = *reinterpret_cast<const float4*>(del_s + 8 * j + 4 * i);
+                const int c = 8 * j + 4 * i;
+                float s0, s1, s2, s3;
+                mulsub2(s0, s1, p[c + 0], p[c + 1], __uint_as_float(raw[c + 0]),
+                        __uint_as_float(raw[c + 1]), Dv.x, Dv.y);
+                mulsub2(s2, s3, p[c + 2], p[c + 3], __uint_as_float(raw[c + 2]),
+                        __uint_as_float(raw[c + 3]), Dv.z, Dv.w);
+                w[2 * i] = pack_bf16(s0, s1);
+                w[2 * i + 1] = pack_bf16(s2, s3);
+              }
+              const uint32_t chunk = static_cast<uint32_t>(j) ^ static_cast<uint32_t>(r & 7);
+              st_shared_v4(row_base + chunk * 16, w[0], w[1], w[2], w[3]);
+            }
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive_warp(bar(A_DSREADY));
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive_warp(bar(A_DSREADY));
       }
       if (!ok) break;
       pending = true;

@@ -378,6 +378,47 @@ __global__ void __launch_bounds__(256) order_kernel(const int32_t* __restrict__ 
   }
 }
 
+// ------------------------------------------------------------------ varlen
+// Bounds of a packed batch: key j of sequence [a, b) (a = cu[s] <= j < b =
+// cu[s+1]) is seen by rows [j, b) (causal) or [a, b): lower interval
+// [b, total), upper interval [0, j) or [0, a).  The sequence is found by a
+// binary search over cu[0..n].  Thread 0..n also checks that cu is a
+// partition of [0, total) (cu[0] = 0, non-decreasing, cu[n] = total) and
+// otherwise sets *bad; keys outside every sequence (only possible then) get
+// bounds that hide them from every row.
+__global__ void varlen_bounds_kernel(const int32_t* __restrict__ cu, int n, int total, int causal,
+                                     int32_t* __restrict__ out, int* bad) {
+  const int stride = gridDim.x * blockDim.x;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i <= n; i += stride) {
+    const int c = cu[i];
+    const bool ok = (i == 0 ? c == 0 : c >= cu[i - 1]) && (i < n || c == total) && c <= total;
+    if (!ok && bad) atomicOr(bad, 1);
+  }
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < total; j += stride) {
+    int lo = 0, hi = n;  // find the last s in [0, n) with cu[s] <= j
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (cu[mid] <= j) lo = mid; else hi = mid;
+    }
+    const int a = cu[lo], b = cu[lo + 1];
+    int4 v;
+    if (a <= j && j < b) v = make_int4(b, total, 0, causal ? j : a);
+    else v = make_int4(0, total, 0, 0);  // hidden from every row
+    out[j] = v.x;
+    out[total + j] = v.y;
+    out[2 * total + j] = v.z;
+    out[3 * total + j] = v.w;
+  }
+}
+
+cudaError_t launch_varlen_bounds(const int32_t* cu, int n, int total, int causal, int32_t* out,
+                                 int* bad, cudaStream_t s) {
+  const int want = (total + 255) / 256;
+  varlen_bounds_kernel<<<want < 1024 ? (want < 1 ? 1 : want) : 1024, 256, 0, s>>>(cu, n, total,
+                                                                                 causal, out, bad);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ localize
 __global__ void localize_kernel(const int32_t* __restrict__ in, int32_t* __restrict__ out,
                                 long long n, const __grid_constant__ ChunkMap cm) {
