@@ -1,0 +1,86 @@
+"""FP8 (e4m3) forward oracle: per-tile quantisation and the attention it
+computes, in float64.  Test infrastructure only (see ``oracle/__init__.py``).
+
+The ROCm page («Современное состояние Flash Attention на ROCm») reports an
+FP8 FlashAttention as the fastest of its comparison and gives no formula.
+The reading written here (and in the library's header):
+
+* e4m3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; normals
+  (1 + m/8) 2^(e-7) for e = 1..15 (e = 15, m = 7 is NaN, so the largest
+  finite value is 448), subnormals (m/8) 2^-6.  Conversion rounds to the
+  nearest value, ties to even, and saturates at +-448.
+* Per-tile quantisation of a [rows][d] head slice: tile t = rows
+  [128 t, 128 t + 128); scale s_t = amax_t / 448 in float32 (1 when the tile
+  is all zero), code = e4m3(x / s_t) with the division in float32.
+* Attention on codes and scales, per query row i over its visible keys j:
+      s_ij = scale * sq_t(i) * sk_t(j) * (q8_i . k8_j)       c_ij = s_ij log2 e
+      M_i  = ceil(max_j c_ij)       p_ij = 2^(c_ij - M_i)     l_i = sum_j p_ij
+      P8_ij = e4m3(p_ij * r_t(j)),  r_t = sv_t / sv_head (sv_head = max_t sv_t)
+      o_i  = sv_head * (sum_j P8_ij v8_j) / l_i,   lse_i = (M_i + log2 l_i) ln 2
+  Rows that see no key: o = 0, lse = -inf.  P is rounded to e4m3 after the
+  V tile's scale ratio is folded into it, so P8 V8 needs one scale per head;
+  the reference exponent M_i is an integer, so a kernel that rescales by whole
+  powers of two meets the same P8 codes (e4m3 rounding commutes with them
+  outside the subnormal range).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .masks import dense_mask
+
+E4M3_MAX = 448.0
+TILE = 128
+
+
+def e4m3(x) -> np.ndarray:
+    """Nearest e4m3 value (ties to even), saturating at +-448; float64 out."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))          # a = m 2^ex, m in [0.5, 1)
+    e = np.maximum(ex - 1, -6)                          # binade; subnormals share 2^-6's
+    q = np.ldexp(1.0, (e - 3).astype(np.int64))         # spacing of 3 mantissa bits there
+    r = np.round(a / q) * q                             # exact quotient; half to even
+    r = np.minimum(r, E4M3_MAX)
+    return np.where(a > 0, np.sign(x) * r, 0.0)
+
+
+def quantize_tiles(x) -> tuple[np.ndarray, np.ndarray]:
+    """Codes (as float64 values) and float32 scales of a [rows][d] slice,
+    per 128-row tile (the last tile may be short)."""
+    x32 = np.asarray(x, dtype=np.float32)
+    rows = x32.shape[0]
+    nt = -(-rows // TILE)
+    codes = np.zeros(x32.shape, dtype=np.float64)
+    scales = np.ones(nt, dtype=np.float32)
+    for t in range(nt):
+        blk = x32[t * TILE:(t + 1) * TILE]
+        amax = np.float32(np.abs(blk).max()) if blk.size else np.float32(0)
+        s = np.float32(amax / np.float32(E4M3_MAX)) if amax > 0 else np.float32(1)
+        scales[t] = s
+        codes[t * TILE:(t + 1) * TILE] = e4m3((blk / s).astype(np.float32))
+    return codes, scales
+
+
+def forward_head_fp8(q8, sq, k8, sk, v8, sv, mvec, scale, rows=None):
+    """O rows and LSE of one head from codes and per-tile scales (see the
+    module docstring); q8 [Sq][d], k8 and v8 [Skv][d] as float64 values."""
+    Sq = q8.shape[0]
+    rows = np.arange(Sq) if rows is None else np.asarray(rows)
+    hidden = dense_mask(*mvec, Sq, rows=rows)               # [len(rows)][Skv]
+    svh = float(np.max(sv))
+    qs = np.asarray(sq, np.float64)[rows // TILE]
+    ks = np.asarray(sk, np.float64)[np.arange(k8.shape[0]) // TILE]
+    c = (q8[rows] @ k8.T) * qs[:, None] * ks[None, :] * scale * np.log2(np.e)
+    c = np.where(hidden, -np.inf, c)
+    mx = c.max(axis=1)
+    dead = ~np.isfinite(mx)
+    M = np.where(dead, 0.0, np.ceil(np.where(dead, 0.0, mx)))
+    p = np.where(hidden, 0.0, np.exp2(c - M[:, None]))
+    l = p.sum(axis=1)
+    r = np.asarray(sv, np.float64)[np.arange(k8.shape[0]) // TILE] / svh
+    p8 = e4m3(p * r[None, :])
+    o = svh * (p8 @ v8) / np.where(dead, 1.0, l)[:, None]
+    o[dead] = 0.0
+    lse = np.where(dead, -np.inf, (M + np.log2(np.where(dead, 1.0, l))) * np.log(2.0))
+    return o, lse
