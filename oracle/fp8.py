@@ -12,16 +12,22 @@ The reading written here (and in the library's header):
 * Per-tile quantisation of a [rows][d] head slice: tile t = rows
   [128 t, 128 t + 128); scale s_t = amax_t / 448 in float32 (1 when the tile
   is all zero), code = e4m3(x / s_t) with the division in float32.
-* Attention on codes and scales, per query row i over its visible keys j:
-      s_ij = scale * sq_t(i) * sk_t(j) * (q8_i . k8_j)       c_ij = s_ij log2 e
-      M_i  = ceil(max_j c_ij)       p_ij = 2^(c_ij - M_i)     l_i = sum_j p_ij
-      P8_ij = e4m3(p_ij * r_t(j)),  r_t = sv_t / sv_head (sv_head = max_t sv_t)
-      o_i  = sv_head * (sum_j P8_ij v8_j) / l_i,   lse_i = (M_i + log2 l_i) ln 2
-  Rows that see no key: o = 0, lse = -inf.  P is rounded to e4m3 after the
-  V tile's scale ratio is folded into it, so P8 V8 needs one scale per head;
-  the reference exponent M_i is an integer, so a kernel that rescales by whole
-  powers of two meets the same P8 codes (e4m3 rounding commutes with them
-  outside the subnormal range).
+* Attention on codes and scales, one query row i at a time, over the k-tiles
+  in ascending order (a streaming pass, as FlashAttention-2 computes it:
+  FlashAttention-2 page, «Блочная обработка сохраняет общую нормализацию»):
+      s_ij = scale * sq_t(i) * sk_t(j) * (q8_i . k8_j),   c_ij = s_ij log2 e
+  The row keeps an integral reference exponent M (from -inf), a sum l and an
+  accumulator a.  For tile t with maximum m_t of c over its visible keys: if
+  m_t > M + 8, M moves to ceil(m_t) and l, a are multiplied by 2^(M_old -
+  M_new) (0 from -inf).  Then, for the tile's visible keys,
+      p_ij = 2^(c_ij - M),  l += sum p_ij,  a += sum e4m3(p_ij r_t) v8_j,
+  with r_t = sv_t / sv_head (sv_head = max_t sv_t).  Finally
+      o_i = sv_head a / l,   lse_i = (M + log2 l) ln 2.
+  Rows that see no key: o = 0, lse = -inf.  P is rounded after the V tile's
+  scale ratio is folded into it, so P8 V8 needs one scale per head.  The
+  reference exponent is part of the definition: e4m3 rounding commutes with
+  power-of-two scaling only outside its subnormal range, which small P r_t
+  reach.
 """
 from __future__ import annotations
 
@@ -65,22 +71,38 @@ def quantize_tiles(x) -> tuple[np.ndarray, np.ndarray]:
 def forward_head_fp8(q8, sq, k8, sk, v8, sv, mvec, scale, rows=None):
     """O rows and LSE of one head from codes and per-tile scales (see the
     module docstring); q8 [Sq][d], k8 and v8 [Skv][d] as float64 values."""
-    Sq = q8.shape[0]
+    Sq, Skv = q8.shape[0], k8.shape[0]
     rows = np.arange(Sq) if rows is None else np.asarray(rows)
     hidden = dense_mask(*mvec, Sq, rows=rows)               # [len(rows)][Skv]
     svh = float(np.max(sv))
     qs = np.asarray(sq, np.float64)[rows // TILE]
-    ks = np.asarray(sk, np.float64)[np.arange(k8.shape[0]) // TILE]
+    ks = np.asarray(sk, np.float64)[np.arange(Skv) // TILE]
     c = (q8[rows] @ k8.T) * qs[:, None] * ks[None, :] * scale * np.log2(np.e)
     c = np.where(hidden, -np.inf, c)
-    mx = c.max(axis=1)
-    dead = ~np.isfinite(mx)
-    M = np.where(dead, 0.0, np.ceil(np.where(dead, 0.0, mx)))
-    p = np.where(hidden, 0.0, np.exp2(c - M[:, None]))
-    l = p.sum(axis=1)
-    r = np.asarray(sv, np.float64)[np.arange(k8.shape[0]) // TILE] / svh
-    p8 = e4m3(p * r[None, :])
-    o = svh * (p8 @ v8) / np.where(dead, 1.0, l)[:, None]
+    n = len(rows)
+    M = np.full(n, -np.inf)
+    l = np.zeros(n)
+    a = np.zeros((n, v8.shape[1]))
+    for t in range(-(-Skv // TILE)):
+        cols = slice(t * TILE, min(Skv, (t + 1) * TILE))
+        ct = c[:, cols]
+        mt = ct.max(axis=1)
+        grow = mt > M + 8
+        Mn = np.where(grow, np.ceil(np.where(grow, mt, 0.0)), M)
+        finite = np.isfinite(M)
+        alpha = np.where(grow & finite, np.exp2(np.where(finite, M, 0.0) - Mn), 0.0)
+        alpha = np.where(grow, alpha, 1.0)
+        l *= alpha
+        a *= alpha[:, None]
+        M = Mn
+        live = np.isfinite(M)
+        p = np.where(live[:, None], np.exp2(ct - np.where(live, M, 0.0)[:, None]), 0.0)
+        l += p.sum(axis=1)
+        a += e4m3(p * (float(sv[t]) / svh)) @ v8[cols]
+    dead = ~np.isfinite(M)
+    o = svh * a / np.where(dead, 1.0, l)[:, None]
     o[dead] = 0.0
-    lse = np.where(dead, -np.inf, (M + np.log2(np.where(dead, 1.0, l))) * np.log(2.0))
+    lse = np.where(dead, -np.inf, (np.where(dead, 0.0, M) + np.log2(np.where(dead, 1.0, l)))
+                   * np.log(2.0))
     return o, lse
+
