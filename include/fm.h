@@ -231,6 +231,39 @@ fm_status fm_localize(const int32_t* bounds, int B, int Hm, int Skv,
                       const int32_t* chunk_start, const int32_t* chunk_len, int n_chunks,
                       int32_t* local_bounds, void* stream);
 
+/* FP8 (e4m3) forward, head_dim 128 only (FM_ERR_UNSUPPORTED otherwise).  The
+ * ROCm page («Современное состояние Flash Attention на ROCm») names an FP8
+ * FlashAttention as the fastest in its comparison and gives no formula; the
+ * reading here is per-tile scaling:
+ *
+ * fm_quantize_fp8: for each (batch, head) and 128-row tile of Q, K and V, the
+ * scale s = amax / 448 in fp32 (1 for an all-zero tile) and the codes
+ * e4m3(x / s) (fp32 division, round to nearest even, saturating at +-448).
+ * Inputs q, k, v: bf16 with desc's strides.  Outputs (caller-owned device
+ * memory): q8 uint8 [B][Sq][H][128] and k8 uint8 [B][Skv][Hkv][128] (BSHD,
+ * contiguous); v8t uint8 [B][Hkv][128][nK*128], V transposed per head with the
+ * key axis padded to whole tiles (padding 0); q_scale fp32 [B][H][nQ],
+ * k_scale and v_scale fp32 [B][Hkv][nK], v_head_scale fp32 [B][Hkv] (the
+ * largest V tile scale of the head).
+ *
+ * fm_fwd_fp8: the forward pass on those codes and scales, with the same
+ * masks, scale, outputs (o bf16 with o_stride, lse fp32) and workspace
+ * (FM_WS_FWD) as fm_fwd; desc's q/k/v strides are not used.  Per query row
+ * i and visible key j: s_ij = scale * sq * sk * (q8_i . k8_j), c = s log2 e;
+ * P is taken against an integral reference exponent M (ceil of the running
+ * row maximum of c, moved only when it grows by more than 8), multiplied by
+ * the V tile's ratio sv / sv_head and rounded to e4m3 for the P V product;
+ * O = sv_head * sum_j P8_ij v8_j / sum_j 2^(c_ij - M), LSE = (M + log2 l) ln 2.
+ * Both products run as e4m3 tensor-core MMAs with fp32 accumulation. */
+fm_status fm_quantize_fp8(const fm_desc* desc, const void* q, const void* k, const void* v,
+                          void* q8, void* k8, void* v8t, float* q_scale, float* k_scale,
+                          float* v_scale, float* v_head_scale, void* stream);
+fm_status fm_fwd_fp8(const fm_desc* desc, const void* q8, const void* k8, const void* v8t,
+                     const float* q_scale, const float* k_scale, const float* v_scale,
+                     const float* v_head_scale, const int32_t* lts, const int32_t* lte,
+                     const int32_t* uts, const int32_t* ute, float scale, void* o, float* lse,
+                     void* ws, size_t ws_bytes, void* stream);
+
 /* Bounds of a packed variable-length batch: the FlashAttention-2 page's
  * fixed-token batch («Как понимать заявленное ускорение»: 16K tokens per
  * batch) in the column-bound form of the FlashMask-3 page.  Sequence s holds

@@ -14,6 +14,7 @@ or UTS[j] <= i < UTE[j].
 from __future__ import annotations
 
 import ctypes
+from typing import NamedTuple
 
 import torch
 
@@ -144,6 +145,54 @@ def backward(q, k, v, o, lse, do, bounds, scale, dq=None, dk=None, dv=None, ws=N
                                *_bounds_ptrs(bounds), ctypes.c_float(scale), _p(dq), _p(dk),
                                _p(dv), _p(ws), ws.numel(), _stream_ptr(stream)), name)
     return dq, dk, dv
+
+
+class Fp8Inputs(NamedTuple):
+    """e4m3 codes and per-tile scales of Q, K, V (fm_quantize_fp8)."""
+    q8: torch.Tensor           # uint8 [B][Sq][H][128]
+    k8: torch.Tensor           # uint8 [B][Skv][Hkv][128]
+    v8t: torch.Tensor          # uint8 [B][Hkv][128][nK*128], V transposed per head
+    q_scale: torch.Tensor      # fp32 [B][H][nQ]
+    k_scale: torch.Tensor      # fp32 [B][Hkv][nK]
+    v_scale: torch.Tensor      # fp32 [B][Hkv][nK]
+    v_head_scale: torch.Tensor  # fp32 [B][Hkv]
+
+
+def quantize_fp8(q, k, v, stream=None) -> Fp8Inputs:
+    """Per-tile e4m3 quantisation of bf16 Q, K, V (head_dim 128)."""
+    B, Sq, H, d = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    nQ, nK = -(-Sq // 128), -(-Skv // 128)
+    dev = q.device
+    out = Fp8Inputs(
+        torch.empty(B, Sq, H, d, dtype=torch.uint8, device=dev),
+        torch.empty(B, Skv, Hkv, d, dtype=torch.uint8, device=dev),
+        torch.empty(B, Hkv, d, nK * 128, dtype=torch.uint8, device=dev),
+        torch.empty(B, H, nQ, dtype=torch.float32, device=dev),
+        torch.empty(B, Hkv, nK, dtype=torch.float32, device=dev),
+        torch.empty(B, Hkv, nK, dtype=torch.float32, device=dev),
+        torch.empty(B, Hkv, dtype=torch.float32, device=dev))
+    desc = make_desc(q, k, v)
+    check(lib().fm_quantize_fp8(ctypes.byref(desc), _p(q), _p(k), _p(v), *(_p(t) for t in out),
+                                _stream_ptr(stream)), "fm_quantize_fp8")
+    return out
+
+
+def forward_fp8(f: Fp8Inputs, bounds, scale, o=None, lse=None, ws=None, stream=None):
+    """FP8 forward (fm_fwd_fp8) on quantised inputs: O bf16 [B][Sq][H][128], LSE."""
+    B, Sq, H, d = f.q8.shape
+    if o is None:
+        o = torch.empty(B, Sq, H, d, dtype=torch.bfloat16, device=f.q8.device)
+    if lse is None:
+        lse = torch.empty(B, H, Sq, dtype=torch.float32, device=f.q8.device)
+    desc = make_desc(f.q8, f.k8, f.k8, o, Hm=bounds.shape[2])
+    if ws is None:
+        ws = workspace(desc, WS_FWD, f.q8.device)
+    check(lib().fm_fwd_fp8(ctypes.byref(desc), _p(f.q8), _p(f.k8), _p(f.v8t), _p(f.q_scale),
+                           _p(f.k_scale), _p(f.v_scale), _p(f.v_head_scale), *_bounds_ptrs(bounds),
+                           ctypes.c_float(scale), _p(o), _p(lse), _p(ws), ws.numel(),
+                           _stream_ptr(stream)), "fm_fwd_fp8")
+    return o, lse
 
 
 def varlen_bounds(cu_seqlens, total=None, causal=True, stream=None, validate=True):

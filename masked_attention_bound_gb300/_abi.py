@@ -62,6 +62,9 @@ SIGNATURES = {
                                       I32P, ctypes.c_float, P, P, P, P, ctypes.c_size_t, P]),
     "fm_fwd_static": (ctypes.c_int, [ctypes.POINTER(FmDesc), P, P, P, I32P, I32P, I32P, I32P,
                                      ctypes.c_float, P, P, P]),
+    "fm_quantize_fp8": (ctypes.c_int, [ctypes.POINTER(FmDesc), P, P, P, P, P, P, P, P, P, P, P]),
+    "fm_fwd_fp8": (ctypes.c_int, [ctypes.POINTER(FmDesc), P, P, P, P, P, P, P, I32P, I32P, I32P,
+                                  I32P, ctypes.c_float, P, P, P, ctypes.c_size_t, P]),
     "fm_varlen_bounds": (ctypes.c_int, [I32P, ctypes.c_int, ctypes.c_int, ctypes.c_int, I32P, P,
                                         P]),
     "fm_localize": (ctypes.c_int, [I32P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
@@ -76,7 +79,7 @@ SIGNATURES = {
     "fm_measure_exp2_rate": (ctypes.c_int, [P, P]),
 }
 
-KERNEL_IDS = 9
+KERNEL_IDS = 11
 
 
 def lib():

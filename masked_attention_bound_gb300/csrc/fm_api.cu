@@ -234,6 +234,45 @@ fm_status fm_bwd_planned(const fm_desc* desc, const void* q, const void* k, cons
                   ws_bytes, stream, 1);
 }
 
+fm_status fm_quantize_fp8(const fm_desc* desc, const void* q, const void* k, const void* v,
+                          void* q8, void* k8, void* v8t, float* q_scale, float* k_scale,
+                          float* v_scale, float* v_head_scale, void* stream) {
+  Plan p;
+  fm_status st = make_plan(desc, FM_WS_FWD, &p);
+  if (st != FM_OK) return st;
+  if (p.d != 128) return FM_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q8) || !aligned16(k8) ||
+      !aligned16(v8t) || !q_scale || !k_scale || !v_scale || !v_head_scale)
+    return FM_ERR_INVALID;
+  return launch_quantize_fp8(p, *desc, q, k, v, q8, k8, v8t, q_scale, k_scale, v_scale,
+                             v_head_scale, static_cast<cudaStream_t>(stream));
+}
+
+fm_status fm_fwd_fp8(const fm_desc* desc, const void* q8, const void* k8, const void* v8t,
+                     const float* q_scale, const float* k_scale, const float* v_scale,
+                     const float* v_head_scale, const int32_t* lts, const int32_t* lte,
+                     const int32_t* uts, const int32_t* ute, float scale, void* o, float* lse,
+                     void* ws, size_t ws_bytes, void* stream) {
+  Plan p;
+  fm_status st = make_plan(desc, FM_WS_FWD, &p);
+  if (st != FM_OK) return st;
+  if (p.d != 128) return FM_ERR_UNSUPPORTED;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8t) || !aligned16(o) || !lse ||
+      !q_scale || !k_scale || !v_scale || !v_head_scale)
+    return FM_ERR_INVALID;
+  if (!lts || !lte || !uts || !ute) return FM_ERR_INVALID;
+  if ((st = check_ws(p, ws, ws_bytes)) != FM_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  if ((st = run_plan(p, lts, lte, uts, ute, w, FM_WS_FWD, s)) != FM_OK) return st;
+  TensorArgs t{};
+  t.o_out = o; t.lse_out = lse;
+  t.bounds[0] = lts; t.bounds[1] = lte; t.bounds[2] = uts; t.bounds[3] = ute;
+  t.scale = scale;
+  Fp8Args f{q8, k8, v8t, q_scale, k_scale, v_scale, v_head_scale};
+  return launch_fwd_fp8(p, *desc, t, f, w, s);
+}
+
 fm_status fm_varlen_bounds(const int32_t* cu_seqlens, int n_seqs, int total, int causal,
                            int32_t* bounds, int* bad, void* stream) {
   if (!cu_seqlens || !bounds || n_seqs < 1 || total < 1 || total > (1 << 24)) return FM_ERR_INVALID;

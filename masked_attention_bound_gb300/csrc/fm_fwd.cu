@@ -28,6 +28,16 @@
 //   warp 10    loads V.
 // TMEM (512 columns): S/P of slot s at [128 s, 128 s + 128), O of slot s at
 // [256 + 128 s, 256 + 128 s + D).
+//
+// FP8 variant (F8 = true, d = 128): Q and K are e4m3 codes with one scale per
+// 128-row tile, V is e4m3 transposed per head ([d][key], a K-major operand)
+// with one scale per 128-key tile and the head's largest tile scale.  Both
+// products are kind::f8f6f4 MMAs on K-major shared-memory operands (32
+// elements per MMA).  The softmax multiplies each S tile by scale * sq * sk,
+// keeps its reference exponent integral (so rescales are exact powers of two),
+// folds the V tile's scale ratio sv / sv_head into the exponent of P, rounds P
+// to e4m3 into a per-slot shared-memory tile, and the epilogue multiplies O by
+// sv_head / l.
 #include <cuda_bf16.h>
 
 #include "fm_internal.h"
@@ -36,14 +46,18 @@
 
 namespace fm {
 
-template <int D>
+template <int D, bool F8 = false>
 struct FwdCfg {
-  static constexpr int SLABS = D / 64;
-  static constexpr int TILE = 128 * D * 2;  // bytes of one 128-row tile
+  static constexpr int ESIZE = F8 ? 1 : 2;          // bytes per element of Q, K, V
+  static constexpr int SLABS = D * ESIZE / 128;     // 128-byte swizzle slabs per row
+  static constexpr int SLAB_ELEMS = 128 / ESIZE;    // elements per slab row
+  static constexpr int KSTEPS = D * ESIZE / 32;     // MMA steps of 32 bytes along d
+  static constexpr int TILE = 128 * D * ESIZE;      // bytes of one 128-row tile
   static constexpr int OFF_Q = 0;                              // slots a, b
   static constexpr int OFF_K = OFF_Q + 2 * TILE;               // 2 stages
   static constexpr int OFF_V = OFF_K + 2 * TILE;               // 2 stages
-  static constexpr int OFF_MSK = OFF_V + 2 * TILE;             // [stage][slot] bit masks
+  static constexpr int OFF_P = OFF_V + 2 * TILE;               // F8: [slot] P, 128 x 128 e4m3
+  static constexpr int OFF_MSK = OFF_P + (F8 ? 2 * 128 * 128 : 0);  // [stage][slot] bit masks
   static constexpr int OFF_DESC = OFF_MSK + 4 * kMaskBytes;    // [stage] entry word
   static constexpr int OFF_RING = OFF_DESC + 16;               // [UNIT_RING] claimed units
   static constexpr int OFF_BAR = OFF_RING + 16;
@@ -107,6 +121,12 @@ struct FwdParams {
   int* status;
   uint64_t wait_ns;  // limit of every mbarrier wait
   int withhold;      // test hook: 1 = slot a's softmax withholds its first P-ready arrival
+  // FP8 variant: per-tile scales [B][H][nQ] (Q), [B][Hkv][nK] (K, V), and
+  // the per-head V scale [B][Hkv]
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
+  const float* v_head_scale;
 };
 
 // Each CTA claims units idx = 0, 1, 2, ... of the longest-first order as it
@@ -145,11 +165,11 @@ struct Pair {
   }
 };
 
-template <int D>
-__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+template <int D, bool F8>
+__global__ void __launch_bounds__(FwdCfg<D, F8>::THREADS, 1)
     fwd_kernel(const __grid_constant__ FwdParams P, const __grid_constant__ CUtensorMap tmQ,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, F8>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {  // swizzled tiles need a 1024-aligned base
     if (threadIdx.x == 0) atomicOr(P.status, DEV_LAYOUT);
@@ -337,7 +357,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
             for (int x = 0; x < C::SLABS; ++x)
               tma_load_4d(sbase + C::OFF_Q + s * C::TILE + x * 16384, &tmQ, bar(B_QFULL0 + s),
-                          x * 64, u.h, (u.qa + s) * kTile, u.b);
+                          x * C::SLAB_ELEMS, u.h, (u.qa + s) * kTile, u.b);
           }
         }
         qn.set(s, qn.get(s) + 1);
@@ -391,7 +411,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
           for (int x = 0; x < C::SLABS; ++x)
             tma_load_4d(sbase + C::OFF_K + st * C::TILE + x * 16384, &tmK, bar(B_KFULL0 + st),
-                        x * 64, u.h / P.G, kj * kTile, u.b);
+                        x * C::SLAB_ELEMS, u.h / P.G, kj * kTile, u.b);
           // a slot whose tile here is not partial never reads this stage's bits
           if (ca != CLS_PARTIAL) mbar_arrive_count(bar(B_MEMPTY0 + st), 4);
           if (cb != CLS_PARTIAL) mbar_arrive_count(bar(B_MEMPTY0 + st), 4);
@@ -438,10 +458,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           const uint32_t use = e >> 1;
           if (use > 0 && !wait(B_KVEMPTY0 + st, (use - 1) & 1)) { ok = false; break; }
           mbar_arrive_expect_tx(bar(B_VFULL0 + st), C::TILE);
+          if constexpr (F8) {
+            // V^T tile: 128 keys (contiguous) x d rows of the K/V head
+            tma_load_4d(sbase + C::OFF_V + st * C::TILE, &tmV, bar(B_VFULL0 + st), kj * kTile,
+                        0, u.h / P.G, u.b);
+          } else {
 #pragma unroll
-          for (int x = 0; x < C::SLABS; ++x)
-            tma_load_4d(sbase + C::OFF_V + st * C::TILE + x * 16384, &tmV, bar(B_VFULL0 + st),
-                        x * 64, u.h / P.G, kj * kTile, u.b);
+            for (int x = 0; x < C::SLABS; ++x)
+              tma_load_4d(sbase + C::OFF_V + st * C::TILE + x * 16384, &tmV, bar(B_VFULL0 + st),
+                          x * 64, u.h / P.G, kj * kTile, u.b);
+          }
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -464,14 +490,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       const int s = warp == MMA_WARP ? 0 : 1;
       const uint32_t fA = s ? E_B : E_A, fFIRST = s ? E_FIRST_B : E_FIRST_A,
                      fLAST = s ? E_LAST_B : E_LAST_A;
-      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
+      constexpr uint32_t idS = F8 ? idesc_e4m3(128, 128) : idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idPV = F8 ? idesc_e4m3(128, D) : idesc_bf16(128, D, false, true);
       const uint32_t sQ = sbase + C::OFF_Q + s * C::TILE;
       // operand descriptors of each buffer, computed once (each MMA adds a
       // constant offset): Q and K K-major, V MN-major
       const uint32_t dQ = sdesc_lo(sQ, 16);
       const uint32_t dK0 = sdesc_lo(sbase + C::OFF_K, 16);
-      const uint32_t dV0 = sdesc_lo(sbase + C::OFF_V, 128 * 128);
+      // V: MN-major [key][d] tiles, or (F8) K-major V^T [d][key] tiles; P (F8)
+      // the slot's K-major [q][key] tile
+      const uint32_t dV0 = F8 ? sdesc_lo(sbase + C::OFF_V, 16) : sdesc_lo(sbase + C::OFF_V, 128 * 128);
+      const uint32_t dP8 = sdesc_lo(sbase + C::OFF_P + s * 128 * 128, 16);
       const uint32_t tS = tbase + 128 * s, tO = tbase + 256 + 128 * s;
       uint32_t qn = 0, np = 0, un = 0;
       // entry word of entry e, once its K tile (and bits) have landed
@@ -491,9 +520,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         tc_fence_after();
         const uint32_t dK = dK0 + (e & 1) * (C::TILE >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < C::KSTEPS; ++kk) {
           const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tS, sdesc_at(dQ, koff), sdesc_at(dK, koff), idS, kk > 0 ? 1u : 0u);
+          if constexpr (F8) mma_ss_f8(tS, sdesc_at(dQ, koff), sdesc_at(dK, koff), idS, kk > 0 ? 1u : 0u);
+          else mma_ss(tS, sdesc_at(dQ, koff), sdesc_at(dK, koff), idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(B_SFULL0 + s));
         if (f & fLAST) mma_commit(bar(B_QEMPTY0 + s));
@@ -512,9 +542,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         if (!wait(B_VFULL0 + st, (e >> 1) & 1)) return false;
         tc_fence_after();
         const uint32_t dV = dV0 + st * (C::TILE >> 4);
+        if constexpr (F8) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tO, tS + kk * 8, sdesc_at(dV, kk * 2048), idPV, (!first || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)  // 128 keys, 32 per MMA
+            mma_ss_f8(tO, sdesc_at(dP8, kk * 32), sdesc_at(dV, kk * 32), idPV,
+                      (!first || kk > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tO, tS + kk * 8, sdesc_at(dV, kk * 2048), idPV, (!first || kk > 0) ? 1u : 0u);
+        }
         // the epilogue reads O after the unit's last PV only
         if (f & fLAST) mma_commit(bar(B_PVDONE0 + s));
         return true;
@@ -586,6 +623,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       float m_used = -INFINITY, l = 0.f;  // running max (base-2 exponent domain) and sum
       int done = 0;                       // tiles of this unit done
+      // F8: this row's Q tile scale, the K/V head's scales
+      const int hk = u.h / P.G;
+      const float sq_row = F8 ? P.q_scale[(static_cast<size_t>(u.b) * P.H + u.h) * P.nQ + qt] : 1.f;
+      const size_t kv_row = (static_cast<size_t>(u.b) * (P.H / P.G) + hk) * P.nK;
+      const float sv_head = F8 ? P.v_head_scale[static_cast<size_t>(u.b) * (P.H / P.G) + hk] : 1.f;
       for (int t = 0; t < u.n; ++t, ++e) {
         const int ent = P.pair_list[static_cast<size_t>(u.prow) * P.nK + t];
         const int cls = slot ? (ent & 3) : ((ent >> 2) & 3);
@@ -632,12 +674,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         for (int x = 0; x < 8; ++x) mx8[x] = fmaxf(mx8[x], sv[120 + x]);
         const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
                                fmaxf(mx8[6], mx8[7]));
-        const float m_tile = mx * P.scale_log2;
+        // S * scale * log2 e; F8: times the Q and K tile scales
+        float ct = P.scale_log2, vr = 1.f;
+        if constexpr (F8) {
+          const int kj = ent >> 4;
+          ct *= sq_row * P.k_scale[kv_row + kj];
+          vr = P.v_scale[kv_row + kj] / sv_head;  // this V tile's scale ratio, <= 1
+        }
+        const float m_tile = mx * ct;
         // lazy rescale: move the reference max only when it grows by more than
         // 8 (factor 256); below that the unnormalised p stay within bf16/fp32
         // range and the result is unchanged
         const bool grow = m_tile > m_used + 8.f;
-        const float m_new = grow ? m_tile : m_used;
+        // F8: an integral reference, so every rescale is a power of two and
+        // P's e4m3 codes do not depend on when the reference moved
+        const float m_new = grow ? (F8 ? ceilf(m_tile) : m_tile) : m_used;
         const float alpha = grow ? ex2(m_used - m_new) : 1.f;  // m_used = -inf gives 0
         l *= alpha;
         m_used = m_new;
@@ -645,8 +696,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         // p = exp2(s * scale*log2e - m) from the registers, packed to bf16 into
         // the first 64 columns of S (the row was read whole above)
         // two columns per packed FMA and per packed add
-        const uint64_t sc2 = splat2(P.scale_log2), nm2 = splat2(-m_ref);
+        const uint64_t sc2 = splat2(ct), nm2 = splat2(-m_ref);
         float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        // F8: row r of the slot's P tile (128 bytes, 128-byte swizzle)
+        const uint32_t prow = sbase + C::OFF_P + slot * 128 * 128 + r * 128;
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           uint32_t pk[16];
@@ -658,9 +711,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             const float p1 = ex2(a1);
             if (x & 1) add2_acc(sum4[2], sum4[3], p0, p1);
             else add2_acc(sum4[0], sum4[1], p0, p1);
-            pk[x] = pack_bf16(p0, p1);
+            if constexpr (F8) {
+              const uint32_t h = pack_e4m3x2(p0 * vr, p1 * vr);
+              pk[x >> 1] = (x & 1) ? (pk[x >> 1] | (h << 16)) : h;
+            } else {
+              pk[x] = pack_bf16(p0, p1);
+            }
           }
-          tmem_st16(tS + c4 * 16, pk);
+          if constexpr (F8) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+              st_shared_v4(prow + (static_cast<uint32_t>(c4 * 2 + k) ^ static_cast<uint32_t>(r & 7)) * 16,
+                           pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          } else {
+            tmem_st16(tS + c4 * 16, pk);
+          }
         }
         const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
         // rescale O by alpha (after P: the S registers are free by now).  O
@@ -678,6 +743,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
         l += sum;
         tmem_wait_st();
+        if constexpr (F8) fence_proxy_async_smem();  // P (smem) is read by the tensor cores
         tc_fence_before();
         // (a test of the wait limit withholds the first P-ready arrival of
         // slot a: the slot's MMA thread then gives up on it and the launch
@@ -692,7 +758,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       if (!wait_all(B_PVDONE0 + slot, pd & 1)) break;
       ++pd;
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? sv_head / l : 0.f;
       uint32_t ro[D];
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + c * 32, ro + 32 * c);
@@ -721,15 +787,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   }
 }
 
-template <int D>
+template <int D, bool F8>
 static fm_status launch_fwd_d(const Plan& p, const fm_desc& desc, const TensorArgs& t, char* ws,
-                              cudaStream_t s) {
-  using C = FwdCfg<D>;
+                              cudaStream_t s, const Fp8Args* f8 = nullptr) {
+  using C = FwdCfg<D, F8>;
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_bshd(&tq, t.q, p.B, p.Sq, p.H, D, desc.q_stride, 128) ||
-      !make_tmap_bshd(&tk, t.k, p.B, p.Skv, p.Hkv, D, desc.k_stride, 128) ||
-      !make_tmap_bshd(&tv, t.v, p.B, p.Skv, p.Hkv, D, desc.v_stride, 128))
+  if constexpr (F8) {
+    if (!make_tmap_bshd8(&tq, f8->q8, p.B, p.Sq, p.H, D, 128) ||
+        !make_tmap_bshd8(&tk, f8->k8, p.B, p.Skv, p.Hkv, D, 128) ||
+        !make_tmap_vt8(&tv, f8->v8t, p.B, p.Hkv, D, p.nK * 128))
+      return FM_ERR_CUDA;
+  } else if (!make_tmap_bshd(&tq, t.q, p.B, p.Sq, p.H, D, desc.q_stride, 128) ||
+             !make_tmap_bshd(&tk, t.k, p.B, p.Skv, p.Hkv, D, desc.k_stride, 128) ||
+             !make_tmap_bshd(&tv, t.v, p.B, p.Skv, p.Hkv, D, desc.v_stride, 128)) {
     return FM_ERR_CUDA;
+  }
   FwdParams P{};
   P.B = p.B; P.H = p.H; P.Hm = p.Hm; P.Sq = p.Sq; P.Skv = p.Skv; P.nQ = p.nQ; P.nK = p.nK;
   P.G = p.G;
@@ -750,7 +822,13 @@ static fm_status launch_fwd_d(const Plan& p, const fm_desc& desc, const TensorAr
   const TestHooks th = test_hooks();
   P.wait_ns = th.wait_ns;
   P.withhold = th.withhold;
-  auto kern = fwd_kernel<D>;
+  if (f8) {
+    P.q_scale = f8->q_scale;
+    P.k_scale = f8->k_scale;
+    P.v_scale = f8->v_scale;
+    P.v_head_scale = f8->v_head_scale;
+  }
+  auto kern = fwd_kernel<D, F8>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)
     return FM_ERR_CUDA;
@@ -761,17 +839,23 @@ static fm_status launch_fwd_d(const Plan& p, const fm_desc& desc, const TensorAr
     if (fa.numRegs < C::MIN_LAUNCH_REGS) return FM_ERR_UNSUPPORTED;
   }
   const int grid = P.n_units < num_sms() ? P.n_units : num_sms();
-  prof_begin(K_FWD, s);
+  prof_begin(F8 ? K_FWD8 : K_FWD, s);
   kern<<<grid, C::THREADS, C::SMEM, s>>>(P, tq, tk, tv);
-  prof_end(K_FWD, s);
+  prof_end(F8 ? K_FWD8 : K_FWD, s);
   return cudaGetLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
 fm_status launch_fwd(const Plan& p, const fm_desc& desc, const TensorArgs& t, char* ws,
                      cudaStream_t s) {
-  if (p.d == 64) return launch_fwd_d<64>(p, desc, t, ws, s);
-  if (p.d == 128) return launch_fwd_d<128>(p, desc, t, ws, s);
+  if (p.d == 64) return launch_fwd_d<64, false>(p, desc, t, ws, s);
+  if (p.d == 128) return launch_fwd_d<128, false>(p, desc, t, ws, s);
   return FM_ERR_UNSUPPORTED;
+}
+
+fm_status launch_fwd_fp8(const Plan& p, const fm_desc& desc, const TensorArgs& t,
+                         const Fp8Args& f, char* ws, cudaStream_t s) {
+  if (p.d != 128) return FM_ERR_UNSUPPORTED;
+  return launch_fwd_d<128, true>(p, desc, t, ws, s, &f);
 }
 
 }  // namespace fm

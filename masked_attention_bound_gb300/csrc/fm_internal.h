@@ -66,6 +66,17 @@ fm_status launch_fwd(const Plan& p, const fm_desc& desc, const TensorArgs& t, ch
                      cudaStream_t s);
 fm_status launch_bwd(const Plan& p, const fm_desc& desc, const TensorArgs& t, char* ws,
                      cudaStream_t s);
+// FP8 forward: per-tile e4m3 quantisation (fm_quant.cu) and the forward
+// kernel on the codes (fm_fwd.cu); d = 128 only
+fm_status launch_quantize_fp8(const Plan& p, const fm_desc& desc, const void* q, const void* k,
+                              const void* v, void* q8, void* k8, void* v8t, float* q_scale,
+                              float* k_scale, float* v_scale, float* v_head_scale, cudaStream_t s);
+struct Fp8Args {
+  const void* q8; const void* k8; const void* v8t;
+  const float* q_scale; const float* k_scale; const float* v_scale; const float* v_head_scale;
+};
+fm_status launch_fwd_fp8(const Plan& p, const fm_desc& desc, const TensorArgs& t,
+                         const Fp8Args& f, char* ws, cudaStream_t s);
 
 int num_sms();
 
@@ -79,7 +90,7 @@ TestHooks test_hooks();
 
 // Kernel ids for the timing hooks (fm_profile_*).
 enum KernelId : int { K_SUMMARY = 0, K_CLASSIFY, K_ORDER, K_LOCALIZE, K_FWD, K_BWD_PRE, K_BWD,
-                      K_BWD_DQ, K_TILE_MASKS, K_COUNT };
+                      K_BWD_DQ, K_TILE_MASKS, K_QUANT, K_FWD8, K_COUNT };
 void prof_begin(int id, cudaStream_t s);
 void prof_end(int id, cudaStream_t s);
 

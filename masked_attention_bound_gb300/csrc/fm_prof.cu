@@ -127,7 +127,8 @@ fm_status fm_profile_read(double* total_ms, int* launches, int n) {
 const char* fm_kernel_name(int id) {
   static const char* names[K_COUNT] = {"summary_kernel", "classify_kernel", "order_kernel",
                                        "localize_kernel", "fwd_kernel", "bwd_pre_kernel",
-                                       "bwd_kv_kernel", "bwd_dq_kernel", "tile_mask_kernel"};
+                                       "bwd_kv_kernel", "bwd_dq_kernel", "tile_mask_kernel",
+                                       "quant_kernel", "fwd_fp8_kernel"};
   return (id >= 0 && id < K_COUNT) ? names[id] : "unknown";
 }
 

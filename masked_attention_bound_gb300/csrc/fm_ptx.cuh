@@ -155,6 +155,16 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
       : "memory");
 }
 // Same with the A operand read from tensor memory (lane = row of A).
+// The same with 8-bit operands (kind::f8f6f4; K = 32 per MMA).
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -271,6 +281,13 @@ __device__ __forceinline__ uint64_t sdesc_at(uint32_t lo, uint32_t bytes) {
   return (static_cast<uint64_t>(kSdescHi) << 32) | (lo + (bytes >> 4));
 }
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulation.
+// Instruction descriptor of a kind::f8f6f4 MMA with e4m3 A and B (format
+// code 0 in both fields) and an f32 accumulator; both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4)                                  // D format: f32
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4)                                  // D format: f32
          | (1u << 7)                                // A format: bf16
@@ -296,6 +313,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+// Two floats to e4m3 (as pack_e4m3x4), x0 in the low byte of the result.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float x0, float x1) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(x1), "f"(x0));
+  return r;
+}
+// Four floats to e4m3 (nearest, ties to even, saturating at +-448), x0 in
+// the lowest byte: the order of consecutive K elements in a K-major tile.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float x0, float x1, float x2, float x3) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(x1), "f"(x0));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(x3), "f"(x2));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 __device__ __forceinline__ float ex2(float x) {
   float y;

@@ -44,4 +44,37 @@ inline bool make_tmap_bshd(CUtensorMap* m, const void* base, int B, int S, int H
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// e4m3 codes (one byte each): BSHD with head_dim 128 contiguous, one box =
+// `box_rows` rows x 128 elements (one 128-byte swizzle slab).
+inline bool make_tmap_bshd8(CUtensorMap* m, const void* base, int B, int S, int H, int D,
+                            int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H) * D,
+                           static_cast<cuuint64_t>(S) * H * D};
+  cuuint32_t box[4] = {128, 1, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// e4m3 V^T codes [B][H][D][S_pad] (keys contiguous): one box = 128 keys x 128
+// head_dim rows of one (batch, head).
+inline bool make_tmap_vt8(CUtensorMap* m, const void* base, int B, int H, int D, int S_pad) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(S_pad), static_cast<cuuint64_t>(D),
+                        static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(S_pad), static_cast<cuuint64_t>(D) * S_pad,
+                           static_cast<cuuint64_t>(H) * D * S_pad};
+  cuuint32_t box[4] = {128, 128, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace fm
