@@ -247,15 +247,16 @@ def run_ours(args):
                                    ws, stream, world)
     # the secondary (exp2) ceiling, measured outside the timed regions
     exp2_rate = fm.measure_exp2_rate(stream) if rank == 0 else None
-    per_mask = None
+    per_mask = fp8_points = None
     if not args.no_per_mask and rank == 0:
         del q, k, v, do, o, lse, dq, dk, dv, ws
         torch.cuda.empty_cache()
         per_mask = run_per_mask(args, fm)
+        fp8_points = run_fp8_points(args, fm)
     if world > 1:
         dist.barrier()
     report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2d, d2h, clk,
-           per_mask, exp2_rate)
+           per_mask, exp2_rate, fp8_points)
     if world > 1:
         dist.destroy_process_group()
 
@@ -337,6 +338,70 @@ def run_e2e(args, fm, q, k, v, do, bounds, scale, o, lse, dq, dk, dv, ws, stream
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo, hb))
     d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdq, hdk, hdv))
     return e2e_ms, h2d, d2h
+
+
+# FP8 (e4m3) forward points: (workload, B, H, S, mask, params)
+FP8_POINTS = (
+    ("suite_32k", 1, 32, 32768, "causal", {}),
+    ("suite_32k", 1, 32, 32768, "causal_document", {}),
+    ("long_128k", 1, 8, 131072, "causal_document_window", {"window": 8192}),
+)
+
+
+def run_fp8_points(args, fm):
+    """FP8 forward throughput on pre-quantised inputs (fm_quantize_fp8 timed
+    apart), beside the bf16 forward on the same inputs; effective TFLOP/s on
+    the visible entries (4 * d flop each) against the fp8 peak taken as the
+    measured bf16 peak times 2 (the nominal dense fp8 / bf16 ratio)."""
+    import torch
+
+    from fm_inputs.tensors import qkv_do
+    peak = float(_peaks()[0]["bf16_tflops"])
+    stream = torch.cuda.current_stream()
+    out = []
+    for name, B, H, S, mask, params in FP8_POINTS:
+        q, k, v, _ = qkv_do(B, S, S, H, 128, seed=0, device="cuda")
+        bounds = _point_bounds(fm, mask, B, S, params)
+        n_vis = _visible_entries(bounds.cpu().numpy(), S, H)
+        scale = 128 ** -0.5
+        o = torch.empty_like(q)
+        lse = torch.empty(B, H, S, dtype=torch.float32, device="cuda")
+        desc = fm.make_desc(q, k, v, o)
+        ws = fm.workspace(desc, fm.WS_FWD)
+        f = fm.quantize_fp8(q, k, v, stream=stream)
+        n = args.mask_steps
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        for i in range(2 + n):
+            if i == 2:
+                ev[0].record(stream)
+            fm.quantize_fp8(q, k, v, stream=stream)
+            if i == 2:
+                ev[1].record(stream)
+        ev[2].record(stream)
+        for i in range(n):
+            fm.forward_fp8(f, bounds, scale, o=o, lse=lse, ws=ws, stream=stream)
+        ev[3].record(stream)
+        for i in range(n):
+            fm.forward(q, k, v, bounds, scale, o=o, lse=lse, ws=ws, stream=stream)
+        ev[4].record(stream)
+        torch.cuda.synchronize()
+        if fm.device_status(ws) != 0:
+            raise RuntimeError(f"device status not OK for fp8 {name}/{mask}")
+        f8_ms = ev[2].elapsed_time(ev[3]) / n
+        bf_ms = ev[3].elapsed_time(ev[4]) / n
+        flop = 4.0 * 128 * n_vis
+        t8 = flop / (f8_ms * 1e-3) / 1e12
+        out.append({"workload": name, "mask": mask, "B": B, "H": H, "S": S, "d": 128,
+                    "visible_entries": n_vis, "fwd_fp8_ms": round(f8_ms, 4),
+                    "fwd_fp8_tflops": round(t8, 1),
+                    "pct_fp8_peak": round(100.0 * t8 / (2 * peak), 1),
+                    "fwd_bf16_ms": round(bf_ms, 4),
+                    "fwd_bf16_tflops": round(flop / (bf_ms * 1e-3) / 1e12, 1),
+                    "quantize_ms": round(ev[0].elapsed_time(ev[1]), 4),
+                    "peak": "fp8 = 2 x bf16_tflops (burst) of measured"})
+        del q, k, v, o, f, ws
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_per_mask(args, fm):
@@ -490,7 +555,7 @@ def exp2_ceiling(rate, d):
 
 
 def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2d, d2h, clk,
-           per_mask=None, exp2_rate=None):
+           per_mask=None, exp2_rate=None, fp8_points=None):
     B, H, S, d = W["B"], W["H"], W["S"], W["d"]
     flop_step = flop_fwd + flop_bwd
     if rank == 0:
@@ -552,6 +617,8 @@ def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2
         }
         if per_mask is not None:
             out["per_mask"] = per_mask
+        if fp8_points is not None:
+            out["fp8_forward"] = fp8_points
         if not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
         print(json.dumps(out), flush=True)
