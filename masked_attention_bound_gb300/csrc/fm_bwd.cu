@@ -1208,17 +1208,24 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive_warp(bar(Q_DQEMPTY));
-      if (prow < P.Sq) {
-        uint4* dst = reinterpret_cast<uint4*>(P.out0 + pb * P.s0[0] +
-                                              static_cast<int64_t>(prow) * P.s0[1] + ph * P.s0[2] +
-                                              half * (D / 2));
+      {
+        // this thread's half row as NC 16-byte chunks, regrouped so that each
+        // store instruction writes whole 16 * NC-byte runs of NC rows instead
+        // of 16 bytes of 32 rows
+        constexpr int NC = D / 16;
+        uint32_t pk[4 * NC];
         const float sc = P.scale;
 #pragma unroll
-        for (int i = 0; i < D / 16; ++i)
-          dst[i] = make_uint4(pack_bf16(__uint_as_float(rq[8 * i + 0]) * sc, __uint_as_float(rq[8 * i + 1]) * sc),
-                              pack_bf16(__uint_as_float(rq[8 * i + 2]) * sc, __uint_as_float(rq[8 * i + 3]) * sc),
-                              pack_bf16(__uint_as_float(rq[8 * i + 4]) * sc, __uint_as_float(rq[8 * i + 5]) * sc),
-                              pack_bf16(__uint_as_float(rq[8 * i + 6]) * sc, __uint_as_float(rq[8 * i + 7]) * sc));
+        for (int i = 0; i < 4 * NC; ++i)
+          pk[i] = pack_bf16(__uint_as_float(rq[2 * i]) * sc, __uint_as_float(rq[2 * i + 1]) * sc);
+        transpose_chunks<NC>(pk);
+        const int row0 = prow - lane + (lane & ~(NC - 1));  // q row of this lane group's first row
+        __nv_bfloat16* base = P.out0 + pb * P.s0[0] + ph * P.s0[2] + half * (D / 2) + (lane & (NC - 1)) * 8;
+#pragma unroll
+        for (int i = 0; i < NC; ++i)
+          if (row0 + i < P.Sq)
+            *reinterpret_cast<uint4*>(base + static_cast<int64_t>(row0 + i) * P.s0[1]) =
+                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
       }
       pending = false;
       return true;

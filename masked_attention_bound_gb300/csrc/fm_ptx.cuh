@@ -388,4 +388,37 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// Row-per-lane data (lane L holds NC 16-byte chunks of row L, chunk i in
+// c[4i .. 4i+3]) regrouped for coalesced stores: within each group of NC
+// lanes, an NC x NC transpose of the chunks in log2(NC) butterfly stages
+// (stage b swaps bit b of the lane and of the chunk index through one
+// exchange with lane ^ 2^b).  Afterwards lane NC*g + j holds in c[4i ..]
+// chunk j of row NC*g + i, so the i-th store of the warp writes NC rows of
+// NC contiguous chunks each, instead of 32 rows of 16 bytes.
+template <int NC>
+__device__ __forceinline__ void transpose_chunks(uint32_t (&c)[4 * NC]) {
+  static_assert(NC == 4 || NC == 8, "groups of 4 or 8 lanes");
+  const int j = threadIdx.x & (NC - 1);
+#pragma unroll
+  for (int b = 0; (1 << b) < NC; ++b) {
+    const int m = 1 << b;
+    const bool upper = ((j >> b) & 1) != 0;
+#pragma unroll
+    for (int k = 0; k < NC / 2; ++k) {
+      // the pair of chunks whose indices differ in bit b only
+      const int lo = ((k >> b) << (b + 1)) | (k & (m - 1));
+      const int hi = lo | m;
+      // a lane sends the chunk whose bit b differs from its own lane bit and
+      // puts the partner's chunk in its place
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t send = upper ? c[4 * lo + w] : c[4 * hi + w];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
+        if (upper) c[4 * lo + w] = recv;
+        else c[4 * hi + w] = recv;
+      }
+    }
+  }
+}
+
 }  // namespace fm
