@@ -207,10 +207,11 @@ def run_ours(args):
     ws = fm.workspace(desc, fm.WS_STEP)
     stream = torch.cuda.current_stream()
 
-    def step():
-        fm.plan(q, k, bounds, ws=ws, for_bwd=fm.WS_STEP, stream=stream)
-        fm.forward(q, k, v, bounds, scale, o=o, lse=lse, ws=ws, stream=stream, planned=True)
-        fm.backward(q, k, v, o, lse, do, bounds, scale, dq=dq, dk=dk, dv=dv, ws=ws, stream=stream,
+    def step(st=None):
+        st = stream if st is None else st
+        fm.plan(q, k, bounds, ws=ws, for_bwd=fm.WS_STEP, stream=st)
+        fm.forward(q, k, v, bounds, scale, o=o, lse=lse, ws=ws, stream=st, planned=True)
+        fm.backward(q, k, v, o, lse, do, bounds, scale, dq=dq, dk=dk, dv=dv, ws=ws, stream=st,
                     planned=True)
 
     for _ in range(args.warmup):
@@ -219,26 +220,50 @@ def run_ours(args):
     if fm.device_status(ws) != 0:
         raise RuntimeError("device status not OK after warm-up")
 
-    # ---- timed region: K steps, inputs (1 GiB of Q/K/V/dO) larger than L2
+    def timed(run, n):
+        """ms per call of run() over n calls, events on the launching stream,
+        barrier and synchronize on both sides, max over ranks."""
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(n):
+            run()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        return _max_over_ranks(ev0.elapsed_time(ev1) / n, world, "cuda")
+
+    # ---- timed regions: K steps each, inputs (1 GiB of Q/K/V/dO) larger
+    # than L2.  The headline has no per-kernel events (they add about 2 % to
+    # a step); the same K steps are then run with the library's per-kernel
+    # events for the breakdown and the roofline, and replayed once more as a
+    # CUDA graph of the step.
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
+    ms = timed(step, args.steps)
     fm.profile_enable(True)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    prof_ms = timed(step, args.steps)
     fm.profile_enable(False)
     prof = fm.profile_read()
     clk = clocks.stop()
-    ms = _max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, "cuda")
+    graph_ms = None
+    if not args.no_graph:
+        # captured on a side stream (capture needs a non-default stream),
+        # replayed on the timing stream
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            step(side)
+        stream.wait_stream(side)
+        graph.replay()
+        graph_ms = timed(graph.replay, args.steps)
+    if fm.device_status(ws) != 0:
+        raise RuntimeError("device status not OK after the timed steps")
 
     if args.no_e2e:
         e2e_ms, h2d, d2h = float("nan"), 0, 0
@@ -256,7 +281,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2d, d2h, clk,
-           per_mask, exp2_rate, fp8_points)
+           per_mask, exp2_rate, fp8_points, prof_ms=prof_ms, graph_ms=graph_ms)
     if world > 1:
         dist.destroy_process_group()
 
@@ -555,7 +580,7 @@ def exp2_ceiling(rate, d):
 
 
 def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2d, d2h, clk,
-           per_mask=None, exp2_rate=None, fp8_points=None):
+           per_mask=None, exp2_rate=None, fp8_points=None, prof_ms=None, graph_ms=None):
     B, H, S, d = W["B"], W["H"], W["S"], W["d"]
     flop_step = flop_fwd + flop_bwd
     if rank == 0:
@@ -584,6 +609,12 @@ def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2
             "steps": args.steps,
             "warmup": args.warmup,
             "ms_per_step": round(ms, 4),
+            "profiled_ms_per_step": None if prof_ms is None else round(prof_ms, 4),
+            "graph_ms_per_step": None if graph_ms is None else round(graph_ms, 4),
+            "timing": "ms_per_step: the step through the public API, no per-kernel events; "
+                      "profiled_ms_per_step: the same K steps with per-kernel CUDA events "
+                      "(kernel_ms_per_step, roofline); graph_ms_per_step: the step captured "
+                      "once as a CUDA graph and replayed K times",
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
@@ -716,6 +747,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-per-mask", action="store_true",
                     help="skip the per-(workload, mask) measurements after the headline step")
     ap.add_argument("--mask-steps", type=int, default=5, help="timed steps per (workload, mask)")

@@ -287,7 +287,7 @@ fm_status fm_varlen_bounds(const int32_t* cu_seqlens, int n_seqs, int total, int
  * total_ms[0..n) and launches[0..n) (either may be NULL), and clears the
  * record.  Kernel ids: 0 block summary, 1 classify, 2 unit order,
  * 3 localize, 4 forward, 5 backward preprocess, 6 backward dK/dV, 7 backward
- * dQ, 8 partial-tile visibility masks;
+ * dQ, 8 partial-tile visibility masks, 9 FP8 quantisation, 10 FP8 forward;
  * fm_kernel_name(id) names them.  At most 65536 launches are recorded per
  * read; later launches are counted but not timed. */
 fm_status fm_profile_enable(int on);
