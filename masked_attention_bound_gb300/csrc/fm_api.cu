@@ -106,10 +106,10 @@ static fm_status run_plan(const Plan& p, const int32_t* lts, const int32_t* lte,
   if (launch_summary(p, lts, lte, uts, ute, ws, s) != cudaSuccess) return FM_ERR_CUDA;
   if (launch_classify(p, ws, mode, s) != cudaSuccess) return FM_ERR_CUDA;
   if (launch_tile_masks(p, lts, lte, uts, ute, ws, s) != cudaSuccess) return FM_ERR_CUDA;
-  if (mode != FM_WS_BWD && launch_order(p, ws, ORDER_PAIRS, s) != cudaSuccess) return FM_ERR_CUDA;
-  if (mode != FM_WS_FWD && (launch_order(p, ws, ORDER_COLS, s) != cudaSuccess ||
-                            launch_order(p, ws, ORDER_ROWS, s) != cudaSuccess))
-    return FM_ERR_CUDA;
+  unsigned orders = 0;
+  if (mode != FM_WS_BWD) orders |= 1u << ORDER_PAIRS;
+  if (mode != FM_WS_FWD) orders |= (1u << ORDER_COLS) | (1u << ORDER_ROWS);
+  if (launch_orders(p, ws, orders, s) != cudaSuccess) return FM_ERR_CUDA;
   return FM_OK;
 }
 

@@ -39,7 +39,8 @@ cudaError_t launch_classify(const Plan& p, char* ws, int mode, cudaStream_t s);
 // unit orders: ORDER_PAIRS (forward, q-tile pairs), ORDER_COLS (dK/dV, k-tile
 // columns), ORDER_ROWS (dQ, q-tile rows)
 enum : int { ORDER_PAIRS = 0, ORDER_COLS, ORDER_ROWS };
-cudaError_t launch_order(const Plan& p, char* ws, int which, cudaStream_t s);
+// builds the orders whose bits (1 << ORDER_*) are set in `which`, in one launch
+cudaError_t launch_orders(const Plan& p, char* ws, unsigned which, cudaStream_t s);
 cudaError_t launch_varlen_bounds(const int32_t* cu, int n, int total, int causal, int32_t* out,
                                  int* bad, cudaStream_t s);
 cudaError_t launch_tile_masks(const Plan& p, const int32_t* lts, const int32_t* lte,

@@ -88,15 +88,12 @@ __device__ __forceinline__ void load_summary(const int32_t* p, int* s) {
 // PARTIAL, or the ragged last key tile) and reserves that many consecutive
 // slots of the visibility-mask region (row_mask = first slot, -1 if none or
 // if the region is full: the forward then builds those tiles' bits itself).
-__global__ void __launch_bounds__(256) classify_rows_kernel(const int32_t* __restrict__ summary,
-                                                            int nBH, int nQ, int nK, int Sq,
-                                                            int Skv, uint8_t* table,
-                                                            int32_t* row_count,
-                                                            int32_t* row_list, int32_t* row_mask,
-                                                            unsigned long long* slot_counter,
-                                                            int mask_cap) {
+__device__ __forceinline__ void classify_row(int w, const int32_t* __restrict__ summary, int nBH,
+                                             int nQ, int nK, int Sq, int Skv, uint8_t* table,
+                                             int32_t* row_count, int32_t* row_list,
+                                             int32_t* row_mask, unsigned long long* slot_counter,
+                                             int mask_cap) {
   const int lane = threadIdx.x & 31;
-  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (w >= nBH * nQ) return;
   const int bh = w / nQ, qi = w - bh * nQ;
   const int r0 = qi * kTile, r1 = min(r0 + kTile, Sq);
@@ -265,14 +262,11 @@ __global__ void __launch_bounds__(256) classify_pairs_kernel(const uint8_t* __re
 }
 
 // One warp per (bh, k-tile): the ascending list of non-empty q-tiles.
-__global__ void __launch_bounds__(256) classify_cols_kernel(const int32_t* __restrict__ summary,
-                                                            int nBH, int nQ, int nK, int Sq,
-                                                            uint8_t* table, int32_t* col_count,
-                                                            int32_t* col_list) {
+__device__ __forceinline__ void classify_col(int w, const int32_t* __restrict__ summary, int nBH,
+                                             int nQ, int nK, int Sq, int32_t* col_count,
+                                             int32_t* col_list) {
   const int lane = threadIdx.x & 31;
-  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (w >= nBH * nK) return;
-  const int bh = w / nK, kj = w - bh * nK;
   int s[8];
   load_summary(summary + static_cast<size_t>(w) * 8, s);
   int32_t* lst = col_list + static_cast<size_t>(w) * nQ;
@@ -283,14 +277,30 @@ __global__ void __launch_bounds__(256) classify_cols_kernel(const int32_t* __res
     int cls = CLS_EMPTY;
     if (qi < nQ) {
       const int r0 = qi * kTile;
-      cls = classify(s, r0, min(r0 + kTile, Sq));
-      table[(static_cast<size_t>(bh) * nQ + qi) * nK + kj] = static_cast<uint8_t>(cls);
+      cls = classify(s, r0, min(r0 + kTile, Sq));  // the rows' pass writes the table
     }
     const unsigned m = __ballot_sync(0xffffffffu, cls != CLS_EMPTY);
     if (cls != CLS_EMPTY) lst[cnt + __popc(m & lt_mask)] = (qi << 2) | cls;
     cnt += __popc(m);
   }
   if (lane == 0) col_count[w] = cnt;
+}
+
+// Rows and columns in one launch (both read only the block summary): blocks
+// [0, row_blocks) classify q-tile rows, the rest k-tile columns (none when
+// col_list is null).  Eight warps per block, one row or column each.
+__global__ void __launch_bounds__(256) classify_rows_cols_kernel(
+    const int32_t* __restrict__ summary, int nBH, int nQ, int nK, int Sq, int Skv,
+    uint8_t* table, int32_t* row_count, int32_t* row_list, int32_t* row_mask,
+    unsigned long long* slot_counter, int mask_cap, int row_blocks, int32_t* col_count,
+    int32_t* col_list) {
+  const int wib = threadIdx.x >> 5;
+  if (static_cast<int>(blockIdx.x) < row_blocks)
+    classify_row(blockIdx.x * 8 + wib, summary, nBH, nQ, nK, Sq, Skv, table, row_count, row_list,
+                 row_mask, slot_counter, mask_cap);
+  else
+    classify_col((blockIdx.x - row_blocks) * 8 + wib, summary, nBH, nQ, nK, Sq, col_count,
+                 col_list);
 }
 
 // ------------------------------------------------------------------ order
@@ -301,16 +311,34 @@ __global__ void __launch_bounds__(256) classify_cols_kernel(const int32_t* __res
 // One block per (b, unit head h); Hu = H / G unit heads.  G > 1: the units
 // belong to K/V heads, each shared by query heads h*G .. h*G+G-1, and a
 // unit's cost is the sum of their counts (maxc covers the sum).
-__global__ void __launch_bounds__(256) order_kernel(const int32_t* __restrict__ counts,
-                                                    int stride, int H, int Hm, int G, int nT,
-                                                    int maxc, int32_t* order) {
+// Up to three orders are built by one launch: blocks [0, jobs[0].blocks)
+// make the first, the next jobs[1].blocks the second, and so on.
+struct OrderJob {
+  const int32_t* counts;
+  int stride, G, nT, maxc, blocks;
+  int32_t* order;
+};
+struct OrderJobs {
+  OrderJob job[3];
+  int n;
+};
+
+__global__ void __launch_bounds__(256) order_kernel(const __grid_constant__ OrderJobs J, int H,
+                                                    int Hm) {
+  int bh = blockIdx.x, ji = 0;
+  while (ji + 1 < J.n && bh >= J.job[ji].blocks) {
+    bh -= J.job[ji].blocks;
+    ++ji;
+  }
+  const int32_t* __restrict__ counts = J.job[ji].counts;
+  const int stride = J.job[ji].stride, G = J.job[ji].G, nT = J.job[ji].nT, maxc = J.job[ji].maxc;
+  int32_t* order = J.job[ji].order;
   extern __shared__ int sh[];
   int* hist = sh;             // maxc + 1
   int* cst = sh + maxc + 1;   // nT costs of this (b, h)
   __shared__ int wsum[8];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Hu = H / G;
-  const int bh = blockIdx.x;
   const int b = bh / Hu, h = bh - b * Hu;
   for (int i = tid; i <= maxc; i += blockDim.x) hist[i] = 0;
   for (int t = tid; t < nT; t += blockDim.x) {
@@ -450,23 +478,20 @@ cudaError_t launch_classify(const Plan& p, char* ws, int mode, cudaStream_t s) {
   const int32_t* summ = reinterpret_cast<const int32_t*>(ws + p.L.summary);
   uint8_t* table = reinterpret_cast<uint8_t*>(ws + p.L.table);
   prof_begin(K_CLASSIFY, s);
-  // q-tile rows (with their mask slots): the forward's pairs are built from
-  // them, and the dQ pass walks them
-  classify_rows_kernel<<<ceil_div(nBH * p.nQ, 8), 256, 0, s>>>(
+  // q-tile rows (with their mask slots: the forward's pairs are built from
+  // them, and the dQ pass walks them) and, for the backward, k-tile columns
+  const int row_blocks = ceil_div(nBH * p.nQ, 8);
+  const int col_blocks = mode != FM_WS_FWD ? ceil_div(nBH * p.nK, 8) : 0;
+  classify_rows_cols_kernel<<<row_blocks + col_blocks, 256, 0, s>>>(
       summ, nBH, p.nQ, p.nK, p.Sq, p.Skv, table, reinterpret_cast<int32_t*>(ws + p.L.row_count),
       reinterpret_cast<int32_t*>(ws + p.L.row_list), reinterpret_cast<int32_t*>(ws + p.L.row_mask),
-      reinterpret_cast<unsigned long long*>(ws + p.L.status + 8), p.mask_cap);
+      reinterpret_cast<unsigned long long*>(ws + p.L.status + 8), p.mask_cap, row_blocks,
+      reinterpret_cast<int32_t*>(ws + p.L.col_count), reinterpret_cast<int32_t*>(ws + p.L.col_list));
   if (mode != FM_WS_BWD) {
     const int pwarps = nBH * p.nP;
     classify_pairs_kernel<<<ceil_div(pwarps, 8), 256, 0, s>>>(
         table, nBH, p.nQ, p.nK, p.nP, p.Skv, reinterpret_cast<int4*>(ws + p.L.pair_info),
         reinterpret_cast<int32_t*>(ws + p.L.pair_list));
-  }
-  if (mode != FM_WS_FWD) {
-    const int warps = nBH * p.nK;
-    classify_cols_kernel<<<ceil_div(warps, 8), 256, 0, s>>>(
-        summ, nBH, p.nQ, p.nK, p.Sq, table, reinterpret_cast<int32_t*>(ws + p.L.col_count),
-        reinterpret_cast<int32_t*>(ws + p.L.col_list));
   }
   prof_end(K_CLASSIFY, s);
   return cudaGetLastError();
@@ -483,36 +508,45 @@ cudaError_t launch_tile_masks(const Plan& p, const int32_t* lts, const int32_t* 
   return cudaGetLastError();
 }
 
-cudaError_t launch_order(const Plan& p, char* ws, int which, cudaStream_t s) {
+cudaError_t launch_orders(const Plan& p, char* ws, unsigned which, cudaStream_t s) {
   // forward: q-tile pairs, cost = the non-empty tiles of both rows
   // (pair_info[.][3]); dK/dV: k-tile columns, dQ: q-tile rows, cost = their
   // non-empty tiles
-  int nT, maxc, stride = 1, G = 1;
-  const int32_t* counts;
-  int32_t* order;
-  if (which == ORDER_PAIRS) {
-    nT = p.nP; maxc = 2 * p.nK; stride = 4;
-    counts = reinterpret_cast<const int32_t*>(ws + p.L.pair_info) + 3;
-    order = reinterpret_cast<int32_t*>(ws + p.L.fwd_order);
-  } else if (which == ORDER_COLS) {
-    // dK/dV units belong to K/V heads: G query heads' columns each
-    nT = p.nK; maxc = p.G * p.nQ; G = p.G;
-    counts = reinterpret_cast<const int32_t*>(ws + p.L.col_count);
-    order = reinterpret_cast<int32_t*>(ws + p.L.bwd_order);
-  } else {
-    nT = p.nQ; maxc = p.nK;
-    counts = reinterpret_cast<const int32_t*>(ws + p.L.row_count);
-    order = reinterpret_cast<int32_t*>(ws + p.L.row_order);
+  OrderJobs J{};
+  size_t smem = 0;
+  int blocks = 0;
+  for (int which_one : {ORDER_PAIRS, ORDER_COLS, ORDER_ROWS}) {
+    if (!(which & (1u << which_one))) continue;
+    OrderJob& jb = J.job[J.n++];
+    jb.stride = 1;
+    jb.G = 1;
+    if (which_one == ORDER_PAIRS) {
+      jb.nT = p.nP; jb.maxc = 2 * p.nK; jb.stride = 4;
+      jb.counts = reinterpret_cast<const int32_t*>(ws + p.L.pair_info) + 3;
+      jb.order = reinterpret_cast<int32_t*>(ws + p.L.fwd_order);
+    } else if (which_one == ORDER_COLS) {
+      // dK/dV units belong to K/V heads: G query heads' columns each
+      jb.nT = p.nK; jb.maxc = p.G * p.nQ; jb.G = p.G;
+      jb.counts = reinterpret_cast<const int32_t*>(ws + p.L.col_count);
+      jb.order = reinterpret_cast<int32_t*>(ws + p.L.bwd_order);
+    } else {
+      jb.nT = p.nQ; jb.maxc = p.nK;
+      jb.counts = reinterpret_cast<const int32_t*>(ws + p.L.row_count);
+      jb.order = reinterpret_cast<int32_t*>(ws + p.L.row_order);
+    }
+    jb.blocks = p.B * (p.H / jb.G);
+    blocks += jb.blocks;
+    const size_t need = static_cast<size_t>(jb.maxc + 1 + jb.nT) * 4;
+    if (need > smem) smem = need;
   }
-  const size_t smem = static_cast<size_t>(maxc + 1 + nT) * 4;
+  if (J.n == 0) return cudaSuccess;
   const size_t limit = 200 * 1024;
   if (smem > limit) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(limit));
   if (e != cudaSuccess) return e;
   prof_begin(K_ORDER, s);
-  order_kernel<<<p.B * (p.H / G), 256, smem, s>>>(counts, stride, p.H, p.Hm, G, nT, maxc,
-                                                 order);
+  order_kernel<<<blocks, 256, smem, s>>>(J, p.H, p.Hm);
   prof_end(K_ORDER, s);
   return cudaGetLastError();
 }

@@ -65,7 +65,7 @@ extern "C" fm_status fm_fwd_static(const fm_desc* desc, const void* q, const voi
   if (launch_summary(p, lts, lte, uts, ute, ws, s) != cudaSuccess) return FM_ERR_CUDA;
   if (launch_classify(p, ws, 0, s) != cudaSuccess) return FM_ERR_CUDA;
   if (launch_tile_masks(p, lts, lte, uts, ute, ws, s) != cudaSuccess) return FM_ERR_CUDA;
-  if (launch_order(p, ws, ORDER_PAIRS, s) != cudaSuccess) return FM_ERR_CUDA;
+  if (launch_orders(p, ws, 1u << ORDER_PAIRS, s) != cudaSuccess) return FM_ERR_CUDA;
   TensorArgs t{};
   t.q = q; t.k = k; t.v = v; t.o_out = o; t.lse_out = lse;
   t.bounds[0] = lts; t.bounds[1] = lte; t.bounds[2] = uts; t.bounds[3] = ute;
