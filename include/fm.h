@@ -237,8 +237,9 @@ fm_status fm_localize(const int32_t* bounds, int B, int Hm, int Skv,
  * reading here is per-tile scaling:
  *
  * fm_quantize_fp8: for each (batch, head) and 128-row tile of Q, K and V, the
- * scale s = amax / 448 in fp32 (1 for an all-zero tile) and the codes
- * e4m3(x / s) (fp32 division, round to nearest even, saturating at +-448).
+ * scale s = amax / 448 and its reciprocal r = 448 / amax in fp32 (both 1
+ * for an all-zero tile; one IEEE division each per tile) and the codes
+ * e4m3(x * r) (fp32 product, round to nearest even, saturating at +-448).
  * Inputs q, k, v: bf16 with desc's strides.  Outputs (caller-owned device
  * memory): q8 uint8 [B][Sq][H][128] and k8 uint8 [B][Skv][Hkv][128] (BSHD,
  * contiguous); v8t uint8 [B][Hkv][128][nK*128], V transposed per head with the

@@ -1,9 +1,10 @@
 // Per-tile e4m3 quantisation of Q, K and V for the FP8 forward.
 //
 // One CTA per (batch, head, 128-row tile) of one tensor: the tile's largest
-// magnitude amax (block reduction), scale s = amax / 448 in fp32 (1 for an
-// all-zero tile), codes e4m3(x / s) with an IEEE fp32 division and the
-// saturating round-to-nearest-even conversion.  Q and K codes keep the BSHD
+// magnitude amax (block reduction), scale s = amax / 448 and its reciprocal
+// r = 448 / amax in fp32 (IEEE divisions, once per tile; both 1 for an
+// all-zero tile), codes e4m3(x * r) with an fp32 product and the saturating
+// round-to-nearest-even conversion.  Q and K codes keep the BSHD
 // layout (one byte per element); V codes are written transposed per head,
 // [b][h][d][key] over a key axis padded to whole tiles (padding = 0), so that
 // V^T tiles are K-major operands of the P V product.  V also records, per
@@ -31,33 +32,39 @@ struct QuantArgs {
 };
 
 template <bool TRANSPOSE>
-__global__ void __launch_bounds__(256) quant_kernel(const __grid_constant__ QuantArgs A) {
+__global__ void __launch_bounds__(256, TRANSPOSE ? 3 : 4) quant_kernel(const __grid_constant__ QuantArgs A) {
   __shared__ float red[8];
-  __shared__ __align__(16) uint8_t tr[TRANSPOSE ? kQuantD * 128 : 16];  // [c][row]
+  // transposed: [c][row] with the 8-byte slots of row group g at slot
+  // g xor (c / 8), so that the stores of a warp hit distinct banks
+  __shared__ __align__(16) uint8_t tr[TRANSPOSE ? kQuantD * 128 : 16];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int bid = blockIdx.x;
   const int t = bid % A.nT, bh = bid / A.nT, b = bh / A.H, h = bh - b * A.H;
   const int r0 = t * 128;
   const int rows = min(128, A.S - r0);
-  // thread: row (tid / 16) + 16 i, 8-column chunk (tid % 16): 8 rows x 8 values
-  const int ch = tid & 15, rb = tid >> 4;
-  float v[8][8];
-  float amax = 0.f;
+  // thread: rows 8 g .. 8 g + 7 (g = tid / 16), 8-column chunk tid % 16:
+  // 8 rows x 8 values, kept as packed bf16 (unpacked once for the maximum
+  // and once for the conversion) so that four CTAs fit on an SM
+  const int ch = tid & 15, g = tid >> 4;
+  uint4 raw[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int r = rb + 16 * i;
-    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    const int r = 8 * g + i;
+    raw[i] = make_uint4(0u, 0u, 0u, 0u);
     if (r < rows)
-      u = *reinterpret_cast<const uint4*>(A.x + b * A.xs[0] + static_cast<int64_t>(r0 + r) * A.xs[1] +
-                                          h * A.xs[2] + ch * 8);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      v[i][2 * j] = __uint_as_float(w[j] << 16);
-      v[i][2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
-      amax = fmaxf(amax, fmaxf(fabsf(v[i][2 * j]), fabsf(v[i][2 * j + 1])));
-    }
+      raw[i] = *reinterpret_cast<const uint4*>(A.x + b * A.xs[0] + static_cast<int64_t>(r0 + r) * A.xs[1] +
+                                               h * A.xs[2] + ch * 8);
   }
+  // |x| of a bf16 is its bit pattern without the sign, and the order of the
+  // magnitudes is the order of those patterns
+  uint32_t mbits = 0u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mbits = max(mbits, max(w[j] & 0x7fffu, (w[j] >> 16) & 0x7fffu));
+  }
+  float amax = __uint_as_float(mbits << 16);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   if (lane == 0) red[warp] = amax;
@@ -66,36 +73,65 @@ __global__ void __launch_bounds__(256) quant_kernel(const __grid_constant__ Quan
 #pragma unroll
   for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
   const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  const float rs = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
   if (tid == 0) {
     A.scales[static_cast<size_t>(bh) * A.nT + t] = s;
     if (TRANSPOSE) atomicMax(reinterpret_cast<int*>(A.head_max) + bh, __float_as_int(s));
   }
+  uint32_t code[8][2];  // row i: columns 0-3, 4-7 of the chunk (byte k = column k mod 4)
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int r = rb + 16 * i;
-    const uint32_t lo = pack_e4m3x4(__fdiv_rn(v[i][0], s), __fdiv_rn(v[i][1], s),
-                                    __fdiv_rn(v[i][2], s), __fdiv_rn(v[i][3], s));
-    const uint32_t hi = pack_e4m3x4(__fdiv_rn(v[i][4], s), __fdiv_rn(v[i][5], s),
-                                    __fdiv_rn(v[i][6], s), __fdiv_rn(v[i][7], s));
+    const int r = 8 * g + i;
+    const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[2 * j] = __uint_as_float(w[j] << 16);
+      v[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+    const uint32_t lo = pack_e4m3x4(v[0] * rs, v[1] * rs, v[2] * rs, v[3] * rs);
+    const uint32_t hi = pack_e4m3x4(v[4] * rs, v[5] * rs, v[6] * rs, v[7] * rs);
     if (!TRANSPOSE) {
       if (r < rows)
         *reinterpret_cast<uint2*>(A.out + b * A.os[0] + static_cast<int64_t>(r0 + r) * A.os[1] +
                                   h * A.os[2] + ch * 8) = make_uint2(lo, hi);
-    } else {
-      // column c = ch * 8 + k of row r goes to tr[c][r] (rows past S hold 0)
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        tr[(ch * 8 + k) * 128 + r] = static_cast<uint8_t>(((k < 4 ? lo : hi) >> (8 * (k & 3))) & 0xffu);
     }
+    code[i][0] = lo;
+    code[i][1] = hi;
   }
   if (TRANSPOSE) {
+    // each 4 x 4 byte block (4 rows x 4 columns) transposed with byte
+    // permutes, so that a column's 8 bytes of rows 8 g .. 8 g + 7 form one
+    // 8-byte store into tile row c (rows past S hold 0)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {        // columns 0-3 / 4-7 of the chunk
+      uint32_t colw[2][4];                  // [row half][column]: 4 row bytes
+#pragma unroll
+      for (int rh = 0; rh < 2; ++rh) {
+        const uint32_t w0 = code[4 * rh][hf], w1 = code[4 * rh + 1][hf], w2 = code[4 * rh + 2][hf],
+                       w3 = code[4 * rh + 3][hf];
+        const uint32_t t0 = __byte_perm(w0, w1, 0x5140), t1 = __byte_perm(w2, w3, 0x5140);
+        const uint32_t t2 = __byte_perm(w0, w1, 0x7362), t3 = __byte_perm(w2, w3, 0x7362);
+        colw[rh][0] = __byte_perm(t0, t1, 0x5410);
+        colw[rh][1] = __byte_perm(t0, t1, 0x7632);
+        colw[rh][2] = __byte_perm(t2, t3, 0x5410);
+        colw[rh][3] = __byte_perm(t2, t3, 0x7632);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int c = ch * 8 + 4 * hf + k;
+        *reinterpret_cast<uint2*>(tr + c * 128 + ((g ^ (c >> 3)) << 3)) = make_uint2(colw[0][k], colw[1][k]);
+      }
+    }
     __syncthreads();
-    // d rows of 128 keys: 16-byte pieces, 8 per row
+    // d rows of 128 keys: 16-byte pieces, 8 per row; piece p of tile row c is
+    // the slot pair p xor (c / 16), its halves swapped when c / 8 is odd
     uint8_t* dst = A.out + (static_cast<size_t>(bh) * kQuantD) * A.S_pad + r0;
     for (int i = tid; i < kQuantD * 8; i += 256) {
-      const int c = i >> 3, piece = i & 7;
-      *reinterpret_cast<uint4*>(dst + static_cast<size_t>(c) * A.S_pad + piece * 16) =
-          *reinterpret_cast<const uint4*>(tr + c * 128 + piece * 16);
+      const int c = i >> 3, piece = i & 7, chc = c >> 3;
+      uint4 v = *reinterpret_cast<const uint4*>(tr + c * 128 + ((piece ^ (chc >> 1)) << 4));
+      if (chc & 1) v = make_uint4(v.z, v.w, v.x, v.y);
+      *reinterpret_cast<uint4*>(dst + static_cast<size_t>(c) * A.S_pad + piece * 16) = v;
     }
   }
 }

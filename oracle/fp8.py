@@ -10,8 +10,11 @@ The reading written here (and in the library's header):
   finite value is 448), subnormals (m/8) 2^-6.  Conversion rounds to the
   nearest value, ties to even, and saturates at +-448.
 * Per-tile quantisation of a [rows][d] head slice: tile t = rows
-  [128 t, 128 t + 128); scale s_t = amax_t / 448 in float32 (1 when the tile
-  is all zero), code = e4m3(x / s_t) with the division in float32.
+  [128 t, 128 t + 128); scale s_t = amax_t / 448 and its reciprocal
+  r_t = 448 / amax_t, each one float32 division (both 1 when the tile is all
+  zero); code = e4m3(x * r_t) with the product in float32.  (The page gives
+  no formula; a reciprocal computed once per tile and multiplied in is the
+  plainest reading that costs one division per tile, not one per element.)
 * Attention on codes and scales, one query row i at a time, over the k-tiles
   in ascending order (a streaming pass, as FlashAttention-2 computes it:
   FlashAttention-2 page, «Блочная обработка сохраняет общую нормализацию»):
@@ -63,8 +66,9 @@ def quantize_tiles(x) -> tuple[np.ndarray, np.ndarray]:
         blk = x32[t * TILE:(t + 1) * TILE]
         amax = np.float32(np.abs(blk).max()) if blk.size else np.float32(0)
         s = np.float32(amax / np.float32(E4M3_MAX)) if amax > 0 else np.float32(1)
+        r = np.float32(np.float32(E4M3_MAX) / amax) if amax > 0 else np.float32(1)
         scales[t] = s
-        codes[t * TILE:(t + 1) * TILE] = e4m3((blk / s).astype(np.float32))
+        codes[t * TILE:(t + 1) * TILE] = e4m3((blk * r).astype(np.float32))
     return codes, scales
 
 

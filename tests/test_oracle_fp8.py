@@ -48,7 +48,8 @@ def test_quantize_tiles_properties():
         assert s[ti] == np.float32(np.abs(blk).max() / np.float32(448))
         # the tile's largest magnitude maps to 448 up to the float32 division
         assert abs(np.abs(codes[lo:hi]).max() - 448) <= 448 * 2 ** -3
-        # every code is x / s rounded: within half a step of e4m3 at its size
+        # every code is x * (448 / amax) rounded: within half a step of e4m3
+        # at its size of x / s
         err = np.abs(codes[lo:hi] - blk / s[ti])
         assert np.all(err <= np.maximum(np.abs(blk / s[ti]) * 2 ** -4, 2 ** -10))
 
