@@ -18,7 +18,7 @@ KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "
         "clocks"}
 
 
-def _report(world=1, ms=2.0, e2e_ms=7.0):
+def _report(world=1, ms=2.0, e2e_ms=7.0, prof_ms=2.04, graph_ms=1.98):
     args = types.SimpleNamespace(steps=10, warmup=3, no_e2e=False, no_cpu_baseline=True)
     W = dict(bench.WORKLOAD)
     prof = {"fwd_kernel": (6.0, 10), "bwd_kv_kernel": (8.0, 10), "bwd_dq_kernel": (5.0, 10),
@@ -27,7 +27,7 @@ def _report(world=1, ms=2.0, e2e_ms=7.0):
     with contextlib.redirect_stdout(buf):
         bench.report(args, W, world, 0, ms, prof, 3.0e11, 7.5e11, 123456, e2e_ms, 1000, 2000,
                      {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3},
-                     exp2_rate=1.0e13)
+                     exp2_rate=1.0e13, prof_ms=prof_ms, graph_ms=graph_ms)
     return json.loads(buf.getvalue().strip().splitlines()[-1])
 
 
@@ -36,6 +36,11 @@ def test_device_arm_line():
     assert KEYS <= d.keys()
     assert d["value"] == pytest.approx(1.05e12 / 2e-3 / 1e12, rel=1e-3)
     assert d["ms_per_step"] == pytest.approx(2.0)
+    # the headline is the pass without per-kernel events; the per-kernel
+    # pass and the CUDA-graph replay are reported beside it, not in `value`
+    assert d["profiled_ms_per_step"] == pytest.approx(2.04)
+    assert d["graph_ms_per_step"] == pytest.approx(1.98)
+    assert _report(prof_ms=None, graph_ms=None)["graph_ms_per_step"] is None
     assert d["higher_is_better"] is True and d["scaling"] == "weak" and d["n_gpus"] == 1
     r = d["roofline"]
     assert {"bound", "achieved", "peak", "unit", "frac", "traffic"} <= r.keys()
