@@ -69,6 +69,49 @@ def test_planned_step_equals_separate_calls(name):
 
 
 @pytest.mark.parametrize("d", [64, 128])
+def test_step_captured_as_cuda_graph(d):
+    """A training step (analysis on a step workspace, planned forward and
+    backward) captured once as a CUDA graph replays to bit-identical outputs,
+    with new inputs copied into the captured buffers between replays."""
+    B, S, H = 2, 1000, 4
+    scale = d ** -0.5
+    q, k, v, do = qkv_do(B, S, S, H, d, seed=21, device="cuda")
+    bounds = mask_bounds("causal_document", B, S, device="cuda")
+    desc = fm.make_desc(q, k, v, q)
+    ws = fm.workspace(desc, fm.WS_STEP)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, S, dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def step(st):
+        fm.plan(q, k, bounds, ws=ws, for_bwd=fm.WS_STEP, stream=st)
+        fm.forward(q, k, v, bounds, scale, o=o, lse=lse, ws=ws, stream=st, planned=True)
+        fm.backward(q, k, v, o, lse, do, bounds, scale, dq=dq, dk=dk, dv=dv, ws=ws, stream=st,
+                    planned=True)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step(side)                      # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        step(side)
+    for seed in (22, 23):
+        q2, k2, v2, do2 = qkv_do(B, S, S, H, d, seed=seed, device="cuda")
+        for dst, src in ((q, q2), (k, k2), (v, v2), (do, do2)):
+            dst.copy_(src)
+        for t in (o, dq, dk, dv):
+            t.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert fm.device_status(ws) == 0
+        ref = _run(q, k, v, do, bounds, scale)
+        for a, b_ in zip(ref, (o, lse, dq, dk, dv)):
+            assert torch.equal(a, b_)
+
+
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("S", [1, 77, 128, 300, 1000])
 @pytest.mark.parametrize("name", ["full", "causal", "causal_document", "qk_sparse",
                                   "share_question", "random_eviction", "global_sliding"])
