@@ -262,6 +262,18 @@ def run_ours(args):
         stream.wait_stream(side)
         graph.replay()
         graph_ms = timed(graph.replay, args.steps)
+    # the mask analysis alone (latency-bound kernels of a few MB): captured
+    # once as a CUDA graph and replayed 100 times
+    plan_ms = None
+    if not args.no_graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        pgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(pgraph, stream=side):
+            fm.plan(q, k, bounds, ws=ws, for_bwd=fm.WS_STEP, stream=side)
+        stream.wait_stream(side)
+        pgraph.replay()
+        plan_ms = timed(pgraph.replay, 100)
     if fm.device_status(ws) != 0:
         raise RuntimeError("device status not OK after the timed steps")
 
@@ -281,7 +293,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2d, d2h, clk,
-           per_mask, exp2_rate, fp8_points, prof_ms=prof_ms, graph_ms=graph_ms)
+           per_mask, exp2_rate, fp8_points, prof_ms=prof_ms, graph_ms=graph_ms, plan_ms=plan_ms)
     if world > 1:
         dist.destroy_process_group()
 
@@ -580,7 +592,8 @@ def exp2_ceiling(rate, d):
 
 
 def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2d, d2h, clk,
-           per_mask=None, exp2_rate=None, fp8_points=None, prof_ms=None, graph_ms=None):
+           per_mask=None, exp2_rate=None, fp8_points=None, prof_ms=None, graph_ms=None,
+           plan_ms=None):
     B, H, S, d = W["B"], W["H"], W["S"], W["d"]
     flop_step = flop_fwd + flop_bwd
     if rank == 0:
@@ -611,10 +624,12 @@ def report(args, W, world, rank, ms, prof, flop_fwd, flop_bwd, n_vis, e2e_ms, h2
             "ms_per_step": round(ms, 4),
             "profiled_ms_per_step": None if prof_ms is None else round(prof_ms, 4),
             "graph_ms_per_step": None if graph_ms is None else round(graph_ms, 4),
+            "analysis_graph_ms": None if plan_ms is None else round(plan_ms, 4),
             "timing": "ms_per_step: the step through the public API, no per-kernel events; "
                       "profiled_ms_per_step: the same K steps with per-kernel CUDA events "
                       "(kernel_ms_per_step, roofline); graph_ms_per_step: the step captured "
-                      "once as a CUDA graph and replayed K times",
+                      "once as a CUDA graph and replayed K times; analysis_graph_ms: the "
+                      "step's mask analysis (fm_plan) alone, as a CUDA graph replayed 100 times",
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
