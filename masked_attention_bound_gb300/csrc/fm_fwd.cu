@@ -32,12 +32,13 @@
 // FP8 variant (F8 = true, d = 128): Q and K are e4m3 codes with one scale per
 // 128-row tile, V is e4m3 transposed per head ([d][key], a K-major operand)
 // with one scale per 128-key tile and the head's largest tile scale.  Both
-// products are kind::f8f6f4 MMAs on K-major shared-memory operands (32
-// elements per MMA).  The softmax multiplies each S tile by scale * sq * sk,
-// keeps its reference exponent integral (so rescales are exact powers of two),
-// folds the V tile's scale ratio sv / sv_head into the exponent of P, rounds P
-// to e4m3 into a per-slot shared-memory tile, and the epilogue multiplies O by
-// sv_head / l.
+// products are kind::f8f6f4 MMAs (32 elements of k per MMA): S on K-major
+// shared-memory operands, P V with P from tensor memory.  The softmax
+// multiplies each S tile by scale * sq * sk, keeps its reference exponent
+// integral (so rescales are exact powers of two), folds the V tile's scale
+// ratio sv / sv_head into P, rounds P to e4m3 over the first 32 columns of
+// the slot's S region (four values per column), and the epilogue multiplies
+// O by sv_head / l.
 #include <cuda_bf16.h>
 
 #include "fm_internal.h"
@@ -56,8 +57,7 @@ struct FwdCfg {
   static constexpr int OFF_Q = 0;                              // slots a, b
   static constexpr int OFF_K = OFF_Q + 2 * TILE;               // 2 stages
   static constexpr int OFF_V = OFF_K + 2 * TILE;               // 2 stages
-  static constexpr int OFF_P = OFF_V + 2 * TILE;               // F8: [slot] P, 128 x 128 e4m3
-  static constexpr int OFF_MSK = OFF_P + (F8 ? 2 * 128 * 128 : 0);  // [stage][slot] bit masks
+  static constexpr int OFF_MSK = OFF_V + 2 * TILE;             // [stage][slot] bit masks
   static constexpr int OFF_DESC = OFF_MSK + 4 * kMaskBytes;    // [stage] entry word
   static constexpr int OFF_RING = OFF_DESC + 16;               // [UNIT_RING] claimed units
   static constexpr int OFF_BAR = OFF_RING + 16;
@@ -497,10 +497,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::THREADS, 1)
       // constant offset): Q and K K-major, V MN-major
       const uint32_t dQ = sdesc_lo(sQ, 16);
       const uint32_t dK0 = sdesc_lo(sbase + C::OFF_K, 16);
-      // V: MN-major [key][d] tiles, or (F8) K-major V^T [d][key] tiles; P (F8)
-      // the slot's K-major [q][key] tile
+      // V: MN-major [key][d] tiles, or (F8) K-major V^T [d][key] tiles
       const uint32_t dV0 = F8 ? sdesc_lo(sbase + C::OFF_V, 16) : sdesc_lo(sbase + C::OFF_V, 128 * 128);
-      const uint32_t dP8 = sdesc_lo(sbase + C::OFF_P + s * 128 * 128, 16);
       const uint32_t tS = tbase + 128 * s, tO = tbase + 256 + 128 * s;
       uint32_t qn = 0, np = 0, un = 0;
       // entry word of entry e, once its K tile (and bits) have landed
@@ -544,9 +542,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::THREADS, 1)
         const uint32_t dV = dV0 + st * (C::TILE >> 4);
         if constexpr (F8) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // 128 keys, 32 per MMA
-            mma_ss_f8(tO, sdesc_at(dP8, kk * 32), sdesc_at(dV, kk * 32), idPV,
-                      (!first || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)  // 128 keys, 32 per MMA (8 columns of P)
+            mma_ts_f8(tO, tS + kk * 8, sdesc_at(dV, kk * 32), idPV, (!first || kk > 0) ? 1u : 0u);
         } else {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
@@ -698,8 +695,6 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::THREADS, 1)
         // two columns per packed FMA and per packed add
         const uint64_t sc2 = splat2(ct), nm2 = splat2(-m_ref);
         float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-        // F8: row r of the slot's P tile (128 bytes, 128-byte swizzle)
-        const uint32_t prow = sbase + C::OFF_P + slot * 128 * 128 + r * 128;
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           uint32_t pk[16];
@@ -718,14 +713,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::THREADS, 1)
               pk[x] = pack_bf16(p0, p1);
             }
           }
-          if constexpr (F8) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-              st_shared_v4(prow + (static_cast<uint32_t>(c4 * 2 + k) ^ static_cast<uint32_t>(r & 7)) * 16,
-                           pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-          } else {
-            tmem_st16(tS + c4 * 16, pk);
-          }
+          if constexpr (F8) tmem_st8(tS + c4 * 8, pk);  // 32 keys, four per column
+          else tmem_st16(tS + c4 * 16, pk);
         }
         const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
         // rescale O by alpha (after P: the S registers are free by now).  O
@@ -743,7 +732,6 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::THREADS, 1)
         }
         l += sum;
         tmem_wait_st();
-        if constexpr (F8) fence_proxy_async_smem();  // P (smem) is read by the tensor cores
         tc_fence_before();
         // (a test of the wait limit withholds the first P-ready arrival of
         // slot a: the slot's MMA thread then gives up on it and the launch
