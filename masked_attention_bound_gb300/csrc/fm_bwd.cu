@@ -184,7 +184,9 @@ constexpr int A_READERS = 10;
 // run, so the tensor pipe need not wait for them.  dS^T(t) goes into the
 // one dS buffer only after dP^T(t) has completed, which implies dK(t-1),
 // issued before it by the same thread, has completed too.
-template <int D>
+// WIDE: every dK and dV row starts on a 32-byte boundary (32-byte epilogue
+// stores at d = 128)
+template <int D, bool WIDE>
 __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     bwd_kv_kernel(const __grid_constant__ BwdParams P, const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -534,19 +536,42 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
           __syncwarp();
           __nv_bfloat16* base = m ? P.out0 : P.out1;
           const int64_t* st3 = m ? P.s0 : P.s1;
-          const int jj = lane & 7;
+          if constexpr (WIDE) {
+            // 32 bytes per lane: four lanes per row, eight rows per store
+            const int jj = lane & 3;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rl = i * 4 + (lane >> 3);  // row within the warp's 32 keys
-            const uint32_t chunk = static_cast<uint32_t>(jj) ^ static_cast<uint32_t>(rl & 7);
-            uint4 val;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                         : "r"(patch + rl * 128 + chunk * 16));
-            const int kr = key0 + rl;
-            if (kr < P.Skv)
-              *reinterpret_cast<uint4*>(base + b * st3[0] + static_cast<int64_t>(kr) * st3[1] +
-                                        h * st3[2] + half * (D / 2) + jj * 8) = val;
+            for (int i = 0; i < 4; ++i) {
+              const int rl = i * 8 + (lane >> 2);  // row within the warp's 32 keys
+              const uint32_t c0 = static_cast<uint32_t>(2 * jj) ^ static_cast<uint32_t>(rl & 7);
+              const uint32_t c1 = static_cast<uint32_t>(2 * jj + 1) ^ static_cast<uint32_t>(rl & 7);
+              uint32_t w[8];
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                           : "r"(patch + rl * 128 + c0 * 16));
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                           : "r"(patch + rl * 128 + c1 * 16));
+              const int kr = key0 + rl;
+              if (kr < P.Skv)
+                st_global_v8(base + b * st3[0] + static_cast<int64_t>(kr) * st3[1] + h * st3[2] +
+                                 half * (D / 2) + jj * 16,
+                             w);
+            }
+          } else {
+            const int jj = lane & 7;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rl = i * 4 + (lane >> 3);  // row within the warp's 32 keys
+              const uint32_t chunk = static_cast<uint32_t>(jj) ^ static_cast<uint32_t>(rl & 7);
+              uint4 val;
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                           : "r"(patch + rl * 128 + chunk * 16));
+              const int kr = key0 + rl;
+              if (kr < P.Skv)
+                *reinterpret_cast<uint4*>(base + b * st3[0] + static_cast<int64_t>(kr) * st3[1] +
+                                          h * st3[2] + half * (D / 2) + jj * 8) = val;
+            }
           }
           __syncwarp();
         }
@@ -788,7 +813,10 @@ constexpr int Q_READERS = 10;
 // barrier per S region: dP(t+1) is issued before the wait for dS(t), and a
 // region's barrier cannot run two phases ahead of that wait (dS(t+2) needs
 // S(t+2), issued only after dQ(t)).
-template <int D>
+// WIDE: every dQ row starts on a 32-byte boundary (32-byte epilogue stores;
+// a template parameter because a run-time choice between the two store forms
+// made the rest of the kernel slower)
+template <int D, bool WIDE>
 __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ BwdParams P, const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -1205,14 +1233,27 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 4 * NC; ++i)
           pk[i] = pack_bf16(__uint_as_float(rq[2 * i]) * sc, __uint_as_float(rq[2 * i + 1]) * sc);
-        transpose_chunks<NC>(pk);
-        const int row0 = prow - lane + (lane & ~(NC - 1));  // q row of this lane group's first row
-        __nv_bfloat16* base = P.out0 + pb * P.s0[0] + ph * P.s0[2] + half * (D / 2) + (lane & (NC - 1)) * 8;
+        __nv_bfloat16* base = P.out0 + pb * P.s0[0] + ph * P.s0[2] + half * (D / 2);
+        if constexpr (WIDE) {
+          // 32-byte chunks where the layout allows: half the exchanges and
+          // half the store instructions
+          constexpr int N2 = NC / 2;
+          transpose_chunks<N2, 8>(pk);
+          const int row0 = prow - lane + (lane & ~(N2 - 1));  // q row of this lane group's first row
+          base += (lane & (N2 - 1)) * 16;
 #pragma unroll
-        for (int i = 0; i < NC; ++i)
-          if (row0 + i < P.Sq)
-            *reinterpret_cast<uint4*>(base + static_cast<int64_t>(row0 + i) * P.s0[1]) =
-                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          for (int i = 0; i < N2; ++i)
+            if (row0 + i < P.Sq) st_global_v8(base + static_cast<int64_t>(row0 + i) * P.s0[1], pk + 8 * i);
+        } else {
+          transpose_chunks<NC>(pk);
+          const int row0 = prow - lane + (lane & ~(NC - 1));  // q row of this lane group's first row
+          base += (lane & (NC - 1)) * 8;
+#pragma unroll
+          for (int i = 0; i < NC; ++i)
+            if (row0 + i < P.Sq)
+              *reinterpret_cast<uint4*>(base + static_cast<int64_t>(row0 + i) * P.s0[1]) =
+                  make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
       }
       pending = false;
       return true;
@@ -1374,7 +1415,9 @@ static fm_status launch_bwd_d(const Plan& p, const fm_desc& desc, const TensorAr
     }
     A.withhold = th.withhold;
     using C = KvCfg<D>;
-    auto kern = bwd_kv_kernel<D>;
+    auto kern = rows_32b_aligned(t.dk, desc.k_stride) && rows_32b_aligned(t.dv, desc.v_stride)
+                    ? bwd_kv_kernel<D, true>
+                    : bwd_kv_kernel<D, false>;
     if ((st = prepare(kern, C::SMEM, C::MIN_LAUNCH_REGS)) != FM_OK) return st;
     const int grid = A.n_units < num_sms() ? A.n_units : num_sms();
     prof_begin(K_BWD, s);
@@ -1396,7 +1439,7 @@ static fm_status launch_bwd_d(const Plan& p, const fm_desc& desc, const TensorAr
     for (int i = 0; i < 3; ++i) Q.s0[i] = desc.q_stride[i];
     Q.withhold = 0;
     using C = DqCfg<D>;
-    auto kern = bwd_dq_kernel<D>;
+    auto kern = rows_32b_aligned(t.dq, desc.q_stride) ? bwd_dq_kernel<D, true> : bwd_dq_kernel<D, false>;
     if ((st = prepare(kern, C::SMEM, C::MIN_LAUNCH_REGS)) != FM_OK) return st;
     const int grid = Q.n_units < num_sms() ? Q.n_units : num_sms();
     prof_begin(K_BWD_DQ, s);

@@ -17,6 +17,16 @@ enum : int { CLS_EMPTY = 0, CLS_PARTIAL = 1, CLS_FULL = 2 };
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// A bf16 [B][S][H][d] tensor whose every row (and every 16-element piece of
+// one) starts on a 32-byte boundary: the base is 32-byte aligned and every
+// stride (in elements) is a multiple of 16.
+inline bool rows_32b_aligned(const void* base, const int64_t (&stride)[3]) {
+  if (reinterpret_cast<uintptr_t>(base) % 32 != 0) return false;
+  for (int i = 0; i < 3; ++i)
+    if (stride[i] % 16 != 0) return false;
+  return true;
+}
+
 struct Plan {
   int B, H, Hm, Sq, Skv, d, nQ, nK;
   int Hkv, G;    // K/V heads and query heads per K/V head (H = G * Hkv)

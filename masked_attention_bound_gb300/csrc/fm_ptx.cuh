@@ -404,16 +404,26 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-// Row-per-lane data (lane L holds NC 16-byte chunks of row L, chunk i in
-// c[4i .. 4i+3]) regrouped for coalesced stores: within each group of NC
-// lanes, an NC x NC transpose of the chunks in log2(NC) butterfly stages
-// (stage b swaps bit b of the lane and of the chunk index through one
-// exchange with lane ^ 2^b).  Afterwards lane NC*g + j holds in c[4i ..]
-// chunk j of row NC*g + i, so the i-th store of the warp writes NC rows of
-// NC contiguous chunks each, instead of 32 rows of 16 bytes.
-template <int NC>
-__device__ __forceinline__ void transpose_chunks(uint32_t (&c)[4 * NC]) {
-  static_assert(NC == 4 || NC == 8, "groups of 4 or 8 lanes");
+// One 32-byte global store (sm_100 and later; the address must be 32-byte
+// aligned).  A warp's 32 lanes writing to 32 different rows touch as many
+// cache lines per instruction as with 16-byte stores, so a row written in
+// 32-byte pieces costs half the instructions and line accesses.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+// Row-per-lane data (lane L holds NC chunks of W 32-bit words of row L, chunk
+// i in c[W*i .. W*i + W-1]) regrouped for coalesced stores: within each
+// group of NC lanes, an NC x NC transpose of the chunks in log2(NC)
+// butterfly stages (stage b swaps bit b of the lane and of the chunk index
+// through one exchange with lane ^ 2^b).  Afterwards lane NC*g + j holds in
+// c[W*i ..] chunk j of row NC*g + i, so the i-th store of the warp writes NC
+// rows of NC contiguous chunks each, instead of 32 rows of one chunk.
+template <int NC, int W = 4>
+__device__ __forceinline__ void transpose_chunks(uint32_t (&c)[W * NC]) {
+  static_assert(NC == 2 || NC == 4 || NC == 8, "groups of 2, 4 or 8 lanes");
   const int j = threadIdx.x & (NC - 1);
 #pragma unroll
   for (int b = 0; (1 << b) < NC; ++b) {
@@ -427,11 +437,11 @@ __device__ __forceinline__ void transpose_chunks(uint32_t (&c)[4 * NC]) {
       // a lane sends the chunk whose bit b differs from its own lane bit and
       // puts the partner's chunk in its place
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const uint32_t send = upper ? c[4 * lo + w] : c[4 * hi + w];
+      for (int w = 0; w < W; ++w) {
+        const uint32_t send = upper ? c[W * lo + w] : c[W * hi + w];
         const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
-        if (upper) c[4 * lo + w] = recv;
-        else c[4 * hi + w] = recv;
+        if (upper) c[W * lo + w] = recv;
+        else c[W * hi + w] = recv;
       }
     }
   }

@@ -166,6 +166,37 @@ def test_per_head_masks_strides_and_cross_lengths():
     compare_bwd(q, k, v, do, bounds, 0.1, dq, dk, dv)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_outputs_in_16_byte_aligned_rows(d):
+    """Rows that start on 16-byte but not 32-byte boundaries (head stride
+    d + 8, for every tensor) take the kernels' 16-byte store paths for O, dQ,
+    dK and dV; the results equal, bit for bit, those of the contiguous
+    layout, which takes the 32-byte paths, and match the oracle."""
+    B, S, H = 1, 700, 2
+    q, k, v, do = qkv_do(B, S, S, H, d, seed=21, device="cuda")
+    bounds = mask_bounds("causal_document", B, S, device="cuda")
+    ref = _run(q, k, v, do, bounds, d ** -0.5)
+
+    def padded(t):
+        big = torch.zeros(B, S, H, d + 8, device="cuda", dtype=torch.bfloat16)
+        view = big[..., 8:]
+        view.copy_(t)
+        return view
+
+    qp, kp, vp, dop = padded(q), padded(k), padded(v), padded(do)
+    o = padded(torch.zeros_like(q))
+    o, lse = fm.forward(qp, kp, vp, bounds, d ** -0.5, o=o)
+    dq, dk, dv = (padded(torch.zeros_like(t)) for t in (q, k, v))
+    dq, dk, dv = fm.backward(qp, kp, vp, o, lse, dop, bounds, d ** -0.5, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    for t in (o, dq, dk, dv):
+        assert t.data_ptr() % 32 == 16 and t.stride(2) % 16 == 8
+    for got, want in zip((o, lse, dq, dk, dv), ref):
+        assert torch.equal(got, want)
+    compare_fwd(q, k, v, bounds, d ** -0.5, o, lse)
+    compare_bwd(q, k, v, do, bounds, d ** -0.5, dq, dk, dv)
+
+
 @pytest.mark.parametrize("name", SWEEP_4K.masks)
 def test_sweep_4k_sampled_heads(name):
     W = SWEEP_4K
