@@ -25,7 +25,10 @@
  *  - Q, K, V, O, dO, dQ, dK, dV are bf16 in BSHD layout: element (b, s, h, c)
  *    at  b*stride[0] + s*stride[1] + h*stride[2] + c  (elements; the head
  *    dimension is contiguous).  Base pointers must be 16-byte aligned and the
- *    three strides multiples of 8 elements (16 bytes).
+ *    three strides multiples of 8 elements (16 bytes).  Outputs (O, dQ, dK,
+ *    dV) whose base is 32-byte aligned and whose strides are multiples of 16
+ *    elements are written with 32-byte stores, which is faster; the results
+ *    are the same either way.
  *  - Bounds are int32 arrays of shape [B][Hm][Skv], contiguous.  Query head h
  *    reads mask head 0 if Hm == 1, else mask head h.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
