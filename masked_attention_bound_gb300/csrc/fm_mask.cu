@@ -224,18 +224,19 @@ __global__ void __launch_bounds__(kTile) tile_mask_kernel(
 // One warp per (bh, q-tile pair p): the union of the non-empty k-tiles of
 // q-tiles 2p and 2p+1 (the second absent when nQ is odd), ascending, each
 // entry (kj << 4) | (class_a << 2) | class_b, a non-empty ragged last k-tile
-// as PARTIAL; info = {entries, tiles of 2p, tiles of 2p+1, their sum}.
-__global__ void __launch_bounds__(256) classify_pairs_kernel(const uint8_t* __restrict__ table,
-                                                             int nBH, int nQ, int nK, int nP,
-                                                             int Skv, int4* pair_info,
-                                                             int32_t* pair_list) {
+// as PARTIAL; info = {entries, tiles of 2p, tiles of 2p+1, their sum}.  The
+// classes come from the block summary by the same rule as the table's, so
+// the pairs need not wait for the rows' pass.
+__device__ __forceinline__ void classify_pair(int w, const int32_t* __restrict__ summary, int nBH,
+                                              int nQ, int nK, int nP, int Sq, int Skv,
+                                              int4* pair_info, int32_t* pair_list) {
   const int lane = threadIdx.x & 31;
-  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (w >= nBH * nP) return;
   const int bh = w / nP, p = w - bh * nP;
-  const uint8_t* ta = table + (static_cast<size_t>(bh) * nQ + 2 * p) * nK;
+  const int32_t* sm = summary + static_cast<size_t>(bh) * nK * 8;
+  const int ra0 = 2 * p * kTile, ra1 = min(ra0 + kTile, Sq);
   const bool has_b = 2 * p + 1 < nQ;
-  const uint8_t* tb = ta + nK;
+  const int rb0 = ra0 + kTile, rb1 = min(rb0 + kTile, Sq);
   int32_t* lst = pair_list + static_cast<size_t>(w) * nK;
   const unsigned lt_mask = (1u << lane) - 1u;
   const bool ragged = (Skv & (kTile - 1)) != 0;
@@ -244,8 +245,10 @@ __global__ void __launch_bounds__(256) classify_pairs_kernel(const uint8_t* __re
     const int kj = base + lane;
     int ca = CLS_EMPTY, cb = CLS_EMPTY;
     if (kj < nK) {
-      ca = ta[kj];
-      cb = has_b ? tb[kj] : CLS_EMPTY;
+      int s[8];
+      load_summary(sm + kj * 8, s);
+      ca = classify(s, ra0, ra1);
+      cb = has_b ? classify(s, rb0, rb1) : CLS_EMPTY;
       if (ragged && kj == nK - 1) {
         if (ca != CLS_EMPTY) ca = CLS_PARTIAL;
         if (cb != CLS_EMPTY) cb = CLS_PARTIAL;
@@ -286,21 +289,25 @@ __device__ __forceinline__ void classify_col(int w, const int32_t* __restrict__ 
   if (lane == 0) col_count[w] = cnt;
 }
 
-// Rows and columns in one launch (both read only the block summary): blocks
-// [0, row_blocks) classify q-tile rows, the rest k-tile columns (none when
-// col_list is null).  Eight warps per block, one row or column each.
-__global__ void __launch_bounds__(256) classify_rows_cols_kernel(
-    const int32_t* __restrict__ summary, int nBH, int nQ, int nK, int Sq, int Skv,
+// Rows, columns and the forward's pairs in one launch (all read only the
+// block summary): blocks [0, row_blocks) classify q-tile rows, the next
+// col_blocks k-tile columns, the rest q-tile pairs.  Eight warps per block,
+// one row, column or pair each.
+__global__ void __launch_bounds__(256) classify_kernel(
+    const int32_t* __restrict__ summary, int nBH, int nQ, int nK, int nP, int Sq, int Skv,
     uint8_t* table, int32_t* row_count, int32_t* row_list, int32_t* row_mask,
-    unsigned long long* slot_counter, int mask_cap, int row_blocks, int32_t* col_count,
-    int32_t* col_list) {
+    unsigned long long* slot_counter, int mask_cap, int row_blocks, int col_blocks,
+    int32_t* col_count, int32_t* col_list, int4* pair_info, int32_t* pair_list) {
   const int wib = threadIdx.x >> 5;
-  if (static_cast<int>(blockIdx.x) < row_blocks)
-    classify_row(blockIdx.x * 8 + wib, summary, nBH, nQ, nK, Sq, Skv, table, row_count, row_list,
+  const int blk = static_cast<int>(blockIdx.x);
+  if (blk < row_blocks)
+    classify_row(blk * 8 + wib, summary, nBH, nQ, nK, Sq, Skv, table, row_count, row_list,
                  row_mask, slot_counter, mask_cap);
+  else if (blk < row_blocks + col_blocks)
+    classify_col((blk - row_blocks) * 8 + wib, summary, nBH, nQ, nK, Sq, col_count, col_list);
   else
-    classify_col((blockIdx.x - row_blocks) * 8 + wib, summary, nBH, nQ, nK, Sq, col_count,
-                 col_list);
+    classify_pair((blk - row_blocks - col_blocks) * 8 + wib, summary, nBH, nQ, nK, nP, Sq, Skv,
+                  pair_info, pair_list);
 }
 
 // ------------------------------------------------------------------ order
@@ -477,22 +484,19 @@ cudaError_t launch_classify(const Plan& p, char* ws, int mode, cudaStream_t s) {
   const int nBH = p.B * p.Hm;
   const int32_t* summ = reinterpret_cast<const int32_t*>(ws + p.L.summary);
   uint8_t* table = reinterpret_cast<uint8_t*>(ws + p.L.table);
-  prof_begin(K_CLASSIFY, s);
-  // q-tile rows (with their mask slots: the forward's pairs are built from
-  // them, and the dQ pass walks them) and, for the backward, k-tile columns
+  // q-tile rows (with their mask slots: the dQ pass walks them and the
+  // forward's tile masks are filed by them), for the backward k-tile
+  // columns, for the forward q-tile pairs
   const int row_blocks = ceil_div(nBH * p.nQ, 8);
   const int col_blocks = mode != FM_WS_FWD ? ceil_div(nBH * p.nK, 8) : 0;
-  classify_rows_cols_kernel<<<row_blocks + col_blocks, 256, 0, s>>>(
-      summ, nBH, p.nQ, p.nK, p.Sq, p.Skv, table, reinterpret_cast<int32_t*>(ws + p.L.row_count),
+  const int pair_blocks = mode != FM_WS_BWD ? ceil_div(nBH * p.nP, 8) : 0;
+  prof_begin(K_CLASSIFY, s);
+  classify_kernel<<<row_blocks + col_blocks + pair_blocks, 256, 0, s>>>(
+      summ, nBH, p.nQ, p.nK, p.nP, p.Sq, p.Skv, table, reinterpret_cast<int32_t*>(ws + p.L.row_count),
       reinterpret_cast<int32_t*>(ws + p.L.row_list), reinterpret_cast<int32_t*>(ws + p.L.row_mask),
-      reinterpret_cast<unsigned long long*>(ws + p.L.status + 8), p.mask_cap, row_blocks,
-      reinterpret_cast<int32_t*>(ws + p.L.col_count), reinterpret_cast<int32_t*>(ws + p.L.col_list));
-  if (mode != FM_WS_BWD) {
-    const int pwarps = nBH * p.nP;
-    classify_pairs_kernel<<<ceil_div(pwarps, 8), 256, 0, s>>>(
-        table, nBH, p.nQ, p.nK, p.nP, p.Skv, reinterpret_cast<int4*>(ws + p.L.pair_info),
-        reinterpret_cast<int32_t*>(ws + p.L.pair_list));
-  }
+      reinterpret_cast<unsigned long long*>(ws + p.L.status + 8), p.mask_cap, row_blocks, col_blocks,
+      reinterpret_cast<int32_t*>(ws + p.L.col_count), reinterpret_cast<int32_t*>(ws + p.L.col_list),
+      reinterpret_cast<int4*>(ws + p.L.pair_info), reinterpret_cast<int32_t*>(ws + p.L.pair_list));
   prof_end(K_CLASSIFY, s);
   return cudaGetLastError();
 }
