@@ -834,10 +834,9 @@ static fm_status launch_fwd_d(const Plan& p, const fm_desc& desc, const TensorAr
     P.v_scale = f8->v_scale;
     P.v_head_scale = f8->v_head_scale;
   }
-  // 32-byte O stores where every row allows them (bf16 instances; the FP8
-  // one keeps 16-byte stores)
-  const bool wide = !F8 && rows_32b_aligned(t.o_out, desc.o_stride);
-  auto kern = wide ? fwd_kernel<D, F8, !F8> : fwd_kernel<D, F8, false>;
+  // 32-byte O stores where every row allows them
+  const bool wide = rows_32b_aligned(t.o_out, desc.o_stride);
+  auto kern = wide ? fwd_kernel<D, F8, true> : fwd_kernel<D, F8, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)
     return FM_ERR_CUDA;

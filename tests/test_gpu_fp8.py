@@ -115,3 +115,21 @@ def test_fp8_forward_32k_sampled_head():
     o, lse = fm.forward_fp8(f, bounds, W.scale)
     torch.cuda.synchronize()
     _check(q, k, v, bounds, W.scale, o, lse, [(0, 7)], rows=512)
+
+
+def test_forward_into_16_byte_aligned_rows():
+    """An O whose rows start on 16-byte but not 32-byte boundaries takes the
+    FP8 forward's 16-byte store instance; O and LSE equal, bit for bit, those
+    written into a contiguous O (the 32-byte instance)."""
+    B, S, H = 1, 700, 2
+    q, k, v = _inputs(B, S, S, H, H, seed=91)
+    bounds = mask_bounds("causal_document", B, S, device="cuda")
+    f = fm.quantize_fp8(q, k, v)
+    o_ref, lse_ref = fm.forward_fp8(f, bounds, 128 ** -0.5)
+    big = torch.zeros(B, S, H, 128 + 8, device="cuda", dtype=torch.bfloat16)
+    o = big[..., 8:]
+    o, lse = fm.forward_fp8(f, bounds, 128 ** -0.5, o=o)
+    torch.cuda.synchronize()
+    assert o.data_ptr() % 32 == 16 and o.stride(2) % 16 == 8
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+    assert torch.all(big[..., :8] == 0)
