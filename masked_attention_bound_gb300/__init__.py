@@ -7,7 +7,9 @@ missing, every call raises: there is no CPU or PyTorch fallback.
 
 Tensors: q/k/v/o/dO/dq/dk/dv are bf16 CUDA tensors in BSHD layout
 ([batch][seq][head][head_dim], head_dim contiguous, other strides multiples of
-8 elements).  ``bounds`` is an int32 CUDA tensor [4][B][Hm][Skv] holding
+8 elements; outputs whose strides are multiples of 16 elements, on 32-byte
+aligned storage such as torch's own allocations, take the kernels' faster
+32-byte stores).  ``bounds`` is an int32 CUDA tensor [4][B][Hm][Skv] holding
 LTS, LTE, UTS, UTE; key j is hidden from query row i iff LTS[j] <= i < LTE[j]
 or UTS[j] <= i < UTE[j].
 """
