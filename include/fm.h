@@ -316,8 +316,10 @@ fm_status fm_measure_exp2_rate(double* per_second, void* stream);
  * leaving its outputs undefined.  withhold_release makes one consumer
  * release never happen, so that a wait runs out on purpose: 0 none,
  * 1 fm_fwd (the softmax warps of the first q-tile of each unit pair skip
- * their first "P ready" arrival in each CTA), 2 fm_bwd (the compute warps
- * skip their first "P ready" arrival in each CTA).  For tests of the unwind
+ * their first "P ready" arrival in each CTA), 2 fm_bwd's dK/dV pass (the
+ * compute warps skip their first "P ready" arrival in each CTA), 3 fm_bwd's
+ * dQ pass (the compute warps skip their first "dS ready" arrival in each
+ * CTA).  For tests of the unwind
  * path only; calls that overlap a change of these settings see either value.
  * FM_ERR_INVALID for other withhold values. */
 fm_status fm_test_hooks(uint64_t wait_limit_ns, int withhold_release);

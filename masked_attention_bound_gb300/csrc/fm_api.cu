@@ -325,7 +325,7 @@ fm_status fm_device_status(const void* ws, void* stream) {
 }
 
 fm_status fm_test_hooks(uint64_t wait_limit_ns, int withhold_release) {
-  if (withhold_release < 0 || withhold_release > 2) return FM_ERR_INVALID;
+  if (withhold_release < 0 || withhold_release > 3) return FM_ERR_INVALID;
   g_hooks.wait_ns = wait_limit_ns ? wait_limit_ns : FM_WAIT_LIMIT_NS;
   g_hooks.withhold = withhold_release;
   return FM_OK;

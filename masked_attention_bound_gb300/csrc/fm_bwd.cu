@@ -126,7 +126,8 @@ struct BwdParams {
   int64_t s0[3], s1[3];       // strides of out0, out1
   int* status;
   uint64_t wait_ns;  // limit of every mbarrier wait
-  int withhold;      // test hook: 2 = the dK/dV compute warps withhold their first P-ready arrival
+  int withhold;      // test hook: 2 = the dK/dV compute warps withhold their first P-ready arrival,
+                     // 3 = the dQ compute warps their first dS-ready arrival
 };
 
 // Bits [a, b) of a 64-bit word, with a and b clipped to [0, 64].
@@ -1030,7 +1031,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         }
       }
       ++un;
-      if (!__all_sync(0xffffffffu, ok)) break;
+      // lane 0 alone may have cleared ok: make it the warp's, so that no
+      // lane stays in the unit loop after the others have left it
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
       const int mb = P.row_mask[row];
       int mo = 0;  // partial tiles of the row so far
       for (int t = 0; t < n; ++t, ++g) {
@@ -1057,7 +1061,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             }
           }
         }
-        if (!__all_sync(0xffffffffu, ok)) break;
+        ok = __all_sync(0xffffffffu, ok);  // the warp's, as above
+        if (!ok) break;
         if (is_partial(ent)) {
           // the bits buffer, once the compute warps have read the previous
           // partial tile's
@@ -1331,7 +1336,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
           tmem_wait_st();
         }
         tc_fence_before();
-        mbar_arrive_warp(bar(Q_DSREADY0 + x));
+        // (a test of the wait limit withholds the first dS-ready arrival: the
+        // dQ MMA thread then gives up on it and the launch unwinds with
+        // DEV_TIMEOUT)
+        if (!(P.withhold == 3 && gt == 0)) mbar_arrive_warp(bar(Q_DSREADY0 + x));
       }
       if (!ok) break;
       g += n;
@@ -1437,7 +1445,7 @@ static fm_status launch_bwd_d(const Plan& p, const fm_desc& desc, const TensorAr
     Q.masks = reinterpret_cast<const uint8_t*>(ws + p.L.masks);
     Q.out0 = static_cast<__nv_bfloat16*>(t.dq);
     for (int i = 0; i < 3; ++i) Q.s0[i] = desc.q_stride[i];
-    Q.withhold = 0;
+    Q.withhold = th.withhold;
     using C = DqCfg<D>;
     auto kern = rows_32b_aligned(t.dq, desc.q_stride) ? bwd_dq_kernel<D, true> : bwd_dq_kernel<D, false>;
     if ((st = prepare(kern, C::SMEM, C::MIN_LAUNCH_REGS)) != FM_OK) return st;

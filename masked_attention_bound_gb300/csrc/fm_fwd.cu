@@ -363,7 +363,10 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::THREADS, 1)
         }
         qn.set(s, qn.get(s) + 1);
       }
-      if (!__all_sync(0xffffffffu, ok)) break;
+      // lane 0 alone may have cleared ok: make it the warp's (the end marker
+      // below is written only if it is true, through warp-wide waits)
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
       const int mb0 = P.row_mask[u.row_a];
       const int mb1 = u.nb > 0 ? P.row_mask[u.row_a + 1] : -1;
       int mo0 = 0, mo1 = 0;      // partial tiles of each slot so far in this unit

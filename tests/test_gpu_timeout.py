@@ -4,7 +4,8 @@ Every mbarrier wait in the attention kernels is bounded; on expiry the launch
 records FM_ERR_TIMEOUT, drains what it issued, frees its tensor memory and
 returns.  Here a test hook shortens the limit to 20 ms and withholds one
 consumer release ("P ready", which the MMA thread waits for before the PV or
-dV product), so the wait runs out on purpose: no fault, no trap, no endless
+dV product, or "dS ready", before the dQ product), so the wait runs out on
+purpose: no fault, no trap, no endless
 loop.  The status word must say FM_ERR_TIMEOUT, and the next ordinary call on
 the same GPU must be clean and match the oracle.
 """
@@ -73,13 +74,16 @@ def test_forward_wait_timeout_is_reported_then_next_call_is_clean():
     compare_fwd(q, k, v, bounds, SCALE, o2, lse2)
 
 
-def test_backward_wait_timeout_is_reported_then_next_call_is_clean():
+# 2: the dK/dV pass's "P ready" (its MMA thread waits before dV); 3: the dQ
+# pass's "dS ready" (its dQ MMA thread waits before the dQ product)
+@pytest.mark.parametrize("withhold", [2, 3])
+def test_backward_wait_timeout_is_reported_then_next_call_is_clean(withhold):
     q, k, v, do, bounds = _inputs()
     o, lse = fm.forward(q, k, v, bounds, SCALE)
     desc = fm.make_desc(q, k, v, o)
     ws = fm.workspace(desc, True)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    assert fm.lib().fm_test_hooks(20_000_000, 2) == _abi.FM_OK
+    assert fm.lib().fm_test_hooks(20_000_000, withhold) == _abi.FM_OK
     try:
         t0 = time.time()
         assert _raw_bwd(q, k, v, o, lse, do, bounds, dq, dk, dv, ws) == _abi.FM_OK
@@ -96,6 +100,6 @@ def test_backward_wait_timeout_is_reported_then_next_call_is_clean():
 
 
 def test_hook_values_are_checked():
-    assert fm.lib().fm_test_hooks(0, 3) == _abi.FM_ERR_INVALID
+    assert fm.lib().fm_test_hooks(0, 4) == _abi.FM_ERR_INVALID
     assert fm.lib().fm_test_hooks(0, -1) == _abi.FM_ERR_INVALID
     assert fm.lib().fm_test_hooks(0, 0) == _abi.FM_OK
